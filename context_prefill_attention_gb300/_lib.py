@@ -1,0 +1,200 @@
+"""ctypes binding of libpcp (include/pcp.h). Argument marshalling only: every
+step of the path runs in the library. The binding refuses to work without the
+compiled library; there is no fallback of any kind."""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpcp.so")
+
+PCP_OK = 0
+PCP_ERR_ARG = -1
+PCP_ERR_RANGE = -2
+PCP_ERR_UNSUPPORTED = -3
+PCP_ERR_ALIGN = -4
+PCP_ERR_CUDA = -5
+PCP_ERR_TIMEOUT = -6
+PCP_ERR_WORKSPACE = -7
+
+PCP_SPLIT_CONTIGUOUS = 0
+PCP_SPLIT_DUAL_CHUNK = 1
+
+PCP_ATTN_SEPARATE_CONTEXT = 1
+PCP_ATTN_SPLIT_AT_ROW_START = 2
+
+ROW_FIELDS = ("req", "shard", "q_start", "q_len", "ctx_len", "kv_end", "causal_off", "is_decode")
+
+# every symbol include/pcp.h declares
+EXPORTS = ("pcp_build_row_plan", "pcp_mask_slots_for_shard", "pcp_kv_cache_write",
+           "pcp_attn_workspace_size", "pcp_attn_varlen", "pcp_lse_merge", "pcp_last_cuda_error",
+           "pcp_status_string")
+
+_lib = None
+
+
+class PcpError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        msg = "?"
+        if _lib is not None:
+            msg = _lib.pcp_status_string(code).decode()
+        extra = ""
+        if code == PCP_ERR_CUDA and _lib is not None:
+            extra = f" (cudaError {_lib.pcp_last_cuda_error()})"
+        super().__init__(f"{what}: {msg} [{code}]{extra}")
+        self.code = code
+
+
+def load(path: Optional[str] = None):
+    """Load libpcp.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with context_prefill_attention_gb300.build.build() "
+                           "(nvcc, sm_103a); there is no fallback path")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    lib.pcp_build_row_plan.argtypes = [i32, P, P, P, i32, i32, i32, i32, P, i32, P, P, P, P]
+    lib.pcp_build_row_plan.restype = ctypes.c_int
+    lib.pcp_mask_slots_for_shard.argtypes = [P, P, i32, i32, P]
+    lib.pcp_mask_slots_for_shard.restype = ctypes.c_int
+    lib.pcp_kv_cache_write.argtypes = [P, P, P, i32, P, P, i64, i32, i32, i32, P, P]
+    lib.pcp_kv_cache_write.restype = ctypes.c_int
+    lib.pcp_attn_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.pcp_attn_workspace_size.restype = sz
+    lib.pcp_attn_varlen.argtypes = [P, P, P, P, i32, i32, i64, i32, P, i32, i32, i32, i32, i32, f32, P, P, P,
+                                    sz, i32, P, P]
+    lib.pcp_attn_varlen.restype = ctypes.c_int
+    lib.pcp_lse_merge.argtypes = [P, P, P, P, P, P, i32, i32, i32, P]
+    lib.pcp_lse_merge.restype = ctypes.c_int
+    lib.pcp_last_cuda_error.argtypes = []
+    lib.pcp_last_cuda_error.restype = ctypes.c_int
+    lib.pcp_status_string.argtypes = [ctypes.c_int]
+    lib.pcp_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _np_ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _t_ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(rc: int, what: str):
+    if rc != PCP_OK:
+        raise PcpError(rc, what)
+
+
+def pcp_build_row_plan(query_len, num_computed, block_table, block_size: int, num_shards: int,
+                       split_mode: int = PCP_SPLIT_CONTIGUOUS, rows_capacity: Optional[int] = None):
+    """Host row plan and slot mapping. Returns a dict of numpy arrays:
+    ``rows`` int32[n, 8], ``cu_q`` int32[n+1], ``slot_mapping`` int64[T],
+    ``owner_shard`` int8[T]."""
+    lib = load()
+    ql = np.ascontiguousarray(np.asarray(query_len, dtype=np.int32))
+    nc = np.ascontiguousarray(np.asarray(num_computed, dtype=np.int32))
+    bt = block_table.numpy() if isinstance(block_table, torch.Tensor) else block_table
+    bt = np.ascontiguousarray(np.asarray(bt, dtype=np.int32))
+    R = int(ql.shape[0])
+    mb = int(bt.shape[1]) if bt.ndim == 2 else 0
+    T = int(ql.sum())
+    cap = rows_capacity if rows_capacity is not None else max(1, 2 * num_shards * R)
+    rows = np.zeros((max(cap, 1), 8), dtype=np.int32)
+    cu = np.zeros(max(cap, 1) + 1, dtype=np.int32)
+    slot = np.zeros(max(T, 1), dtype=np.int64)
+    owner = np.zeros(max(T, 1), dtype=np.int8)
+    n = np.zeros(1, dtype=np.int32)
+    rc = lib.pcp_build_row_plan(R, _np_ptr(ql), _np_ptr(nc), _np_ptr(bt), mb, block_size, num_shards,
+                                split_mode, _np_ptr(rows), cap, _np_ptr(n), _np_ptr(cu), _np_ptr(slot),
+                                _np_ptr(owner))
+    _check(rc, "pcp_build_row_plan")
+    k = int(n[0])
+    return dict(rows=rows[:k], cu_q=cu[:k + 1], slot_mapping=slot[:T], owner_shard=owner[:T])
+
+
+def pcp_mask_slots_for_shard(slot_mapping: np.ndarray, owner_shard: np.ndarray, shard: int) -> np.ndarray:
+    """PAD-masked slot mapping of one shard (host arrays)."""
+    lib = load()
+    s = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    o = np.ascontiguousarray(owner_shard, dtype=np.int8)
+    out = np.empty_like(s)
+    _check(lib.pcp_mask_slots_for_shard(_np_ptr(s), _np_ptr(o), int(s.shape[0]), shard, _np_ptr(out)),
+           "pcp_mask_slots_for_shard")
+    return out
+
+
+def pcp_kv_cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                       key_cache: torch.Tensor, value_cache: torch.Tensor,
+                       status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Scatter new K/V ``[T, Hkv, D]`` into the paged caches ``[num_blocks, bs, Hkv, D]``."""
+    lib = load()
+    T = int(k.shape[0])
+    nb, bs, hkv, d = (int(x) for x in key_cache.shape)
+    rc = lib.pcp_kv_cache_write(_t_ptr(k), _t_ptr(v), _t_ptr(slot_mapping), T, _t_ptr(key_cache),
+                                _t_ptr(value_cache), nb, bs, hkv, d, _t_ptr(status), _stream(stream))
+    _check(rc, "pcp_kv_cache_write")
+
+
+def pcp_attn_workspace_size(num_rows: int, total_q: int, num_q_heads: int, head_dim: int,
+                            max_kv_len: int, flags: int = 0) -> int:
+    return int(load().pcp_attn_workspace_size(num_rows, total_q, num_q_heads, head_dim, max_kv_len, flags))
+
+
+def pcp_attn_varlen(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                    block_table: torch.Tensor, rows: torch.Tensor, scale: float,
+                    out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                    workspace: Optional[torch.Tensor] = None, flags: int = 0,
+                    status: Optional[torch.Tensor] = None, stream=None):
+    """Attention of every planned row. ``q`` ``[T, Hq, D]`` bf16; ``rows`` int32
+    ``[n, 8]`` on the device; returns ``(out [T, Hq, D] bf16, lse [Hq, T] fp32)``.
+    Pass ``out``/``lse``/``workspace`` to avoid allocating per call."""
+    lib = load()
+    T, hq, d = (int(x) for x in q.shape)
+    nb, bs, hkv, d2 = (int(x) for x in key_cache.shape)
+    n_rows = int(rows.shape[0])
+    mb = int(block_table.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
+    need = pcp_attn_workspace_size(n_rows, T, hq, d, mb * bs, flags)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = lib.pcp_attn_varlen(_t_ptr(q), _t_ptr(key_cache), _t_ptr(value_cache), _t_ptr(block_table),
+                             int(block_table.shape[0]), mb, nb,
+                             bs, _t_ptr(rows), n_rows, T, hq, hkv, d, float(scale), _t_ptr(out), _t_ptr(lse),
+                             _t_ptr(workspace), int(workspace.numel() * workspace.element_size()), flags,
+                             _t_ptr(status), _stream(stream))
+    _check(rc, "pcp_attn_varlen")
+    return out, lse
+
+
+def pcp_lse_merge(out_a: torch.Tensor, lse_a: torch.Tensor, out_b: torch.Tensor, lse_b: torch.Tensor,
+                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None, stream=None):
+    """LSE merge of two fp32 partials ``[T, Hq, D]`` / ``[Hq, T]`` into bf16 out and fp32 lse."""
+    lib = load()
+    T, hq, d = (int(x) for x in out_a.shape)
+    if out is None:
+        out = torch.empty(out_a.shape, dtype=torch.bfloat16, device=out_a.device)
+    if lse is None:
+        lse = torch.empty_like(lse_a)
+    rc = lib.pcp_lse_merge(_t_ptr(out_a), _t_ptr(lse_a), _t_ptr(out_b), _t_ptr(lse_b), _t_ptr(out), _t_ptr(lse),
+                           T, hq, d, _stream(stream))
+    _check(rc, "pcp_lse_merge")
+    return out, lse

@@ -1,0 +1,198 @@
+// The C ABI of libpcp (declared in include/pcp.h): argument validation on the
+// host, workspace layout and the launch sequence of one attention call.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "pcp.h"
+#include "pcp_internal.h"
+
+namespace pcp {
+
+namespace {
+thread_local int g_last_cuda_error = 0;
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+void set_last_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
+
+int num_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+WorkspaceLayout workspace_layout(int32_t num_rows, int32_t total_q, int32_t num_q_heads,
+                                 int32_t head_dim, int32_t max_kv_len, int32_t flags) {
+    WorkspaceLayout w{};
+    const bool separate = (flags & PCP_ATTN_SEPARATE_CONTEXT) != 0;
+    const int64_t passes = separate ? 2 : 1;
+    w.max_units = passes * ((int64_t)(total_q + kBlockM - 1) / kBlockM + num_rows);
+    w.max_splits = max_kv_len > 0 ? (max_kv_len + kDecodeChunk - 1) / kDecodeChunk : 1;
+    size_t o = 0;
+    w.header = o;
+    o = align256(o + 64 * sizeof(int32_t));
+    w.row_ok = o;
+    o = align256(o + (size_t)num_rows * sizeof(int32_t));
+    w.units = o;
+    o = align256(o + (size_t)w.max_units * sizeof(Unit));
+    w.units_sorted = o;
+    o = align256(o + (size_t)w.max_units * sizeof(Unit));
+    const size_t part = (size_t)total_q * num_q_heads * head_dim * sizeof(float);
+    const size_t plse = (size_t)total_q * num_q_heads * sizeof(float);
+    for (int i = 0; i < 2; ++i) {
+        w.part_out[i] = o;
+        o = align256(o + (separate ? part : 0));
+        w.part_lse[i] = o;
+        o = align256(o + (separate ? plse : 0));
+    }
+    const size_t dec = (size_t)num_rows * num_q_heads * w.max_splits;
+    w.dec_out = o;
+    o = align256(o + dec * head_dim * sizeof(float));
+    w.dec_lse = o;
+    o = align256(o + dec * sizeof(float));
+    w.total = o;
+    return w;
+}
+
+}  // namespace pcp
+
+using namespace pcp;
+
+extern "C" int pcp_last_cuda_error(void) { return g_last_cuda_error; }
+
+extern "C" const char* pcp_status_string(int status) {
+    switch (status) {
+        case PCP_OK: return "ok";
+        case PCP_ERR_ARG: return "invalid argument";
+        case PCP_ERR_RANGE: return "index out of range";
+        case PCP_ERR_UNSUPPORTED: return "unsupported configuration";
+        case PCP_ERR_ALIGN: return "misaligned pointer";
+        case PCP_ERR_CUDA: return "CUDA error";
+        case PCP_ERR_TIMEOUT: return "device wait timed out";
+        case PCP_ERR_WORKSPACE: return "workspace too small";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int pcp_kv_cache_write(const void* k, const void* v, const int64_t* slot_mapping,
+                                  int32_t num_tokens, void* key_cache, void* value_cache,
+                                  int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t* status, pcp_stream_t stream) {
+    if (num_tokens < 0 || num_blocks < 0 || block_size < 1 || num_kv_heads < 1 || head_dim < 1)
+        return PCP_ERR_ARG;
+    if (num_tokens == 0) return PCP_OK;
+    if (!k || !v || !slot_mapping || !key_cache || !value_cache) return PCP_ERR_ARG;
+    if (((int64_t)head_dim * 2 * num_kv_heads) % 16 != 0) return PCP_ERR_UNSUPPORTED;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(key_cache) || !aligned16(value_cache) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PCP_ERR_ALIGN;
+    const int32_t vec_per_tok = (int32_t)((int64_t)head_dim * 2 * num_kv_heads / 16);
+    return launch_cache_write(k, v, slot_mapping, num_tokens, vec_per_tok, key_cache, value_cache,
+                              num_blocks * block_size, status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t pcp_attn_workspace_size(int32_t num_rows, int32_t total_q, int32_t num_q_heads,
+                                          int32_t head_dim, int32_t max_kv_len, int32_t flags) {
+    if (num_rows < 0 || total_q < 0 || num_q_heads < 1 || head_dim < 1 || max_kv_len < 0) return 0;
+    return workspace_layout(num_rows, total_q, num_q_heads, head_dim, max_kv_len, flags).total;
+}
+
+extern "C" int pcp_attn_varlen(const void* q, const void* key_cache, const void* value_cache,
+                               const int32_t* block_table, int32_t num_reqs,
+                               int32_t max_blocks_per_req, int64_t num_blocks, int32_t block_size, const pcp_row_t* rows,
+                               int32_t num_rows, int32_t total_q, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, float scale, void* out,
+                               float* lse, void* workspace, size_t workspace_bytes, int32_t flags,
+                               int32_t* status, pcp_stream_t stream) {
+    if (num_rows < 0 || total_q < 0 || num_reqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || max_blocks_per_req < 0 ||
+        num_blocks < 0 || block_size < 1)
+        return PCP_ERR_ARG;
+    if (flags & ~(PCP_ATTN_SEPARATE_CONTEXT | PCP_ATTN_SPLIT_AT_ROW_START)) return PCP_ERR_ARG;
+    if (num_q_heads % num_kv_heads != 0) return PCP_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PCP_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
+        return PCP_ERR_UNSUPPORTED;
+    if (num_q_heads / num_kv_heads > 16) return PCP_ERR_UNSUPPORTED;
+    if (num_rows == 0 || total_q == 0) return PCP_OK;
+    if (!q || !key_cache || !value_cache || !block_table || !rows || !out || !lse || !workspace)
+        return PCP_ERR_ARG;
+    if (!aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+        (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(rows) & 3u))
+        return PCP_ERR_ALIGN;
+    if (num_blocks * (int64_t)block_size > INT32_MAX || (int64_t)total_q * num_q_heads > INT32_MAX)
+        return PCP_ERR_ARG;
+    const int64_t max_kv = (int64_t)max_blocks_per_req * block_size;
+    if (max_kv > INT32_MAX) return PCP_ERR_ARG;
+    const WorkspaceLayout w =
+        workspace_layout(num_rows, total_q, num_q_heads, head_dim, (int32_t)max_kv, flags);
+    if (workspace_bytes < w.total) return PCP_ERR_WORKSPACE;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    PrefillArgs a{};
+    a.q = q;
+    a.key_cache = key_cache;
+    a.value_cache = value_cache;
+    a.block_table = block_table;
+    a.num_reqs = num_reqs;
+    a.max_blocks = max_blocks_per_req;
+    a.num_blocks = num_blocks;
+    a.block_size = block_size;
+    a.rows = rows;
+    a.num_rows = num_rows;
+    a.total_q = total_q;
+    a.hq = num_q_heads;
+    a.hkv = num_kv_heads;
+    a.d = head_dim;
+    a.scale = scale;
+    a.out = out;
+    a.lse = lse;
+    for (int i = 0; i < 2; ++i) {
+        a.part_out[i] = reinterpret_cast<float*>(ws + w.part_out[i]);
+        a.part_lse[i] = reinterpret_cast<float*>(ws + w.part_lse[i]);
+    }
+    a.row_ok = reinterpret_cast<const int32_t*>(ws + w.row_ok);
+    a.units = reinterpret_cast<const Unit*>(ws + w.units_sorted);
+    a.num_units = reinterpret_cast<const int32_t*>(ws + w.header);
+    a.status = status;
+
+    int rc = launch_schedule(a, flags, reinterpret_cast<Unit*>(ws + w.units),
+                             reinterpret_cast<Unit*>(ws + w.units_sorted),
+                             reinterpret_cast<int32_t*>(ws + w.header),
+                             reinterpret_cast<int32_t*>(ws + w.row_ok), w.max_units, s);
+    if (rc != PCP_OK) return rc;
+    rc = launch_decode(a, reinterpret_cast<float*>(ws + w.dec_out), reinterpret_cast<float*>(ws + w.dec_lse),
+                       w.max_splits, s);
+    if (rc != PCP_OK) return rc;
+    rc = launch_prefill(a, s);
+    if (rc != PCP_OK) return rc;
+    if (flags & PCP_ATTN_SEPARATE_CONTEXT) rc = launch_separate_merge(a, s);
+    return rc;
+}
+
+extern "C" int pcp_lse_merge(const float* out_a, const float* lse_a, const float* out_b,
+                             const float* lse_b, void* out, float* lse, int32_t total_q,
+                             int32_t num_q_heads, int32_t head_dim, pcp_stream_t stream) {
+    if (total_q < 0 || num_q_heads < 1 || head_dim < 1) return PCP_ERR_ARG;
+    if (head_dim % 8 != 0) return PCP_ERR_UNSUPPORTED;
+    if (total_q == 0) return PCP_OK;
+    if (!out_a || !lse_a || !out_b || !lse_b || !out || !lse) return PCP_ERR_ARG;
+    if (lse == lse_a || lse == lse_b) return PCP_ERR_ARG;
+    if (!aligned16(out_a) || !aligned16(out_b) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(lse_a) & 3u) || (reinterpret_cast<uintptr_t>(lse_b) & 3u) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return PCP_ERR_ALIGN;
+    return launch_lse_merge(out_a, lse_a, out_b, lse_b, out, lse, total_q, num_q_heads, head_dim,
+                            reinterpret_cast<cudaStream_t>(stream));
+}

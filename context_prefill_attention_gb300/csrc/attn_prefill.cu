@@ -1,0 +1,647 @@
+// Prefill / context attention of PCP rows on the 5th-generation tensor cores.
+//
+// What it computes ("Feat/pcp qwen36 hybrid", "Changes": end-aligned causal
+// attention of a rank's contiguous slice over the reconstructed K/V; "[MRv2]
+// FlashAttention PCP support for GQA on MRv2", overview: cached-prefix context
+// attention combined by log-sum-exp; "[MRv2][PCP] Carry the row plan ...",
+// "What made it removable": a row's seq_len is its end position): for query j
+// of a row at position p = kv_end - q_len + j, the softmax of
+// scale * q . k over keys k in [k_lo, min(k_hi, p + 1)), its weighted sum of V,
+// and the natural-log LSE.
+//
+// Design (sm_103a):
+//  * persistent grid, one CTA per SM; work items = (row tile of 128 tokens,
+//    pass, pair of q heads sharing one kv head), longest first;
+//  * warp 8 produces: TMA loads of the Q tiles and of K/V pages (one 3-D box
+//    of block_size keys x 64 dims per page and half head-dim) straight from the
+//    paged cache through the block table, 128-byte swizzled;
+//  * warp 9 issues tcgen05 MMAs from one lane: S = Q K^T into TMEM (A and B
+//    from shared memory), then O += P V with P read from TMEM (it overwrites S)
+//    and V from shared memory;
+//  * warps 0-3 and 4-7 are two softmax warpgroups, one per q head of the item,
+//    one thread per query row: they read S from TMEM, mask, keep the running
+//    max and sum, rescale O in TMEM when the max grows by more than 2^8, write
+//    P back as bf16, and finally normalise O and store out and lse;
+//  * the two heads' MMAs interleave (S0 S1 | PV0 S0' PV1 S1' | ...) so each
+//    warpgroup's softmax overlaps the other head's MMAs;
+//  * every mbarrier wait is bounded: a wait that runs out sets PCP_ERR_TIMEOUT
+//    in the status word and the CTA winds down, freeing its TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include "pcp_device.cuh"
+#include "pcp_internal.h"
+
+namespace pcp {
+
+namespace {
+
+constexpr int kThreads = 320;  // 10 warps
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kNK = 2;  // K stages
+constexpr int kNV = 2;  // V stages
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct Cfg {
+    static constexpr int kHalves = D / 64;                 // 64-column (128-byte) sub-tiles
+    static constexpr int kHalfBytes = 128 * 128;           // 128 rows x 128 bytes
+    static constexpr int kTileBytes = kHalves * kHalfBytes;
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + 2 * kTileBytes;
+    static constexpr int kV = kK + kNK * kTileBytes;
+    static constexpr int kBar = kV + kNV * kTileBytes;
+    static constexpr int kNumBars = 2 + 2 * kNK + 2 * kNV + 8;
+    static constexpr int kMisc = kBar + kNumBars * 8;      // tmem address, abort flag
+    static constexpr int kSmem = kMisc + 16 + 1024;        // + alignment slack
+    static constexpr uint32_t kTmemCols = 512;
+    __host__ __device__ static constexpr uint32_t tmem_s(int g) { return g ? 128u : 0u; }
+    __host__ __device__ static constexpr uint32_t tmem_o(int g) { return g ? 256u + D : 256u; }
+    static constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
+    static constexpr uint32_t kIdescO = idesc_bf16(128, D, false, true);
+};
+
+struct Item {
+    int32_t req, q_tok0, rows_valid, pos0, k_lo, k_hi, k_end, kb, n_tiles, pass, h0, hk, nslots;
+};
+
+__device__ __forceinline__ int32_t tiles_of(int32_t k_lo, int32_t k_end, int32_t bs) {
+    if (k_end <= k_lo) return 0;
+    const int32_t kb = (k_lo / bs) * bs;
+    return (k_end - kb + kBlockN - 1) / kBlockN;
+}
+
+__device__ __forceinline__ Item decode_item(const Unit* units, int32_t idx, int32_t slots_per_unit,
+                                            bool dual, int32_t G, const pcp_row_t* rows,
+                                            int32_t bs) {
+    const Unit u = units[idx / slots_per_unit];
+    const int32_t hs = idx % slots_per_unit;
+    const pcp_row_t r = rows[u.row];
+    Item it;
+    const int32_t mt = u.mt_pass & 0xFFFFFF;
+    it.pass = u.mt_pass >> 24;
+    it.req = r.req;
+    it.q_tok0 = r.q_start + mt * kBlockM;
+    it.rows_valid = min(kBlockM, r.q_len - mt * kBlockM);
+    it.pos0 = r.kv_end - r.q_len + mt * kBlockM;
+    it.k_lo = u.k_lo;
+    it.k_hi = u.k_hi;
+    it.k_end = min(u.k_hi, it.pos0 + it.rows_valid);
+    it.kb = (u.k_lo / bs) * bs;
+    it.n_tiles = tiles_of(u.k_lo, it.k_end, bs);
+    it.nslots = dual ? 2 : 1;
+    it.h0 = dual ? 2 * hs : hs;
+    it.hk = it.h0 / G;
+    return it;
+}
+
+// S = Q_slot K^T over D (K-major A and B, 128-byte swizzle).
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_smem, uint32_t k_smem) {
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t off = (ks / 4) * Cfg<D>::kHalfBytes + (ks % 4) * 32;
+        const uint64_t a = sdesc_sw128(q_smem + off, 16, 1024);
+        const uint64_t b = sdesc_sw128(k_smem + off, 16, 1024);
+        mma_ss(tmem_s, a, b, Cfg<D>::kIdescS, ks > 0 ? 1u : 0u);
+    }
+}
+
+// O (+)= P V: P from TMEM (bf16 pairs in the S columns), V MN-major in shared memory.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_smem,
+                                         bool accumulate) {
+#pragma unroll
+    for (int ks = 0; ks < kBlockN / 16; ++ks) {
+        const uint64_t b = sdesc_sw128(v_smem + ks * 2048, Cfg<D>::kHalfBytes, 1024);
+        mma_ts(tmem_o, tmem_p + ks * 8, b, Cfg<D>::kIdescO, (accumulate || ks > 0) ? 1u : 0u);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, PrefillArgs a) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + C::kBar;
+    // barrier addresses
+    const uint32_t q_full = bar0, q_empty = bar0 + 8;
+    auto k_full = [&](int s) { return bar0 + 16 + 8 * s; };
+    auto k_empty = [&](int s) { return bar0 + 16 + 8 * (kNK + s); };
+    auto v_full = [&](int s) { return bar0 + 16 + 8 * (2 * kNK + s); };
+    auto v_empty = [&](int s) { return bar0 + 16 + 8 * (2 * kNK + kNV + s); };
+    const uint32_t bx = bar0 + 16 + 8 * (2 * kNK + 2 * kNV);
+    auto s_full = [&](int g) { return bx + 8 * g; };
+    auto p_full = [&](int g) { return bx + 16 + 8 * g; };
+    auto o_done = [&](int g) { return bx + 32 + 8 * g; };
+    auto o_free = [&](int g) { return bx + 48 + 8 * g; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int G = a.hq / a.hkv;
+    const bool dual = (G % 2) == 0;
+    const int slots_per_unit = dual ? a.hq / 2 : a.hq;
+    const int32_t bs = a.block_size;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int s = 0; s < kNK; ++s) { mbar_init(k_full(s), 1); mbar_init(k_empty(s), 1); }
+        for (int s = 0; s < kNV; ++s) { mbar_init(v_full(s), 1); mbar_init(v_empty(s), 1); }
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(s_full(g), 1);
+            mbar_init(p_full(g), 128);
+            mbar_init(o_done(g), 1);
+            mbar_init(o_free(g), 128);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int32_t total_items = (*a.num_units) * slots_per_unit;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t kt = 0, vt = 0, c = 0;
+            const int32_t oob = (int32_t)(a.num_blocks * bs);  // a row past the cache: zero fill
+            const int pages = kBlockN / bs;
+            bool ok = true;
+            for (int32_t idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+                const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, bs);
+                if (it.n_tiles == 0) continue;
+                if (c > 0 && !(ok = mbar_wait(q_empty, (c - 1) & 1, abort_flag))) break;
+                mbar_arrive_expect_tx(q_full, it.nslots * C::kTileBytes);
+                for (int g = 0; g < it.nslots; ++g)
+                    for (int h = 0; h < C::kHalves; ++h)
+                        tma_load_3d(sbase + C::kQ + g * C::kTileBytes + h * C::kHalfBytes, &tm_q,
+                                    q_full, h * 64, it.h0 + g, it.q_tok0);
+                const int32_t* table = a.block_table + (size_t)it.req * a.max_blocks;
+                // page id -> first cache row of the page; pages past k_end (and bad ids)
+                // map to a row past the cache, which TMA fills with zeros
+                auto page_row = [&](int32_t key0, int p) -> int32_t {
+                    const int32_t k = key0 + p * bs;
+                    if (k >= it.k_end) return oob;
+                    const int32_t pg = k / bs;
+                    const int32_t id = pg < a.max_blocks ? __ldg(table + pg) : -1;
+                    if (id >= 0 && id < a.num_blocks) return id * bs;
+                    report_status(a.status, PCP_ERR_RANGE);
+                    return oob;
+                };
+                for (int32_t j = 0; j < it.n_tiles && ok; ++j) {
+                    const int32_t key0 = it.kb + j * kBlockN;
+                    const int ks = kt % kNK;
+                    if (!(ok = mbar_wait(k_empty(ks), ((kt / kNK) & 1) ^ 1, abort_flag))) break;
+                    mbar_arrive_expect_tx(k_full(ks), C::kTileBytes);
+                    for (int p = 0; p < pages; ++p)
+                        for (int h = 0; h < C::kHalves; ++h)
+                            tma_load_3d(sbase + C::kK + ks * C::kTileBytes + h * C::kHalfBytes +
+                                            p * bs * 128,
+                                        &tm_k, k_full(ks), h * 64, it.hk, page_row(key0, p));
+                    ++kt;
+                    const int vs = vt % kNV;
+                    if (!(ok = mbar_wait(v_empty(vs), ((vt / kNV) & 1) ^ 1, abort_flag))) break;
+                    mbar_arrive_expect_tx(v_full(vs), C::kTileBytes);
+                    for (int p = 0; p < pages; ++p)
+                        for (int h = 0; h < C::kHalves; ++h)
+                            tma_load_3d(sbase + C::kV + vs * C::kTileBytes + h * C::kHalfBytes +
+                                            p * bs * 128,
+                                        &tm_v, v_full(vs), h * 64, it.hk, page_row(key0, p));
+                    ++vt;
+                }
+                ++c;
+            }
+            if (!ok) report_status(a.status, PCP_ERR_TIMEOUT);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        uint32_t kt = 0, vt = 0, c = 0;
+        uint32_t pph[2] = {0, 0}, nslot_items[2] = {0, 0};
+        bool ok = true;
+        const bool leader = lane == 0;
+        for (int32_t idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+            const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, bs);
+            const int n = it.n_tiles;
+            if (n == 0) continue;
+            if (!(ok = mbar_wait_warp(q_full, c & 1, abort_flag))) break;
+            int ks = kt % kNK;
+            if (!(ok = mbar_wait_warp(k_full(ks), (kt / kNK) & 1, abort_flag))) break;
+            tc_fence_after();
+            if (leader) {
+                for (int g = 0; g < it.nslots; ++g) {
+                    issue_qk<D>(tmem + C::tmem_s(g), sbase + C::kQ + g * C::kTileBytes,
+                                sbase + C::kK + ks * C::kTileBytes);
+                    mma_commit(s_full(g));
+                }
+                mma_commit(k_empty(ks));
+                if (n == 1) mma_commit(q_empty);
+            }
+            __syncwarp();
+            ++kt;
+            for (int j = 0; j < n && ok; ++j) {
+                const int vs = vt % kNV;
+                if (!(ok = mbar_wait_warp(v_full(vs), (vt / kNV) & 1, abort_flag))) break;
+                if (j == n - 1 && (it.k_end % bs) != 0) {
+                    // Keys at or past k_end inside the last loaded page may never have been
+                    // written: zero their V rows so that P = 0 cannot meet a NaN.
+                    const int32_t rel = it.k_end - (it.kb + j * kBlockN);
+                    const int32_t r1 = ((rel + bs - 1) / bs) * bs;
+                    const int nbytes = (r1 - rel) * 128;
+                    for (int h = 0; h < C::kHalves; ++h) {
+                        uint8_t* base = smem + C::kV + vs * C::kTileBytes + h * C::kHalfBytes + rel * 128;
+                        for (int off = lane * 16; off < nbytes; off += 32 * 16)
+                            *reinterpret_cast<uint4*>(base + off) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                for (int g = 0; g < it.nslots && ok; ++g) {
+                    if (!(ok = mbar_wait_warp(p_full(g), pph[g], abort_flag))) break;
+                    pph[g] ^= 1;
+                    if (j == 0 && nslot_items[g] > 0) {
+                        if (!(ok = mbar_wait_warp(o_free(g), (nslot_items[g] - 1) & 1, abort_flag))) break;
+                    }
+                    tc_fence_after();
+                    if (leader)
+                        issue_pv<D>(tmem + C::tmem_o(g), tmem + C::tmem_s(g),
+                                    sbase + C::kV + vs * C::kTileBytes, j > 0);
+                    if (g == it.nslots - 1 && leader) mma_commit(v_empty(vs));
+                    if (j + 1 < n) {
+                        if (g == 0) {
+                            ks = kt % kNK;
+                            if (!(ok = mbar_wait_warp(k_full(ks), (kt / kNK) & 1, abort_flag))) break;
+                            tc_fence_after();
+                        }
+                        if (leader) {
+                            issue_qk<D>(tmem + C::tmem_s(g), sbase + C::kQ + g * C::kTileBytes,
+                                        sbase + C::kK + ks * C::kTileBytes);
+                            mma_commit(s_full(g));
+                            if (g == it.nslots - 1) {
+                                mma_commit(k_empty(ks));
+                                if (j + 1 == n - 1) mma_commit(q_empty);
+                            }
+                        }
+                        if (g == it.nslots - 1) ++kt;
+                    } else if (leader) {
+                        mma_commit(o_done(g));
+                    }
+                    __syncwarp();
+                }
+                ++vt;
+            }
+            for (int g = 0; g < it.nslots; ++g) ++nslot_items[g];
+            ++c;
+        }
+        if (!ok) report_status(a.status, PCP_ERR_TIMEOUT);
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int g = warp / 4;                 // head slot of this warpgroup
+        const int r = threadIdx.x % 128;        // query row within the tile = TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
+        const uint32_t t_s = tmem + lane_base + C::tmem_s(g);
+        const uint32_t t_o = tmem + lane_base + C::tmem_o(g);
+        const float sl2 = a.scale * kLog2e;
+        uint32_t sph = 0, oph = 0;
+        bool ok = true;
+        for (int32_t idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+            const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, bs);
+            if (g >= it.nslots) continue;
+            const int h = it.h0 + g;
+            const bool valid = r < it.rows_valid;
+            const int32_t pos = it.pos0 + min(r, it.rows_valid - 1);
+            const int32_t tok = it.q_tok0 + r;
+            float m = -INFINITY, l = 0.f;
+            const int n = it.n_tiles;
+            for (int j = 0; j < n && ok; ++j) {
+                if (!(ok = mbar_wait_warp(s_full(g), sph, abort_flag))) break;
+                sph ^= 1;
+                tc_fence_after();
+                uint32_t s[128];
+                tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+                tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+                tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+                tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+                tmem_wait_ld();
+                float* sf = reinterpret_cast<float*>(s);
+                const int32_t key0 = it.kb + j * kBlockN;
+                const bool full = key0 >= it.k_lo && key0 + kBlockN <= it.k_hi &&
+                                  key0 + kBlockN - 1 <= it.pos0;
+                if (!full) {
+                    const int32_t lo = it.k_lo - key0;
+                    const int32_t hi = min(it.k_hi, pos + 1) - key0;
+#pragma unroll
+                    for (int c2 = 0; c2 < 128; ++c2)
+                        if (c2 < lo || c2 >= hi) sf[c2] = -INFINITY;
+                }
+                float mx = sf[0];
+#pragma unroll
+                for (int c2 = 1; c2 < 128; ++c2) mx = fmaxf(mx, sf[c2]);
+                const float m_new = fmaxf(m, mx * sl2);
+                // Lazy rescaling: keep the old reference max unless the new one exceeds
+                // it by more than 2^8; O and l then stay consistent with that max.
+                float alpha = 1.f;
+                bool rescale = false;
+                if (j == 0) {
+                    m = m_new;
+                } else {
+                    const bool need = m_new > m + kRescaleThreshold;
+                    rescale = __any_sync(0xffffffffu, need);
+                    if (need) {
+                        alpha = fast_exp2(m - m_new);
+                        l *= alpha;
+                        m = m_new;
+                    }
+                }
+                const float mu = (m == -INFINITY) ? 0.f : m;
+                float rs = 0.f;
+                uint32_t p[64];
+#pragma unroll
+                for (int c2 = 0; c2 < 64; ++c2) {
+                    const float p0 = fast_exp2(fmaf(sf[2 * c2], sl2, -mu));
+                    const float p1 = fast_exp2(fmaf(sf[2 * c2 + 1], sl2, -mu));
+                    rs += p0 + p1;
+                    p[c2] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+                tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+                if (rescale) {
+#pragma unroll
+                    for (int c2 = 0; c2 < D / 32; ++c2) {
+                        uint32_t o[32];
+                        tmem_ld32(t_o + 32 * c2, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(t_o + 32 * c2, o);
+                    }
+                }
+                l += rs;
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(p_full(g));
+            }
+            if (!ok) break;
+            // ---- epilogue: out = O / l, lse = ln 2 * (m + log2 l)
+            const bool has = l > 0.f;
+            const float inv = has ? 1.f / l : 0.f;
+            const float lse_v = has ? (m + __log2f(l)) * kLn2 : -INFINITY;
+            if (n > 0) {
+                if (!(ok = mbar_wait_warp(o_done(g), oph, abort_flag))) break;
+                oph ^= 1;
+                tc_fence_after();
+            }
+            const size_t orow = ((size_t)tok * a.hq + h) * D;
+#pragma unroll
+            for (int c2 = 0; c2 < D / 32; ++c2) {
+                uint32_t o[32];
+                if (n > 0) {
+                    tmem_ld32(t_o + 32 * c2, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                }
+                if (valid) {
+                    if (it.pass == 0) {
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            reinterpret_cast<__nv_bfloat16*>(a.out) + orow + 32 * c2);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
+                            w.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
+                            w.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
+                            w.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
+                            dst[v4] = w;
+                        }
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(a.part_out[it.pass - 1] + orow + 32 * c2);
+#pragma unroll
+                        for (int v4 = 0; v4 < 8; ++v4)
+                            dst[v4] = make_float4(__uint_as_float(o[4 * v4 + 0]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
+                                                  __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
+                    }
+                }
+            }
+            if (valid) {
+                float* lse_dst = it.pass == 0 ? a.lse : a.part_lse[it.pass - 1];
+                lse_dst[(size_t)h * a.total_q + tok] = lse_v;
+            }
+            if (n > 0) {
+                tc_fence_before();
+                mbar_arrive(o_free(g));
+            }
+        }
+        if (!ok) report_status(a.status, PCP_ERR_TIMEOUT);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ scheduler
+
+constexpr int kSchedThreads = 1024;
+constexpr int kSortCap = 4096;
+
+__device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* warp_sums, int32_t* total) {
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+    int32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t w = lane < kSchedThreads / 32 ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        warp_sums[lane] = w;  // inclusive
+    }
+    __syncthreads();
+    const int32_t before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+    *total = warp_sums[kSchedThreads / 32 - 1];
+    __syncthreads();
+    return before;
+}
+
+// Check every row, then build the prefill work list: one unit per (valid
+// non-decode row, 128-token tile, pass), ordered by the number of key tiles,
+// longest first.
+__global__ void __launch_bounds__(kSchedThreads, 1)
+    schedule_kernel(PrefillArgs a, int32_t flags, Unit* units, Unit* sorted, int32_t* header,
+                    int32_t* row_ok, int64_t max_units) {
+    __shared__ int32_t warp_sums[32];
+    __shared__ unsigned long long keys[kSortCap];
+    const pcp_row_t* rows = a.rows;
+    const int32_t num_rows = a.num_rows, bs = a.block_size;
+    const int64_t max_kv = (int64_t)a.max_blocks * bs;
+    const bool separate = (flags & PCP_ATTN_SEPARATE_CONTEXT) != 0;
+    const bool at_row_start = (flags & PCP_ATTN_SPLIT_AT_ROW_START) != 0;
+    const int passes = separate ? 2 : 1;
+    int32_t base = 0;
+    for (int32_t r0 = 0; r0 < num_rows; r0 += kSchedThreads) {
+        const int32_t ri = r0 + threadIdx.x;
+        pcp_row_t row{};
+        int32_t cnt = 0;
+        if (ri < num_rows) {
+            row = rows[ri];
+            const bool ok = row.req >= 0 && row.req < a.num_reqs && row.q_len >= 1 && row.q_start >= 0 &&
+                            (int64_t)row.q_start + row.q_len <= a.total_q && row.kv_end >= row.q_len &&
+                            row.kv_end <= max_kv && row.ctx_len >= 0 && row.ctx_len <= row.kv_end &&
+                            (row.is_decode == 0 || (row.is_decode == 1 && row.q_len == 1));
+            row_ok[ri] = ok ? 1 : 0;
+            if (!ok) report_status(a.status, PCP_ERR_RANGE);
+            if (ok && !row.is_decode) cnt = ((row.q_len + kBlockM - 1) / kBlockM) * passes;
+        }
+        int32_t tot;
+        const int32_t off = base + block_exclusive_scan(cnt, warp_sums, &tot);
+        for (int32_t u = 0; u < cnt; ++u) {
+            if (off + u >= max_units) break;
+            const int32_t mt = u / passes, pass = separate ? 1 + u % passes : 0;
+            const int32_t split = at_row_start ? row.kv_end - row.q_len : row.ctx_len;
+            Unit x;
+            x.row = ri;
+            x.mt_pass = mt | (pass << 24);
+            x.k_lo = pass == 2 ? split : 0;
+            x.k_hi = pass == 1 ? split : row.kv_end;
+            units[off + u] = x;
+        }
+        base += tot;
+    }
+    const int32_t n = (int32_t)min((int64_t)base, max_units);
+    if (threadIdx.x == 0) header[0] = n;
+    if (n > kSortCap) {
+        for (int32_t i = threadIdx.x; i < n; i += kSchedThreads) sorted[i] = units[i];
+        return;
+    }
+    __syncthreads();
+    int32_t pow2 = 1;
+    while (pow2 < n) pow2 <<= 1;
+    for (int32_t i = threadIdx.x; i < pow2; i += kSchedThreads) {
+        unsigned long long key = ~0ull;
+        if (i < n) {
+            const Unit u = units[i];
+            const pcp_row_t row = rows[u.row];
+            const int32_t mt = u.mt_pass & 0xFFFFFF;
+            const int32_t pos0 = row.kv_end - row.q_len + mt * kBlockM;
+            const int32_t rv = min(kBlockM, row.q_len - mt * kBlockM);
+            const int32_t cost = tiles_of(u.k_lo, min(u.k_hi, pos0 + rv), bs);
+            key = ((unsigned long long)(0x7FFFFFFF - cost) << 32) | (unsigned)i;
+        }
+        keys[i] = key;
+    }
+    __syncthreads();
+    for (int32_t k = 2; k <= pow2; k <<= 1) {
+        for (int32_t jj = k >> 1; jj > 0; jj >>= 1) {
+            for (int32_t i = threadIdx.x; i < pow2; i += kSchedThreads) {
+                const int32_t l = i ^ jj;
+                if (l > i) {
+                    const unsigned long long x = keys[i], y = keys[l];
+                    const bool up = (i & k) == 0;
+                    if ((x > y) == up) { keys[i] = y; keys[l] = x; }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int32_t i = threadIdx.x; i < n; i += kSchedThreads) sorted[i] = units[(int32_t)(keys[i] & 0xFFFFFFFFu)];
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 3-D bf16 view [outer][mid][D] with a box of {64, 1, rows}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int D, int64_t mid, int64_t outer, int rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)mid, (cuuint64_t)outer};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)(D * 2 * mid)};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D>
+int launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
+    CUtensorMap tq, tk, tv;
+    if (!make_map(&tq, a.q, D, a.hq, a.total_q, kBlockM) ||
+        !make_map(&tk, a.key_cache, D, a.hkv, a.num_blocks * a.block_size, a.block_size) ||
+        !make_map(&tv, a.value_cache, D, a.hkv, a.num_blocks * a.block_size, a.block_size))
+        return PCP_ERR_CUDA;
+    const int smem = Cfg<D>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
+    prefill_kernel<D><<<num_sms(), kThreads, smem, stream>>>(tq, tk, tv, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
+    return PCP_OK;
+}
+
+}  // namespace
+
+int launch_schedule(const PrefillArgs& a, int32_t flags, Unit* units, Unit* units_sorted,
+                    int32_t* header, int32_t* row_ok, int64_t max_units, cudaStream_t stream) {
+    schedule_kernel<<<1, kSchedThreads, 0, stream>>>(a, flags, units, units_sorted, header, row_ok,
+                                                     max_units);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
+    return PCP_OK;
+}
+
+int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+    if (a.d == 64) return launch_prefill_d<64>(a, stream);
+    if (a.d == 128) return launch_prefill_d<128>(a, stream);
+    return PCP_ERR_UNSUPPORTED;
+}
+
+}  // namespace pcp

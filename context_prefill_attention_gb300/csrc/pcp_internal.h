@@ -1,0 +1,87 @@
+// Internal declarations shared by libpcp's translation units (not installed).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pcp.h"
+
+namespace pcp {
+
+// Query tokens per tile and keys per tile of the prefill kernel.
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+// Keys per split of the decode kernel.
+constexpr int kDecodeChunk = 512;
+
+// A unit of prefill work: one 128-token tile of one row, one pass
+// (0 = the whole key range, 1 = first partial, 2 = second partial), and the
+// key range [k_lo, k_hi) it attends. Items are units x head slots.
+struct Unit {
+    int32_t row;
+    int32_t mt_pass;  // mt | pass << 24
+    int32_t k_lo;
+    int32_t k_hi;
+};
+
+// Workspace layout of pcp_attn_varlen (all offsets 256-byte aligned).
+struct WorkspaceLayout {
+    size_t header;        // int32[64]: [0] = number of units
+    size_t row_ok;        // int32[num_rows]: 1 for a row that passed the checks
+    size_t units;         // Unit[max_units], unsorted
+    size_t units_sorted;  // Unit[max_units], longest first
+    size_t part_out[2];   // fp32 [T][Hq][D] each (separate-context mode)
+    size_t part_lse[2];   // fp32 [Hq][T] each
+    size_t dec_out;       // fp32 [num_rows][Hq][max_splits][D]
+    size_t dec_lse;       // fp32 [num_rows][Hq][max_splits]
+    size_t total;
+    int64_t max_units;
+    int32_t max_splits;
+};
+
+WorkspaceLayout workspace_layout(int32_t num_rows, int32_t total_q, int32_t num_q_heads,
+                                 int32_t head_dim, int32_t max_kv_len, int32_t flags);
+
+void set_last_cuda_error(cudaError_t e);
+int num_sms();
+
+struct PrefillArgs {
+    const void* q;
+    const void* key_cache;
+    const void* value_cache;
+    const int32_t* block_table;
+    int32_t num_reqs;
+    int32_t max_blocks;
+    int64_t num_blocks;
+    int32_t block_size;
+    const pcp_row_t* rows;
+    int32_t num_rows;
+    int32_t total_q;
+    int32_t hq, hkv, d;
+    float scale;
+    void* out;
+    float* lse;
+    float* part_out[2];
+    float* part_lse[2];
+    const int32_t* row_ok;
+    const Unit* units;
+    const int32_t* num_units;
+    int32_t* status;
+};
+
+int launch_schedule(const PrefillArgs& a, int32_t flags, Unit* units, Unit* units_sorted,
+                    int32_t* header, int32_t* row_ok, int64_t max_units, cudaStream_t stream);
+int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+int launch_decode(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
+                  cudaStream_t stream);
+int launch_separate_merge(const PrefillArgs& a, cudaStream_t stream);
+int launch_cache_write(const void* k, const void* v, const int64_t* slot, int32_t num_tokens,
+                       int32_t vec_per_tok, void* key_cache, void* value_cache, int64_t num_slots,
+                       int32_t* status, cudaStream_t stream);
+int launch_lse_merge(const float* out_a, const float* lse_a, const float* out_b, const float* lse_b,
+                     void* out, float* lse, int32_t total_q, int32_t hq, int32_t d,
+                     cudaStream_t stream);
+
+}  // namespace pcp

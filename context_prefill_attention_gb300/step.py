@@ -1,0 +1,105 @@
+"""One PCP attention step through the C ABI, with every buffer preallocated.
+
+A step ("Feat/pcp qwen36 hybrid", "Changes"; "[MRv2][PCP] Carry the row plan
+...", sections 1-2 and "What made it removable") is:
+
+1. ``pcp_build_row_plan`` on the host: shard rows and the slot mapping;
+2. the plan (rows, slots) copied to the device from pinned staging buffers;
+3. ``pcp_kv_cache_write``: the new tokens' K/V into the paged cache, ordered
+   before attention on the same stream;
+4. ``pcp_attn_varlen``: prefill, context and decode rows in one call.
+
+This module only sequences those calls and owns the buffers (the reviewer's
+"use the workspace and pass out so we aren't allocating each step").
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import _lib as L
+
+
+class PcpStep:
+    """Preallocated buffers and the call sequence of one PCP step on one GPU."""
+
+    def __init__(self, *, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                 num_shards: int, split_mode: int, max_tokens: int, max_reqs: int, max_kv_len: int,
+                 flags: int = 0, device: str = "cuda"):
+        self.hq, self.hkv, self.d = num_q_heads, num_kv_heads, head_dim
+        self.bs, self.shards, self.split_mode, self.flags = block_size, num_shards, split_mode, flags
+        self.device = torch.device(device)
+        self.max_rows = max(1, 2 * num_shards * max_reqs)
+        self.max_tokens = max_tokens
+        ws = L.pcp_attn_workspace_size(self.max_rows, max_tokens, num_q_heads, head_dim, max_kv_len, flags)
+        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=self.device)
+        self.out = torch.empty((max(max_tokens, 1), num_q_heads, head_dim), dtype=torch.bfloat16,
+                               device=self.device)
+        self.lse_buf = torch.empty(max(max_tokens, 1) * num_q_heads, dtype=torch.float32, device=self.device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.rows_dev = torch.empty((self.max_rows, 8), dtype=torch.int32, device=self.device)
+        self.slot_dev = torch.empty(max(max_tokens, 1), dtype=torch.int64, device=self.device)
+        self.rows_host = torch.empty((self.max_rows, 8), dtype=torch.int32, pin_memory=True)
+        self.slot_host = torch.empty(max(max_tokens, 1), dtype=torch.int64, pin_memory=True)
+        self.plan = None
+
+    def build_plan(self, query_len: Sequence[int], num_computed: Sequence[int], block_table_host) -> dict:
+        self.plan = L.pcp_build_row_plan(query_len, num_computed, block_table_host, self.bs, self.shards,
+                                         self.split_mode, rows_capacity=self.max_rows)
+        return self.plan
+
+    def upload_plan(self, stream=None) -> None:
+        p = self.plan
+        n, T = p["rows"].shape[0], p["slot_mapping"].shape[0]
+        self.rows_host[:n].numpy()[...] = p["rows"]
+        self.slot_host[:T].numpy()[...] = p["slot_mapping"]
+        self.rows_dev[:n].copy_(self.rows_host[:n], non_blocking=True)
+        self.slot_dev[:T].copy_(self.slot_host[:T], non_blocking=True)
+
+    def write_cache(self, k_new: torch.Tensor, v_new: torch.Tensor, key_cache: torch.Tensor,
+                    value_cache: torch.Tensor, stream=None) -> None:
+        T = int(k_new.shape[0])
+        L.pcp_kv_cache_write(k_new, v_new, self.slot_dev[:T], key_cache, value_cache, status=self.status,
+                             stream=stream)
+
+    def attend(self, q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+               block_table_dev: torch.Tensor, scale: float, stream=None):
+        T = int(q.shape[0])
+        n = int(self.plan["rows"].shape[0])
+        out = self.out[:T]
+        lse = self.lse_buf[:T * self.hq].view(self.hq, T)
+        return L.pcp_attn_varlen(q, key_cache, value_cache, block_table_dev, self.rows_dev[:n], scale,
+                                 out=out, lse=lse, workspace=self.workspace, flags=self.flags,
+                                 status=self.status, stream=stream)
+
+    def run(self, q, k_new, v_new, key_cache, value_cache, block_table_dev, scale: float, stream=None):
+        """Steps 2-4 for a plan already built with :meth:`build_plan`."""
+        self.upload_plan(stream)
+        self.write_cache(k_new, v_new, key_cache, value_cache, stream)
+        return self.attend(q, key_cache, value_cache, block_table_dev, scale, stream)
+
+    def check_status(self) -> None:
+        """Raise if a kernel reported an error (synchronises the device)."""
+        s = int(self.status.item())
+        if s != 0:
+            self.status.zero_()
+            raise L.PcpError(s, "device status")
+
+
+def write_positions(key_cache: torch.Tensor, value_cache: torch.Tensor, block_table_host,
+                    start: Sequence[int], k_list, v_list, block_size: int,
+                    status: Optional[torch.Tensor] = None) -> None:
+    """Write K/V rows of positions ``[start[r], start[r] + len)`` of every request
+    into the paged cache, through the library's own plan (one shard) and cache
+    writer — what earlier steps of a real engine would have left in the cache."""
+    lens = [int(k.shape[0]) for k in k_list]
+    if sum(lens) == 0:
+        return
+    plan = L.pcp_build_row_plan(lens, list(start), block_table_host, block_size, 1, L.PCP_SPLIT_CONTIGUOUS)
+    dev = key_cache.device
+    slot = torch.from_numpy(plan["slot_mapping"]).to(dev)
+    k = torch.cat([x.to(dev) for x in k_list], 0)
+    v = torch.cat([x.to(dev) for x in v_list], 0)
+    L.pcp_kv_cache_write(k, v, slot, key_cache, value_cache, status=status)

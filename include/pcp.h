@@ -1,0 +1,233 @@
+/*
+ * pcp.h — C ABI of libpcp: Prefill Context Parallel (PCP) attention for GQA/MHA
+ * layers on NVIDIA GB300 (sm_103a).
+ *
+ * The method, as the three pull-request pages on PCP for vLLM describe it:
+ *  - "Feat/pcp qwen36 hybrid", section "Changes": each PCP rank takes a
+ *    contiguous slice of the prompt; full-attention layers all-gather K/V and
+ *    run end-aligned (bottom-right) causal attention of the slice against it.
+ *  - "[MRv2] FlashAttention PCP support for GQA on MRv2", "Pull request
+ *    overview": an optional cached-prefix (context) pass returning
+ *    (ctx_out, ctx_lse) merged with the new-token pass by log-sum-exp; mixed
+ *    prefill + decode batches; a PCP-aware KV-cache update. Review: callers
+ *    pass the output and a workspace so nothing is allocated per step.
+ *  - "[MRv2][PCP] Carry the row plan in attention metadata; fix mixed
+ *    prefill+decode crash": a rank-local batch holds up to two rows per
+ *    prefilling request (section 2); the gathered slot mapping masks every
+ *    entry a rank must not write with a negative PAD slot and the cache writer
+ *    skips negative slots, decode rows being written by rank 0 only (commit
+ *    "drop pcp_has_prefill"); a row's seq_len is its end position, so
+ *    seq_len - query_len is the row start ("What made it removable").
+ *
+ * On one GPU the PCP ranks are emulated as query shards of one batch and the
+ * all-gathered K/V is the resident paged cache, so no call here communicates.
+ *
+ * Conventions for every function:
+ *  - The return value is a status: PCP_OK (0) or a negative PCP_ERR_* code.
+ *    No function aborts, throws or prints.
+ *  - Arguments are validated on the host before anything is launched; an
+ *    invalid call launches nothing and leaves every buffer untouched.
+ *  - Device functions are asynchronous on `stream` (0 = the legacy default
+ *    stream). The caller owns every buffer and the stream; the library
+ *    allocates no device memory in any call.
+ *  - `status` (where present) is a device int32 that the kernels set with the
+ *    first error they meet (PCP_ERR_RANGE for an out-of-range block id or
+ *    slot, PCP_ERR_TIMEOUT for a bounded wait that ran out). It is never reset
+ *    by the library: zero it before the call, read it after synchronising.
+ *  - bf16 tensors are raw 16-bit IEEE bfloat16; pointers named *_cache and the
+ *    q/k/v/out tensors must be 16-byte aligned (PCP_ERR_ALIGN otherwise).
+ *
+ * Layouts (T = total new tokens, packed request-major, positions ascending):
+ *  q, out        [T][Hq][D]                 bf16
+ *  k, v (new)    [T][Hkv][D]                bf16
+ *  key_cache,
+ *  value_cache   [num_blocks][block_size][Hkv][D]  bf16 (the paged cache)
+ *  block_table   [num_reqs][max_blocks_per_req]    int32 page ids, row-major
+ *  lse           [Hq][T]                    fp32, natural log
+ *  slot_mapping  [T]                        int64, slot = page * block_size + offset
+ * q head h reads kv head h / (Hq / Hkv).
+ */
+#ifndef PCP_H_
+#define PCP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pcp_stream_t; /* == cudaStream_t */
+
+/* status codes */
+#define PCP_OK 0
+#define PCP_ERR_ARG (-1)         /* null pointer, negative or inconsistent size */
+#define PCP_ERR_RANGE (-2)       /* page id, slot or row range out of range */
+#define PCP_ERR_UNSUPPORTED (-3) /* head_dim, block_size or head ratio not supported */
+#define PCP_ERR_ALIGN (-4)       /* pointer not 16-byte aligned */
+#define PCP_ERR_CUDA (-5)        /* a CUDA call failed; see pcp_last_cuda_error() */
+#define PCP_ERR_TIMEOUT (-6)     /* a bounded device wait ran out (reported via status) */
+#define PCP_ERR_WORKSPACE (-7)   /* workspace missing or too small */
+
+/* split modes of pcp_build_row_plan */
+#define PCP_SPLIT_CONTIGUOUS 0
+#define PCP_SPLIT_DUAL_CHUNK 1
+
+/* flags of pcp_attn_varlen */
+#define PCP_ATTN_SEPARATE_CONTEXT 1  /* compute the context and new-token parts as two
+                                        partials in the workspace and merge them by LSE */
+#define PCP_ATTN_SPLIT_AT_ROW_START 2 /* with SEPARATE_CONTEXT: split each row at its own
+                                        start instead of at the cached prefix */
+
+/* One row of the plan: a contiguous run of one request's new tokens that one
+ * shard evaluates. All fields are int32.
+ *  req        request index
+ *  shard      emulated PCP rank that owns the row
+ *  q_start    packed index of the row's first token in q / out / k / v
+ *  q_len      number of query tokens (> 0)
+ *  ctx_len    cached prefix length of the request (keys [0, ctx_len) are the context)
+ *  kv_end     end position of the row = ctx_len + (row end within the request's new tokens);
+ *             the row's query j sits at position kv_end - q_len + j and sees keys
+ *             [0, kv_end - q_len + j] (end-aligned causal)
+ *  causal_off kv_end - ctx_len - q_len: the row start among the request's new tokens
+ *  is_decode  1 for a single new token after a non-empty prefix */
+typedef struct pcp_row_t {
+    int32_t req, shard, q_start, q_len, ctx_len, kv_end, causal_off, is_decode;
+} pcp_row_t;
+
+/*
+ * pcp_build_row_plan — host function, pure and deterministic.
+ * ("Feat/pcp qwen36 hybrid", "Changes"; "Carry the row plan ...", section 2 and
+ * "What made it removable"; "drop pcp_has_prefill".)
+ *
+ * Request r has query_len[r] >= 0 new tokens after num_computed[r] >= 0 cached
+ * ones. Its new tokens are cut into shard rows:
+ *   PCP_SPLIT_CONTIGUOUS  shard i gets [floor(i N / S), floor((i+1) N / S));
+ *   PCP_SPLIT_DUAL_CHUNK  2S chunks [floor(k N / 2S), floor((k+1) N / 2S)); shard i
+ *                         gets chunk i and chunk 2S-1-i (head and tail);
+ * a request with one new token is a single row on shard 0; empty chunks give no
+ * row. Rows are written shard-major: shard, then request, then chunk order.
+ *
+ * Inputs (host memory): query_len[num_reqs], num_computed[num_reqs],
+ *   block_table[num_reqs][max_blocks_per_req] (only the pages holding new tokens are read).
+ * Outputs (host memory, caller-allocated):
+ *   rows[rows_capacity]     rows_capacity >= 2 * num_shards * num_reqs always suffices
+ *   *num_rows
+ *   cu_q[*num_rows + 1]     running sum of q_len over rows (size it rows_capacity + 1)
+ *   slot_mapping[T]         slot of every new token: block_table[r][pos / bs] * bs + pos % bs
+ *   owner_shard[T]          shard of the row holding each token; may be NULL
+ * Errors: PCP_ERR_ARG (null pointer, negative length, num_shards < 1 or > 127,
+ *   bad split mode, block_size < 1); PCP_ERR_RANGE (a needed page is negative or
+ *   beyond max_blocks_per_req, or the rows do not fit rows_capacity). Outputs are
+ *   unspecified after an error.
+ */
+int pcp_build_row_plan(int32_t num_reqs, const int32_t* query_len, const int32_t* num_computed,
+                       const int32_t* block_table, int32_t max_blocks_per_req, int32_t block_size,
+                       int32_t num_shards, int32_t split_mode, pcp_row_t* rows,
+                       int32_t rows_capacity, int32_t* num_rows, int32_t* cu_q,
+                       int64_t* slot_mapping, int8_t* owner_shard);
+
+/*
+ * pcp_mask_slots_for_shard — host function. The PAD-masked slot mapping one
+ * rank hands to its cache writer ("drop pcp_has_prefill"): out[t] = slot[t]
+ * where owner_shard[t] == shard, else -1. slot/owner/out are host arrays of
+ * num_tokens entries; out may alias slot. Errors: PCP_ERR_ARG.
+ */
+int pcp_mask_slots_for_shard(const int64_t* slot_mapping, const int8_t* owner_shard,
+                             int32_t num_tokens, int32_t shard, int64_t* out);
+
+/*
+ * pcp_kv_cache_write — device. Scatter the new tokens' K and V into the paged
+ * cache: key_cache[slot / bs][slot % bs][h][:] = k[t][h][:] (same for V) for every
+ * t with slot_mapping[t] >= 0; negative slots are skipped ("drop
+ * pcp_has_prefill"). The write must precede the attention of the same step
+ * ("What made it removable": the cache update is ordered before attention);
+ * issuing both on one stream does that.
+ * k, v, slot_mapping, key_cache, value_cache, status: device pointers.
+ * A slot >= num_blocks * block_size is skipped and sets *status = PCP_ERR_RANGE.
+ * Supported: head_dim * 2 bytes a multiple of 16. Errors: PCP_ERR_ARG,
+ * PCP_ERR_ALIGN, PCP_ERR_UNSUPPORTED, PCP_ERR_CUDA (launch failure).
+ */
+int pcp_kv_cache_write(const void* k, const void* v, const int64_t* slot_mapping,
+                       int32_t num_tokens, void* key_cache, void* value_cache, int64_t num_blocks,
+                       int32_t block_size, int32_t num_kv_heads, int32_t head_dim, int32_t* status,
+                       pcp_stream_t stream);
+
+/*
+ * pcp_attn_workspace_size — bytes of device workspace pcp_attn_varlen needs.
+ * max_kv_len is the key capacity of a block-table row
+ * (max_blocks_per_req * block_size). Never fails; returns 0 for invalid sizes.
+ */
+size_t pcp_attn_workspace_size(int32_t num_rows, int32_t total_q, int32_t num_q_heads,
+                               int32_t head_dim, int32_t max_kv_len, int32_t flags);
+
+/*
+ * pcp_attn_varlen — device. Attention of every planned row in one call:
+ * prefill rows (end-aligned causal over the new tokens, plus the non-causal
+ * context over the cached prefix) on the tensor cores, decode rows on a
+ * split-KV bandwidth path. ("Feat/pcp qwen36 hybrid", "Changes"; "[MRv2]
+ * FlashAttention PCP support ...", overview and the context-pass call returning
+ * (ctx_out, ctx_lse); "Carry the row plan ...", "What made it removable".)
+ *
+ * For query j of a row (position p = kv_end - q_len + j) and q head h:
+ *   s_k   = scale * q[t][h] . K[req][k][h / G]           for keys k in [0, p]
+ *   out   = sum_k softmax(s)_k V[req][k][h / G]          (bf16, rounded from fp32)
+ *   lse   = log sum_k exp(s_k)                            (fp32, natural log)
+ * K/V are read from the paged cache through block_table[req].
+ *
+ * q, key_cache, value_cache, block_table ([num_reqs][max_blocks_per_req]), rows,
+ * out, lse, workspace, status: device pointers. rows[num_rows] is the plan (any
+ * row order; the q ranges must be disjoint). The kernels check every row
+ * (0 <= req < num_reqs, q_len >= 1, [q_start, q_start + q_len) inside
+ * [0, total_q), q_len <= kv_end <= max_blocks_per_req * block_size,
+ * 0 <= ctx_len <= kv_end, a decode row has q_len == 1) and skip a bad row with
+ * *status = PCP_ERR_RANGE. Tokens not covered by any row are
+ * not written (padding is never computed). workspace: at least
+ * pcp_attn_workspace_size(num_rows, total_q, Hq, D, max_blocks_per_req * block_size, flags)
+ * bytes, 256-byte aligned; its contents on entry do not matter.
+ * flags: 0 computes every row in one online softmax; PCP_ATTN_SEPARATE_CONTEXT
+ * computes the context part and the new-token part as two partial results in
+ * the workspace and merges them by LSE (a part with no keys has lse = -inf and
+ * out = 0); PCP_ATTN_SPLIT_AT_ROW_START moves the split point to the row start.
+ * Supported: head_dim 64 or 128, block_size in {16, 32, 64, 128}, Hq % Hkv == 0.
+ * Rows with an out-of-range page id are skipped in part and set *status =
+ * PCP_ERR_RANGE; a device wait that runs out sets PCP_ERR_TIMEOUT.
+ * Errors (nothing launched): PCP_ERR_ARG, PCP_ERR_ALIGN, PCP_ERR_UNSUPPORTED,
+ * PCP_ERR_WORKSPACE; PCP_ERR_CUDA for a failed launch.
+ */
+int pcp_attn_varlen(const void* q, const void* key_cache, const void* value_cache,
+                    const int32_t* block_table, int32_t num_reqs, int32_t max_blocks_per_req,
+                    int64_t num_blocks,
+                    int32_t block_size, const pcp_row_t* rows, int32_t num_rows, int32_t total_q,
+                    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
+                    void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t flags,
+                    int32_t* status, pcp_stream_t stream);
+
+/*
+ * pcp_lse_merge — device. Merge two partial results of the same queries by
+ * log-sum-exp ("[MRv2] FlashAttention PCP support ...": (ctx_out, ctx_lse)
+ * combined with the new-token pass; the per-step LSE-combine of the DCP
+ * benchmark):
+ *   m = max(lse_a, lse_b), w_x = exp(lse_x - m),
+ *   out = (w_a out_a + w_b out_b) / (w_a + w_b), lse = m + log(w_a + w_b);
+ * a part with lse = -inf contributes nothing; both -inf give out = 0, lse = -inf.
+ * out_a, out_b: [total_q][Hq][D] fp32; lse_a, lse_b, lse: [Hq][total_q] fp32;
+ * out: [total_q][Hq][D] bf16. All device pointers; lse must not alias lse_a or lse_b
+ * (PCP_ERR_ARG). Errors: PCP_ERR_ARG, PCP_ERR_ALIGN, PCP_ERR_UNSUPPORTED (head_dim % 8 != 0),
+ * PCP_ERR_CUDA.
+ */
+int pcp_lse_merge(const float* out_a, const float* lse_a, const float* out_b, const float* lse_b,
+                  void* out, float* lse, int32_t total_q, int32_t num_q_heads, int32_t head_dim,
+                  pcp_stream_t stream);
+
+/* The cudaError_t value of the last failed CUDA call in this thread (0 if none). */
+int pcp_last_cuda_error(void);
+
+/* A short static description of a status code. */
+const char* pcp_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PCP_H_ */

@@ -1,0 +1,160 @@
+"""The C-ABI library on the host (no GPU needed): it loads, exports every
+function include/pcp.h declares, its host row plan matches the oracle bit for
+bit, and invalid arguments are refused before anything is launched."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def P():
+    from context_prefill_attention_gb300 import build
+    build.build()
+    import context_prefill_attention_gb300 as P
+    P.load()
+    return P
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "pcp.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pcp_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(P):
+    lib = P.load()
+    names = _declared()
+    assert "pcp_attn_varlen" in names and "pcp_build_row_plan" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(P.EXPORTS)
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_host_plan_matches_oracle_random(P, seed):
+    rng = np.random.default_rng(100 + seed)
+    R = int(rng.integers(1, 12))
+    S = int(rng.integers(1, 6))
+    mode = int(rng.integers(0, 2))
+    bs = int(rng.choice([1, 4, 16, 32]))
+    ql = [int(rng.choice([0, 1, 1, 2, 5, 31, 128, 1000])) for _ in range(R)]
+    nc = [int(rng.integers(0, 3000)) for _ in range(R)]
+    need = [-(-(p + n) // bs) for p, n in zip(nc, ql)]
+    pool = rng.permutation(sum(need) + 3)
+    bt = np.full((R, max(1, max(need))), -1, dtype=np.int32)
+    o = 0
+    for r, k in enumerate(need):
+        bt[r, :k] = pool[o:o + k]
+        o += k
+    a = P.pcp_build_row_plan(ql, nc, bt, bs, S, mode)
+    b = oracle.row_plan(ql, nc, bt, bs, S, mode)
+    np.testing.assert_array_equal(a["rows"], b["rows"])
+    np.testing.assert_array_equal(a["cu_q"], b["cu_q"])
+    np.testing.assert_array_equal(a["slot_mapping"], b["slot"])
+    np.testing.assert_array_equal(a["owner_shard"], b["owner"])
+
+
+@pytest.mark.parametrize("workload,mode", [(1, 0), (2, 0), (2, 1), (3, 0), (4, 0), (5, 0)])
+def test_host_plan_matches_oracle_workloads(P, workload, mode):
+    spec = W.workload_spec(workload, split_mode=mode)
+    bt, _ = W.block_tables(spec)
+    a = P.pcp_build_row_plan(spec.query_len, spec.num_computed, bt, spec.block_size, spec.num_shards, mode)
+    b = oracle.row_plan(spec.query_len, spec.num_computed, bt.numpy(), spec.block_size, spec.num_shards, mode)
+    np.testing.assert_array_equal(a["rows"], b["rows"])
+    np.testing.assert_array_equal(a["slot_mapping"], b["slot"])
+    np.testing.assert_array_equal(a["owner_shard"], b["owner"])
+
+
+def test_host_plan_errors(P):
+    with pytest.raises(P.PcpError) as e:
+        P.pcp_build_row_plan([5], [0], np.array([[1, -1, -1]], np.int32), 2, 1)
+    assert e.value.code == P.PCP_ERR_RANGE
+    with pytest.raises(P.PcpError) as e:
+        P.pcp_build_row_plan([5, 5], [0, 0], np.array([[0, 1, 2], [3, 4, 5]], np.int32), 2, 2, rows_capacity=3)
+    assert e.value.code == P.PCP_ERR_RANGE
+    with pytest.raises(P.PcpError) as e:
+        P.pcp_build_row_plan([5], [0], np.array([[0, 1, 2]], np.int32), 2, 0)
+    assert e.value.code == P.PCP_ERR_ARG
+    with pytest.raises(P.PcpError) as e:
+        P.pcp_build_row_plan([-1], [0], np.array([[0]], np.int32), 2, 1)
+    assert e.value.code == P.PCP_ERR_ARG
+
+
+def test_mask_slots_for_shard(P):
+    spec = W.custom_spec([10, 1, 7], [0, 5, 2], num_q_heads=2, num_kv_heads=1, head_dim=8, block_size=4,
+                         num_shards=3)
+    bt, _ = W.block_tables(spec)
+    plan = P.pcp_build_row_plan(spec.query_len, spec.num_computed, bt, 4, 3)
+    seen = np.zeros(spec.total_q, dtype=int)
+    for s in range(3):
+        m = P.pcp_mask_slots_for_shard(plan["slot_mapping"], plan["owner_shard"], s)
+        own = plan["owner_shard"] == s
+        np.testing.assert_array_equal(m[own], plan["slot_mapping"][own])
+        assert np.all(m[~own] == -1)
+        seen += own
+    assert np.all(seen == 1)
+    # the decode token (request 1) is written by shard 0 only
+    assert plan["owner_shard"][10] == 0
+
+
+FAKE = 0x10000  # a 256-byte aligned address that is never dereferenced
+
+
+def _attn(lib, **kw):
+    args = dict(q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, nreq=1, mb=4, nb=64, bs=16, rows=FAKE, nrows=2, T=100,
+                hq=8, hkv=2, d=128, scale=0.1, out=FAKE, lse=FAKE, ws=FAKE, wsb=1 << 30, flags=0, status=None)
+    args.update(kw)
+    P_ = ctypes.c_void_p
+    return lib.pcp_attn_varlen(P_(args["q"]), P_(args["kc"]), P_(args["vc"]), P_(args["bt"]), args["nreq"],
+                               args["mb"], args["nb"], args["bs"], P_(args["rows"]), args["nrows"], args["T"],
+                               args["hq"], args["hkv"], args["d"], args["scale"], P_(args["out"]), P_(args["lse"]),
+                               P_(args["ws"]), args["wsb"], args["flags"], args["status"], None)
+
+
+def test_attn_varlen_validates_before_launch(P):
+    lib = P.load()
+    assert _attn(lib, d=96) == P.PCP_ERR_UNSUPPORTED
+    assert _attn(lib, hq=6, hkv=4) == P.PCP_ERR_UNSUPPORTED
+    assert _attn(lib, bs=12) == P.PCP_ERR_UNSUPPORTED
+    assert _attn(lib, hq=64, hkv=2) == P.PCP_ERR_UNSUPPORTED
+    assert _attn(lib, q=None) == P.PCP_ERR_ARG
+    assert _attn(lib, nrows=-1) == P.PCP_ERR_ARG
+    assert _attn(lib, flags=8) == P.PCP_ERR_ARG
+    assert _attn(lib, q=FAKE + 8) == P.PCP_ERR_ALIGN
+    assert _attn(lib, ws=FAKE + 16) == P.PCP_ERR_ALIGN
+    assert _attn(lib, wsb=100) == P.PCP_ERR_WORKSPACE
+    assert _attn(lib, nb=1 << 28) == P.PCP_ERR_ARG
+    assert _attn(lib, nrows=0) == P.PCP_OK          # nothing to do, nothing launched
+    need = P.pcp_attn_workspace_size(2, 100, 8, 128, 64, 0)
+    assert need > 0 and P.pcp_attn_workspace_size(2, 100, 8, 128, 64, 1) > need
+    assert P.pcp_attn_workspace_size(-1, 100, 8, 128, 64, 0) == 0
+
+
+def test_cache_write_and_merge_validate_before_launch(P):
+    lib = P.load()
+    V = ctypes.c_void_p
+    # every call below fails a host check, so nothing is launched on a fake pointer
+    assert lib.pcp_kv_cache_write(V(FAKE + 4), V(FAKE), V(FAKE), 10, V(FAKE), V(FAKE), 8, 16, 2, 128, None,
+                                  None) == P.PCP_ERR_ALIGN
+    assert lib.pcp_kv_cache_write(None, V(FAKE), V(FAKE), 10, V(FAKE), V(FAKE), 8, 16, 2, 128, None,
+                                  None) == P.PCP_ERR_ARG
+    assert lib.pcp_kv_cache_write(V(FAKE), V(FAKE), V(FAKE), 10, V(FAKE), V(FAKE), 8, 16, 1, 3, None,
+                                  None) == P.PCP_ERR_UNSUPPORTED
+    assert lib.pcp_kv_cache_write(V(FAKE), V(FAKE), V(FAKE), 0, V(FAKE), V(FAKE), 8, 16, 2, 128, None,
+                                  None) == P.PCP_OK
+    assert lib.pcp_lse_merge(V(FAKE), V(FAKE), V(FAKE), V(FAKE), V(FAKE), V(FAKE), 4, 2, 12, None) \
+        == P.PCP_ERR_UNSUPPORTED
+    assert lib.pcp_lse_merge(V(FAKE), V(FAKE), V(FAKE), V(FAKE), V(FAKE), V(FAKE), 4, 2, 128, None) \
+        == P.PCP_ERR_ARG   # lse aliases lse_a
+    assert lib.pcp_lse_merge(V(FAKE + 4), V(FAKE), V(FAKE), V(FAKE + 512), V(FAKE), V(FAKE + 1024), 4, 2, 128,
+                             None) == P.PCP_ERR_ALIGN
+    assert lib.pcp_status_string(P.PCP_ERR_TIMEOUT) == b"device wait timed out"
