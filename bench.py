@@ -1,0 +1,361 @@
+"""Benchmark of one PCP attention step on GB300 (prints one JSON line).
+
+A step is the whole hot path over one batch: the host row plan, its upload,
+the KV-cache write of the new tokens, and attention of every row (prefill,
+cached-prefix context and decode rows) through the C ABI. The default workload
+is the mixed prefill + decode batch (8 prompts of U[1024,8192] tokens in 2
+shard rows each plus 56 decode rows with U[1024,16384] keys, 32 q / 8 kv heads,
+D=128): the one workload on which both halves of the metric (prefill TFLOP/s
+and decode-row HBM GB/s) are defined.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
+    python bench.py --impl reference     # the CPU oracle on a bounded sample
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(no data-path collective); rank 0 prints the line, value = all ranks' work /
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "prefill attn TFLOP/s (% BF16 peak); decode-row HBM GB/s (% peak)"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    """Largest value of x over all ranks (identity for one rank)."""
+    if ws <= 1:
+        return x
+    import torch.distributed as dist
+    backend = dist.get_backend()
+    dev = "cuda" if backend == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int) -> None:
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def plan_work(rows: np.ndarray, hq: int, hkv: int, d: int):
+    """Algorithmic work of a plan: prefill FLOPs (4 D Hq per unmasked query-key
+    pair), decode FLOPs and decode bytes (K and V of every visible key once per
+    kv head, plus q, out and lse)."""
+    r = rows.astype(np.int64)
+    ql, end = r[:, 3], r[:, 5]
+    dec = r[:, 7] == 1
+    pairs = ql * (end - ql) + ql * (ql + 1) // 2
+    pre_pairs = int(pairs[~dec].sum())
+    dec_keys = int(end[dec].sum())
+    n_dec = int(dec.sum())
+    return dict(prefill_flop=4.0 * d * hq * pre_pairs, decode_flop=4.0 * d * hq * dec_keys,
+                decode_bytes=float(dec_keys * hkv * d * 2 * 2 + n_dec * (hq * d * 2 * 2 + hq * 4)),
+                pairs=pre_pairs + dec_keys)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.samples, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def setup(workload: int, device: str, flags: int):
+    import context_prefill_attention_gb300 as P
+    P.load()
+    spec = W.workload_spec(workload)
+    bt, nb = W.block_tables(spec)
+    shape = (nb, spec.block_size, spec.num_kv_heads, spec.head_dim)
+    kc = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+    vc = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+    prefix = [r for r in range(spec.num_reqs) if spec.num_computed[r] > 0]
+    for r in prefix:  # contexts an earlier step would have left in the cache
+        P.write_positions(kc, vc, bt[r:r + 1].numpy(), [0], [W.request_tensor(spec, r, W.KIND_KP, device)],
+                          [W.request_tensor(spec, r, W.KIND_VP, device)], spec.block_size)
+    q = W.packed_new_tokens(spec, W.KIND_Q, device)
+    k = W.packed_new_tokens(spec, W.KIND_K, device)
+    v = W.packed_new_tokens(spec, W.KIND_V, device)
+    step = P.PcpStep(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                     block_size=spec.block_size, num_shards=spec.num_shards, split_mode=spec.split_mode,
+                     max_tokens=spec.total_q, max_reqs=spec.num_reqs, max_kv_len=bt.shape[1] * spec.block_size,
+                     flags=flags, device=device)
+    return P, spec, bt, bt.to(device), kc, vc, q, k, v, step
+
+
+def run_gpu(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    P, spec, bt, bt_dev, kc, vc, q, k, v, step = setup(args.workload, device, args.flags)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def one_step():
+        step.build_plan(spec.query_len, spec.num_computed, bt)
+        return step.run(q, k, v, kc, vc, bt_dev, spec.scale, stream)
+
+    plan = step.build_plan(spec.query_len, spec.num_computed, bt)
+    work = plan_work(plan["rows"], spec.num_q_heads, spec.num_kv_heads, spec.head_dim)
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    step.check_status()
+
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [[mk() for _ in range(6)] for _ in range(args.steps)]
+    for e in ev:
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)  # L2 flush between timed steps, outside the timed window
+            P.pcp_set_profile_events(ev[i][2], ev[i][3], ev[i][4], ev[i][5])
+            ev[i][0].record(stream)
+            one_step()
+            ev[i][1].record(stream)
+        P.pcp_set_profile_events()
+        torch.cuda.synchronize()
+    barrier(ws)
+    step.check_status()
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    pre_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    dec_ms = [e[4].elapsed_time(e[5]) for e in ev]
+    total_ms = max_over_ranks(sum(step_ms), ws)
+    ms = total_ms / args.steps
+    step_flop = work["prefill_flop"] + work["decode_flop"]
+    value = ws * step_flop / (ms * 1e-3) / 1e12
+
+    # end to end: host inputs in pinned memory, copies inside the timed region
+    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+    out_h = torch.empty((spec.total_q, spec.num_q_heads, spec.head_dim), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((spec.num_q_heads, spec.total_q), dtype=torch.float32).pin_memory()
+    e2e_ms = []
+    for i in range(max(3, args.steps // 2)):
+        flush.fill_(i & 0xFF)
+        s0, s1 = mk(), mk()
+        s0.record(stream)
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        out, lse = one_step()
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(s0.elapsed_time(s1))
+    e2e = max_over_ranks(statistics.mean(e2e_ms), ws)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv)) + plan["rows"].nbytes + plan["slot_mapping"].nbytes
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+    peaks = load_peaks()
+    pre_avg = statistics.mean(pre_ms)
+    dec_avg = statistics.mean(dec_ms)
+    achieved = work["prefill_flop"] / (pre_avg * 1e-3) / 1e12
+    dec_gbs = work["decode_bytes"] / (dec_avg * 1e-3) / 1e9 if work["decode_bytes"] > 0 and dec_avg > 0 else None
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded torch.randn, bf16)",
+        "config": {"workload": spec.name, "rows": int(plan["rows"].shape[0]), "total_q": spec.total_q,
+                   "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
+                   "head_dim": spec.head_dim, "block_size": spec.block_size, "num_shards": spec.num_shards,
+                   "flags": args.flags, "l2": "flushed (512 MiB write) between timed steps",
+                   "parallelism": f"replicas x{ws}"},
+        "prefill": {"tflops": round(achieved, 2), "ms": round(pre_avg, 4),
+                    "frac_bf16_peak": round(achieved / peaks["bf16"], 4), "flop": work["prefill_flop"]},
+        "decode": {"gbs": None if dec_gbs is None else round(dec_gbs, 1), "ms": round(dec_avg, 4),
+                   "frac_hbm_peak": None if dec_gbs is None else round(dec_gbs / peaks["hbm"], 4),
+                   "bytes": work["decode_bytes"]},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16"],
+                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4), "traffic": None,
+                     "kernel": "prefill_kernel", "peak_source": f"{peaks['source']} bf16 burst"},
+        "e2e": {"value": round(ws * step_flop / (e2e * 1e-3) / 1e12, 3), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e, 4)},
+        "gpu_launches": args.steps * (5 + (1 if args.flags & 1 else 0)),
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(spec, bt, target_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def _oracle_sample(spec, bt, target_s: float, seed: int):
+    """Run the oracle on a seeded sample of the workload's query tokens, sized to
+    take about target_s seconds; returns (seconds, flop of the sample, description)."""
+    import oracle
+    rows = oracle.row_plan(spec.query_len, spec.num_computed, bt.numpy(), spec.block_size, spec.num_shards,
+                           spec.split_mode)["rows"]
+    q = W.packed_new_tokens(spec, W.KIND_Q)
+    kfull, vfull = zip(*[W.full_kv(spec, r) for r in range(spec.num_reqs)])
+    kv_off = np.cumsum([0] + [k.shape[0] for k in kfull[:-1]])
+    kk, vv = torch.cat(kfull, 0), torch.cat(vfull, 0)
+    rng = np.random.default_rng(seed)
+    tok_rows = [(int(r[2]), int(r[3]), int(r[5])) for r in rows]   # (q_start, q_len, kv_end)
+    all_tok = np.concatenate([np.arange(s, s + n) for s, n, _ in tok_rows])
+    keys_of = np.concatenate([np.arange(e - n + 1, e + 1) for s, n, e in tok_rows])
+    order = rng.permutation(all_tok.shape[0])
+    n = 8
+    while True:
+        sel = order[:n]
+        t0 = time.time()
+        oracle.attention(rows, q, kk, vv, kv_off, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.scale,
+                         all_tok[sel])
+        dt = time.time() - t0
+        flop = 4.0 * spec.head_dim * spec.num_q_heads * float(keys_of[sel].sum())
+        if dt >= target_s * 0.5 or n >= all_tok.shape[0]:
+            return dt, flop, f"{n} seeded random query tokens of {all_tok.shape[0]} (all heads)"
+        n = min(all_tok.shape[0], int(n * max(2.0, min(16.0, target_s / max(dt, 1e-3)))))
+
+
+def cpu_baseline(spec, bt, target_s: float = 15.0):
+    import oracle
+    oracle.build()
+    dt, flop, desc = _oracle_sample(spec, bt, target_s, spec.seed + 99)
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": round(flop / dt / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": desc + f", fp64, {dt:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    spec = W.workload_spec(args.workload)
+    bt, _ = W.block_tables(spec)
+    per_step = max(1.0, args.ref_seconds / (args.steps + args.warmup))
+    for i in range(args.warmup):
+        _oracle_sample(spec, bt, per_step, spec.seed + 1000 + i)
+    tot_t, tot_f, desc = 0.0, 0.0, ""
+    for i in range(args.steps):
+        dt, flop, desc = _oracle_sample(spec, bt, per_step, spec.seed + 2000 + i)
+        tot_t += dt
+        tot_f += flop
+    value = tot_f / tot_t / 1e12
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded torch.randn, bf16)",
+            "config": {"workload": spec.name, "total_q": spec.total_q, "num_q_heads": spec.num_q_heads,
+                       "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"per step: {desc}"},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=4)
+    ap.add_argument("--flags", type=int, default=0)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "native":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

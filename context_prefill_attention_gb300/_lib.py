@@ -32,8 +32,8 @@ ROW_FIELDS = ("req", "shard", "q_start", "q_len", "ctx_len", "kv_end", "causal_o
 
 # every symbol include/pcp.h declares
 EXPORTS = ("pcp_build_row_plan", "pcp_mask_slots_for_shard", "pcp_kv_cache_write",
-           "pcp_attn_workspace_size", "pcp_attn_varlen", "pcp_lse_merge", "pcp_last_cuda_error",
-           "pcp_status_string")
+           "pcp_attn_workspace_size", "pcp_attn_varlen", "pcp_lse_merge", "pcp_set_profile_events",
+           "pcp_last_cuda_error", "pcp_status_string")
 
 _lib = None
 
@@ -74,6 +74,8 @@ def load(path: Optional[str] = None):
     lib.pcp_attn_varlen.restype = ctypes.c_int
     lib.pcp_lse_merge.argtypes = [P, P, P, P, P, P, i32, i32, i32, P]
     lib.pcp_lse_merge.restype = ctypes.c_int
+    lib.pcp_set_profile_events.argtypes = [P, P, P, P]
+    lib.pcp_set_profile_events.restype = ctypes.c_int
     lib.pcp_last_cuda_error.argtypes = []
     lib.pcp_last_cuda_error.restype = ctypes.c_int
     lib.pcp_status_string.argtypes = [ctypes.c_int]
@@ -198,3 +200,12 @@ def pcp_lse_merge(out_a: torch.Tensor, lse_a: torch.Tensor, out_b: torch.Tensor,
                            T, hq, d, _stream(stream))
     _check(rc, "pcp_lse_merge")
     return out, lse
+
+
+def pcp_set_profile_events(prefill_begin=None, prefill_end=None, decode_begin=None, decode_end=None) -> None:
+    """Register ``torch.cuda.Event`` objects (already recorded once, so that they
+    exist) to be recorded around the prefill and decode kernels of later
+    :func:`pcp_attn_varlen` calls in this thread; no arguments unregisters."""
+    def h(e):
+        return None if e is None else ctypes.c_void_p(int(e.cuda_event))
+    load().pcp_set_profile_events(h(prefill_begin), h(prefill_end), h(decode_begin), h(decode_end))

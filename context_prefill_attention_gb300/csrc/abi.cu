@@ -12,6 +12,8 @@ namespace pcp {
 
 namespace {
 thread_local int g_last_cuda_error = 0;
+// Events recorded around the prefill and decode launches when set (profiling hook).
+thread_local cudaEvent_t g_profile[4] = {nullptr, nullptr, nullptr, nullptr};
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -172,13 +174,26 @@ extern "C" int pcp_attn_varlen(const void* q, const void* key_cache, const void*
                              reinterpret_cast<int32_t*>(ws + w.header),
                              reinterpret_cast<int32_t*>(ws + w.row_ok), w.max_units, s);
     if (rc != PCP_OK) return rc;
+    if (g_profile[2]) cudaEventRecord(g_profile[2], s);
     rc = launch_decode(a, reinterpret_cast<float*>(ws + w.dec_out), reinterpret_cast<float*>(ws + w.dec_lse),
                        w.max_splits, s);
     if (rc != PCP_OK) return rc;
+    if (g_profile[3]) cudaEventRecord(g_profile[3], s);
+    if (g_profile[0]) cudaEventRecord(g_profile[0], s);
     rc = launch_prefill(a, s);
     if (rc != PCP_OK) return rc;
+    if (g_profile[1]) cudaEventRecord(g_profile[1], s);
     if (flags & PCP_ATTN_SEPARATE_CONTEXT) rc = launch_separate_merge(a, s);
     return rc;
+}
+
+extern "C" int pcp_set_profile_events(void* prefill_begin, void* prefill_end, void* decode_begin,
+                                      void* decode_end) {
+    g_profile[0] = static_cast<cudaEvent_t>(prefill_begin);
+    g_profile[1] = static_cast<cudaEvent_t>(prefill_end);
+    g_profile[2] = static_cast<cudaEvent_t>(decode_begin);
+    g_profile[3] = static_cast<cudaEvent_t>(decode_end);
+    return PCP_OK;
 }
 
 extern "C" int pcp_lse_merge(const float* out_a, const float* lse_a, const float* out_b,

@@ -101,12 +101,14 @@ __global__ void __launch_bounds__(kDecThreads)
     const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.key_cache);
     const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.value_cache);
     const int32_t stride = 8 * kUnroll;  // keys per CTA iteration over all half-warps
-    for (int32_t k0 = lo + warp * 2 + half; k0 < hi; k0 += stride) {
+    // The trip count depends on the warp only, never on the half-warp, so both
+    // halves always run the full-warp shuffles below together.
+    for (int32_t kw = lo + warp * 2; kw < hi; kw += stride) {
         float kf[kUnroll][VEC], vf[kUnroll][VEC];
         bool live[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const int32_t k = k0 + 8 * u;
+            const int32_t k = kw + half + 8 * u;
             live[u] = false;
             if (k < hi) {
                 const int32_t pg = k / bs;
@@ -144,12 +146,12 @@ __global__ void __launch_bounds__(kDecThreads)
 #pragma unroll
             for (int u = 1; u < kUnroll; ++u) mx = fmaxf(mx, s[u]);
             const float m_new = fmaxf(m[g], mx);
-            if (m_new == -INFINITY) continue;
-            const float alpha = fast_exp2(m[g] - m_new);
+            const float mu = m_new == -INFINITY ? 0.f : m_new;  // no key yet: every weight is 0
+            const float alpha = fast_exp2(m[g] - mu);
             float p[kUnroll], ps = 0.f;
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
-                p[u] = fast_exp2(s[u] - m_new);
+                p[u] = fast_exp2(s[u] - mu);
                 ps += p[u];
             }
             l[g] = l[g] * alpha + ps;

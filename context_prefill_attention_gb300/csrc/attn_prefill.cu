@@ -460,6 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) report_status(a.status, PCP_ERR_TIMEOUT);
     }
 
+    __syncwarp();  // the producer's lane 0 worked alone: reconverge before the CTA barrier
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {

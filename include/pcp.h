@@ -220,6 +220,17 @@ int pcp_lse_merge(const float* out_a, const float* lse_a, const float* out_b, co
                   void* out, float* lse, int32_t total_q, int32_t num_q_heads, int32_t head_dim,
                   pcp_stream_t stream);
 
+/*
+ * pcp_set_profile_events — host. A tracing hook with no counterpart in the
+ * pages: while set, every pcp_attn_varlen call made by this thread records
+ * prefill_begin / prefill_end (cudaEvent_t) on its stream right before and
+ * after the prefill kernel, and decode_begin / decode_end around the decode
+ * kernels, so a caller can time them with cudaEventElapsedTime. Pass NULLs to
+ * stop. The events stay owned by the caller. Never fails (returns PCP_OK).
+ */
+int pcp_set_profile_events(void* prefill_begin, void* prefill_end, void* decode_begin,
+                           void* decode_end);
+
 /* The cudaError_t value of the last failed CUDA call in this thread (0 if none). */
 int pcp_last_cuda_error(void);
 
