@@ -32,7 +32,8 @@ ROW_FIELDS = ("req", "shard", "q_start", "q_len", "ctx_len", "kv_end", "causal_o
 
 # every symbol include/pcp.h declares
 EXPORTS = ("pcp_build_row_plan", "pcp_mask_slots_for_shard", "pcp_kv_cache_write",
-           "pcp_attn_workspace_size", "pcp_attn_varlen", "pcp_lse_merge", "pcp_set_profile_events",
+           "pcp_attn_workspace_size", "pcp_attn_varlen", "pcp_attn_varlen_noalloc", "pcp_lse_merge",
+           "pcp_set_profile_events",
            "pcp_last_cuda_error", "pcp_status_string")
 
 _lib = None
@@ -74,6 +75,9 @@ def load(path: Optional[str] = None):
     lib.pcp_attn_varlen.restype = ctypes.c_int
     lib.pcp_lse_merge.argtypes = [P, P, P, P, P, P, i32, i32, i32, P]
     lib.pcp_lse_merge.restype = ctypes.c_int
+    lib.pcp_attn_varlen_noalloc.argtypes = [P, P, P, P, i32, i32, i64, i32, P, i32, i32, i32, i32, i32, f32,
+                                            P, P, i32, P, P]
+    lib.pcp_attn_varlen_noalloc.restype = ctypes.c_int
     lib.pcp_set_profile_events.argtypes = [P, P, P, P]
     lib.pcp_set_profile_events.restype = ctypes.c_int
     lib.pcp_last_cuda_error.argtypes = []
@@ -184,6 +188,25 @@ def pcp_attn_varlen(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch
                              _t_ptr(workspace), int(workspace.numel() * workspace.element_size()), flags,
                              _t_ptr(status), _stream(stream))
     _check(rc, "pcp_attn_varlen")
+    return out, lse
+
+
+def pcp_attn_varlen_noalloc(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                            block_table: torch.Tensor, rows: torch.Tensor, scale: float, out: torch.Tensor,
+                            lse: torch.Tensor, flags: int = 0, status: Optional[torch.Tensor] = None,
+                            stream=None):
+    """:func:`pcp_attn_varlen` for callers that cannot allocate device memory:
+    the caller passes ``out`` and ``lse``, and the library's own fixed 64 MiB
+    scratch array (reserved on each GPU that loads the library) replaces the
+    workspace. Calls on one device share that array: keep them on one stream."""
+    lib = load()
+    T, hq, d = (int(x) for x in q.shape)
+    nb, bs, hkv, _ = (int(x) for x in key_cache.shape)
+    rc = lib.pcp_attn_varlen_noalloc(_t_ptr(q), _t_ptr(key_cache), _t_ptr(value_cache), _t_ptr(block_table),
+                                     int(block_table.shape[0]), int(block_table.shape[1]), nb, bs, _t_ptr(rows),
+                                     int(rows.shape[0]), T, hq, hkv, d, float(scale), _t_ptr(out), _t_ptr(lse),
+                                     flags, _t_ptr(status), _stream(stream))
+    _check(rc, "pcp_attn_varlen_noalloc")
     return out, lse
 
 

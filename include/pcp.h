@@ -204,6 +204,31 @@ int pcp_attn_varlen(const void* q, const void* key_cache, const void* value_cach
                     int32_t* status, pcp_stream_t stream);
 
 /*
+ * pcp_attn_varlen_noalloc — device. No counterpart on the pages: an addition
+ * for callers that cannot allocate device memory (a host framework that owns
+ * all device memory through its own allocator, or a serving loop that must
+ * not call cudaMalloc after start-up because the call can synchronise the
+ * device and has no latency bound). It is pcp_attn_varlen without the
+ * workspace arguments: the library supplies a fixed 64 MiB scratch array that
+ * every GPU loading the library reserves until the process exits, and the
+ * call allocates nothing.
+ * Same arguments, semantics, checks and errors as pcp_attn_varlen, plus
+ * PCP_ERR_WORKSPACE when pcp_attn_workspace_size(num_rows, total_q, Hq, D,
+ * max_blocks_per_req * block_size, flags) exceeds 64 MiB (nothing launched).
+ * The first call on a device looks up the array's device address with that
+ * device current (cudaGetSymbolAddress); make that first call before any
+ * stream capture. All calls on a device share the array: calls whose kernels
+ * may overlap on the GPU (other streams or threads) race on it — serialise
+ * them on one stream.
+ */
+int pcp_attn_varlen_noalloc(const void* q, const void* key_cache, const void* value_cache,
+                            const int32_t* block_table, int32_t num_reqs, int32_t max_blocks_per_req,
+                            int64_t num_blocks, int32_t block_size, const pcp_row_t* rows,
+                            int32_t num_rows, int32_t total_q, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim, float scale, void* out, float* lse,
+                            int32_t flags, int32_t* status, pcp_stream_t stream);
+
+/*
  * pcp_lse_merge — device. Merge two partial results of the same queries by
  * log-sum-exp ("[MRv2] FlashAttention PCP support ...": (ctx_out, ctx_lse)
  * combined with the new-token pass; the per-step LSE-combine of the DCP
