@@ -40,7 +40,7 @@ namespace pcp {
 
 namespace {
 
-constexpr int kThreads = 320;  // 10 warps
+constexpr int kThreads = 384;  // 12 warps: two softmax warpgroups, producer, MMA, two spare
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kNK = 2;  // K stages
@@ -48,6 +48,7 @@ constexpr int kNV = 2;  // V stages
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kPolyEvery = 4;  // one pair in four of an unmasked tile uses the polynomial exp2
 
 template <int D>
 struct Cfg {
@@ -183,60 +184,69 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int32_t total_items = (*a.num_units) * slots_per_unit;
+    // Registers: the launch gives 168 per thread (384 threads); the producer /
+    // MMA warpgroup gives back to 120 so the softmax warpgroups can hold a full
+    // 128-column score row (192): 128 x 120 + 256 x 192 = 384 x 168. setmaxnreg
+    // sits at the top of each warpgroup's branch so that each role's code is
+    // compiled against its own register limit.
 
+    if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 120;");
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            uint32_t kt = 0, vt = 0, c = 0;
-            const int32_t oob = (int32_t)(a.num_blocks * bs);  // a row past the cache: zero fill
-            const int pages = kBlockN / bs;
-            bool ok = true;
-            for (int32_t idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
-                const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, bs);
-                if (it.n_tiles == 0) continue;
-                if (c > 0 && !(ok = mbar_wait(q_empty, (c - 1) & 1, abort_flag))) break;
+        // The whole warp runs the loop: lane p owns page p of every key tile. It
+        // reads that page's block-table entry (all lanes in parallel, before the
+        // stage is free, so the table read overlaps the wait) and issues that
+        // page's TMA boxes for K and then V.
+        uint32_t kt = 0, vt = 0, c = 0;
+        const int32_t oob = (int32_t)(a.num_blocks * bs);  // a row past the cache: zero fill
+        const int pages = kBlockN / bs;
+        bool ok = true;
+        for (int32_t idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+            const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, bs);
+            if (it.n_tiles == 0) continue;
+            if (c > 0 && !(ok = mbar_wait_warp(q_empty, (c - 1) & 1, abort_flag))) break;
+            if (lane == 0) {
                 mbar_arrive_expect_tx(q_full, it.nslots * C::kTileBytes);
                 for (int g = 0; g < it.nslots; ++g)
                     for (int h = 0; h < C::kHalves; ++h)
                         tma_load_3d(sbase + C::kQ + g * C::kTileBytes + h * C::kHalfBytes, &tm_q,
                                     q_full, h * 64, it.h0 + g, it.q_tok0);
-                const int32_t* table = a.block_table + (size_t)it.req * a.max_blocks;
-                // page id -> first cache row of the page; pages past k_end (and bad ids)
-                // map to a row past the cache, which TMA fills with zeros
-                auto page_row = [&](int32_t key0, int p) -> int32_t {
-                    const int32_t k = key0 + p * bs;
-                    if (k >= it.k_end) return oob;
+            }
+            const int32_t* table = a.block_table + (size_t)it.req * a.max_blocks;
+            for (int32_t j = 0; j < it.n_tiles && ok; ++j) {
+                // this lane's page -> first cache row of the page; pages past k_end (and
+                // bad ids) map to a row past the cache, which TMA fills with zeros
+                int32_t y = oob;
+                const int32_t k = it.kb + j * kBlockN + lane * bs;
+                if (lane < pages && k < it.k_end) {
                     const int32_t pg = k / bs;
                     const int32_t id = pg < a.max_blocks ? __ldg(table + pg) : -1;
-                    if (id >= 0 && id < a.num_blocks) return id * bs;
-                    report_status(a.status, PCP_ERR_RANGE);
-                    return oob;
-                };
-                for (int32_t j = 0; j < it.n_tiles && ok; ++j) {
-                    const int32_t key0 = it.kb + j * kBlockN;
-                    const int ks = kt % kNK;
-                    if (!(ok = mbar_wait(k_empty(ks), ((kt / kNK) & 1) ^ 1, abort_flag))) break;
-                    mbar_arrive_expect_tx(k_full(ks), C::kTileBytes);
-                    for (int p = 0; p < pages; ++p)
-                        for (int h = 0; h < C::kHalves; ++h)
-                            tma_load_3d(sbase + C::kK + ks * C::kTileBytes + h * C::kHalfBytes +
-                                            p * bs * 128,
-                                        &tm_k, k_full(ks), h * 64, it.hk, page_row(key0, p));
-                    ++kt;
-                    const int vs = vt % kNV;
-                    if (!(ok = mbar_wait(v_empty(vs), ((vt / kNV) & 1) ^ 1, abort_flag))) break;
-                    mbar_arrive_expect_tx(v_full(vs), C::kTileBytes);
-                    for (int p = 0; p < pages; ++p)
-                        for (int h = 0; h < C::kHalves; ++h)
-                            tma_load_3d(sbase + C::kV + vs * C::kTileBytes + h * C::kHalfBytes +
-                                            p * bs * 128,
-                                        &tm_v, v_full(vs), h * 64, it.hk, page_row(key0, p));
-                    ++vt;
+                    if (id >= 0 && id < a.num_blocks) y = id * bs;
+                    else report_status(a.status, PCP_ERR_RANGE);
                 }
-                ++c;
+                const int ks = kt % kNK;
+                if (!(ok = mbar_wait_warp(k_empty(ks), ((kt / kNK) & 1) ^ 1, abort_flag))) break;
+                if (lane == 0) mbar_arrive_expect_tx(k_full(ks), C::kTileBytes);
+                __syncwarp();
+                if (lane < pages)
+                    for (int h = 0; h < C::kHalves; ++h)
+                        tma_load_3d(sbase + C::kK + ks * C::kTileBytes + h * C::kHalfBytes + lane * bs * 128,
+                                    &tm_k, k_full(ks), h * 64, it.hk, y);
+                ++kt;
+                const int vs = vt % kNV;
+                if (!(ok = mbar_wait_warp(v_empty(vs), ((vt / kNV) & 1) ^ 1, abort_flag))) break;
+                if (lane == 0) mbar_arrive_expect_tx(v_full(vs), C::kTileBytes);
+                __syncwarp();
+                if (lane < pages)
+                    for (int h = 0; h < C::kHalves; ++h)
+                        tma_load_3d(sbase + C::kV + vs * C::kTileBytes + h * C::kHalfBytes + lane * bs * 128,
+                                    &tm_v, v_full(vs), h * 64, it.hk, y);
+                ++vt;
             }
-            if (!ok) report_status(a.status, PCP_ERR_TIMEOUT);
+            ++c;
         }
+        if (!ok && lane == 0) report_status(a.status, PCP_ERR_TIMEOUT);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         uint32_t kt = 0, vt = 0, c = 0;
@@ -317,7 +327,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++c;
         }
         if (!ok) report_status(a.status, PCP_ERR_TIMEOUT);
+    }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 192;");
         // ------------------------------------------------------------ softmax
         const int g = warp / 4;                 // head slot of this warpgroup
         const int r = threadIdx.x % 128;        // query row within the tile = TMEM lane
@@ -357,9 +369,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c2 = 0; c2 < 128; ++c2)
                         if (c2 < lo || c2 >= hi) sf[c2] = -INFINITY;
                 }
-                float mx = sf[0];
+                // row max: eight independent chains of three-input maxima
+                float part[8];
 #pragma unroll
-                for (int c2 = 1; c2 < 128; ++c2) mx = fmaxf(mx, sf[c2]);
+                for (int i = 0; i < 8; ++i) {
+                    float t = sf[16 * i];
+#pragma unroll
+                    for (int k2 = 1; k2 < 15; k2 += 2) t = fmax3(t, sf[16 * i + k2], sf[16 * i + k2 + 1]);
+                    part[i] = fmaxf(t, sf[16 * i + 15]);
+                }
+                const float mx = fmax3(fmax3(part[0], part[1], part[2]), fmax3(part[3], part[4], part[5]),
+                                       fmaxf(part[6], part[7]));
                 const float m_new = fmaxf(m, mx * sl2);
                 // Lazy rescaling: keep the old reference max unless the new one exceeds
                 // it by more than 2^8; O and l then stay consistent with that max.
@@ -377,17 +397,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const float mu = (m == -INFINITY) ? 0.f : m;
-                float rs = 0.f;
-                uint32_t p[64];
+                // p = 2^(s * scale * log2 e - m), two lanes per instruction; every
+                // kPolyEvery-th pair goes to the FMA-pipe polynomial so the exponential
+                // unit is not the bottleneck (a masked key then gets ~1e-38, not 0).
+                // P is written back to TMEM in two halves to bound register pressure.
+                const float2 sl2v = make_float2(sl2, sl2), nmu = make_float2(-mu, -mu);
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f)};
 #pragma unroll
-                for (int c2 = 0; c2 < 64; ++c2) {
-                    const float p0 = fast_exp2(fmaf(sf[2 * c2], sl2, -mu));
-                    const float p1 = fast_exp2(fmaf(sf[2 * c2 + 1], sl2, -mu));
-                    rs += p0 + p1;
-                    p[c2] = pack_bf16x2(p0, p1);
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t p[32];
+#pragma unroll
+                    for (int c3 = 0; c3 < 32; ++c3) {
+                        const int c2 = half * 32 + c3;
+                        const float2 x = ffma2(make_float2(sf[2 * c2], sf[2 * c2 + 1]), sl2v, nmu);
+                        float2 e;
+                        if (c2 % kPolyEvery == kPolyEvery - 1) {
+                            e = exp2_poly2(x);
+                        } else {
+                            e.x = fast_exp2(x.x);
+                            e.y = fast_exp2(x.y);
+                        }
+                        acc[c2 % 4] = fadd2(acc[c2 % 4], e);
+                        p[c3] = pack_bf16x2(e.x, e.y);
+                    }
+                    tmem_st32(t_s + 32 * half, p);
                 }
-                tmem_st32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
-                tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+                const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+                const float2 a03 = fadd2(a01, a23);
+                const float rs = a03.x + a03.y;
                 if (rescale) {
 #pragma unroll
                     for (int c2 = 0; c2 < D / 32; ++c2) {

@@ -227,6 +227,55 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Packed two-wide fp32 arithmetic (one instruction for both lanes of the pair).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+// max of three floats in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// 2^x for a pair on the FMA pipe instead of the exponential unit, to share
+// the softmax's exponentials between the two. Method: Cody-Waite style range
+// reduction x = n + f with n = round(x) (added and subtracted 1.5 * 2^23 so the
+// FMA pipe rounds), f in [-1/2, 1/2]; 2^f by a degree-3 polynomial whose
+// coefficients minimise the maximum relative error on that interval (found by
+// linear programming; relative error <= 7.5e-5, below bf16 resolution); 2^n is
+// applied by adding n to the exponent field. x is clamped at -126 so the
+// exponent never underflows (the result is then ~1e-38 instead of 0).
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+    constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
+    x.x = fmaxf(x.x, -126.0f);
+    x.y = fmaxf(x.y, -126.0f);
+    const float2 j = fadd2(x, make_float2(kShift, kShift));
+    const float2 n = fadd2(j, make_float2(-kShift, -kShift));
+    const float2 f = ffma2(n, make_float2(-1.f, -1.f), x);
+    float2 p = ffma2(f, make_float2(0.0551716685295105f, 0.0551716685295105f),
+                     make_float2(0.2426111251115799f, 0.2426111251115799f));
+    p = ffma2(p, f, make_float2(0.6932609677314758f, 0.6932609677314758f));
+    p = ffma2(p, f, make_float2(0.9999280571937561f, 0.9999280571937561f));
+    return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(j.x) << 23)),
+                       __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(j.y) << 23)));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
