@@ -49,11 +49,11 @@ def _stale(target: str, sources) -> bool:
     return any(os.path.getmtime(s) > t for s in sources)
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-    if not verbose_ptxas and not _stale(obj, [src] + _deps()):
+def _compile(src: str, verbose_ptxas: bool, build_dir: str = BUILD, extra=()) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
+    if not verbose_ptxas and not extra and not _stale(obj, [src] + _deps()):
         return obj
-    cmd = [_nvcc(), "-c", src, "-o", obj + ".tmp"] + _flags(verbose_ptxas)
+    cmd = [_nvcc(), "-c", src, "-o", obj + ".tmp"] + _flags(verbose_ptxas) + list(extra)
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
@@ -63,21 +63,26 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(verbose_ptxas: bool = False, jobs: int = 0) -> str:
-    """Compile and link ``libpcp.so``; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose_ptxas: bool = False, jobs: int = 0, defines=(), out: str = LIB) -> str:
+    """Compile and link ``libpcp.so``; returns its path. ``defines`` (e.g.
+    ``["PCP_POLY_EXP_EVERY=8"]``) override the kernels' compile-time tuning
+    knobs; such a build goes to ``out`` through a build folder of its own."""
+    extra = [f"-D{d}" for d in defines]
+    build_dir = BUILD if not extra else out + ".build"
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     jobs = jobs or min(len(srcs), max(1, os.cpu_count() or 1))
     with cf.ThreadPoolExecutor(max_workers=jobs) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
-    if _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, build_dir, extra), srcs))
+    LIB_OUT = out
+    if extra or _stale(LIB_OUT, objs):
+        tmp = LIB_OUT + f".tmp{os.getpid()}"
         cmd = [_nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-Xcompiler", "-fPIC"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link of libpcp.so failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, LIB_OUT)
+    return LIB_OUT
 
 
 if __name__ == "__main__":

@@ -2,16 +2,22 @@
 // of its request ("[MRv2] FlashAttention PCP support for GQA on MRv2",
 // overview: mixed-batch decode handled next to the prefill rows; "[MRv2][PCP]
 // Carry the row plan ...", "drop pcp_has_prefill": decode rows carried in the
-// same plan). A single query row cannot fill a 128-row MMA, so this path is
-// bandwidth-bound CUDA-core code:
-//  * split-KV: CTA (split, kv head, row) streams keys [512 s, 512 (s+1)) of one
-//    kv head, every key's K and V row read once for all G q heads of the group;
-//  * 16 lanes per key, each lane one 16-byte (128-bit) load of K and of V
-//    (8 bf16 of D = 128), two keys per warp, four keys in flight per half-warp;
-//  * fp32 online softmax per head, partial (out, lse) per split in the
-//    workspace, merged by log-sum-exp in decode_merge_kernel.
+// same plan). A single query row cannot fill a 128-row MMA and the work is
+// bound by HBM bandwidth (every key's K and V read once per kv head), so this
+// path is CUDA-core code built around the memory system:
+//  * split-KV: CTA (split, kv head, row) streams keys [512 s, 512 (s+1)) of
+//    one kv head for all G q heads of its group;
+//  * a producer warp reads the chunk's block-table entries once, then streams
+//    16-key slabs of K and V into an 8-stage shared-memory ring with TMA (the
+//    same swizzled 64-dim boxes as the prefill path, completion on mbarriers);
+//  * four consumer warps share each slab: 16 lanes per key, each lane one
+//    128-bit (D = 128) or 64-bit (D = 64) shared load of K and of V, fp32 dot
+//    products reduced over the 16 lanes, fp32 online softmax per q head;
+//  * partial (out, lse) per split in the workspace, merged by log-sum-exp in
+//    decode_merge_kernel.
 // Also here: the LSE merge of the two prefill partials when the context and
 // new-token parts are computed separately.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -24,71 +30,137 @@ namespace pcp {
 
 namespace {
 
-constexpr int kDecThreads = 128;
-constexpr int kUnroll = 4;
+constexpr int kSlab = 16;          // keys per pipeline stage
+constexpr int kStages = 8;         // slabs in flight per CTA
+constexpr int kConsumerWarps = 4;
+constexpr int kDecThreads = 32 * (kConsumerWarps + 1);
+constexpr int kMaxPages = kDecodeChunk / 8;  // block-table entries of one chunk (block_size >= 8)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+template <int D, int GMAX>
+struct DecCfg {
+    static constexpr int kHalfBytes = kSlab * 128;                  // 16 rows x 64 dims (bf16)
+    static constexpr int kSlabBytes = (D / 64) * kHalfBytes;        // K (or V) of one slab
+    static constexpr int kStageBytes = 2 * kSlabBytes;
+    static constexpr int kBars = kStages * kStageBytes;
+    static constexpr int kPages = kBars + 2 * kStages * 8;
+    static constexpr int kComb = kPages + kMaxPages * 4 + 16;
+    static constexpr int kSmem = kComb + (2 * kConsumerWarps * GMAX + kConsumerWarps * GMAX * D) * 4 + 1024;
+};
+
+// VEC consecutive bf16 of one key row, read from a 128-byte-swizzled slab:
+// row kr (0..15) of the slab, first dim e0 (a multiple of VEC).
 template <int VEC>
-struct VecLoad;
-template <>
-struct VecLoad<8> {  // 16 bytes
-    __device__ __forceinline__ static void load(const __nv_bfloat16* p, float (&f)[8]) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+__device__ __forceinline__ void load_row(const uint8_t* slab, int kr, int e0, float (&f)[VEC]) {
+    const int b = e0 * 2;
+    const int half = b >> 7, bb = b & 127;
+    const uint8_t* p = slab + half * (kSlab * 128) + kr * 128 + ((((bb >> 4) ^ (kr & 7)) << 4) | (bb & 15));
+    if constexpr (VEC == 8) {
+        const uint4 u = *reinterpret_cast<const uint4*>(p);
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             f[2 * i] = __uint_as_float(w[i] << 16);
             f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
         }
-    }
-};
-template <>
-struct VecLoad<4> {  // 8 bytes
-    __device__ __forceinline__ static void load(const __nv_bfloat16* p, float (&f)[4]) {
-        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    } else {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
         f[0] = __uint_as_float(u.x << 16);
         f[1] = __uint_as_float(u.x & 0xFFFF0000u);
         f[2] = __uint_as_float(u.y << 16);
         f[3] = __uint_as_float(u.y & 0xFFFF0000u);
     }
-};
+}
 
 template <int D, int GMAX>
 __global__ void __launch_bounds__(kDecThreads)
-    decode_kernel(PrefillArgs a, float* __restrict__ dec_out, float* __restrict__ dec_lse, int max_splits) {
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  PrefillArgs a, float* __restrict__ dec_out, float* __restrict__ dec_lse, int max_splits,
+                  int box_rows) {
+    using C = DecCfg<D, GMAX>;
     constexpr int VEC = D / 16;
     const int split = blockIdx.x, hk = blockIdx.y, ri = blockIdx.z;
     if (!a.row_ok[ri]) return;
     const pcp_row_t row = a.rows[ri];
     if (!row.is_decode) return;
-    const int32_t C = row.kv_end;
+    const int32_t C_len = row.kv_end;
     const int32_t lo = split * kDecodeChunk;
-    if (lo >= C) return;
-    const int32_t hi = min(C, lo + kDecodeChunk);
+    if (lo >= C_len) return;
+    const int32_t hi = min(C_len, lo + kDecodeChunk);
+    const int nslab = (hi - lo + kSlab - 1) / kSlab;
     const int G = a.hq / a.hkv;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int half = lane / 16, dl = lane % 16;
-    const float sl2 = a.scale * kLog2e;
     const int32_t bs = a.block_size;
 
-    __shared__ float s_m[4][GMAX], s_l[4][GMAX];
-    __shared__ float s_acc[4][GMAX][D];
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    auto full_bar = [&](int s) { return sbase + C::kBars + 8 * s; };
+    auto empty_bar = [&](int s) { return sbase + C::kBars + 8 * (kStages + s); };
+    int32_t* page_row = reinterpret_cast<int32_t*>(smem + C::kPages);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kPages + kMaxPages * 4);
+    float* s_m = reinterpret_cast<float*>(smem + C::kComb);
+    float* s_l = s_m + kConsumerWarps * GMAX;
+    float* s_acc = s_l + kConsumerWarps * GMAX;
 
-    float qf[GMAX][VEC];
-    const __nv_bfloat16* qbase = reinterpret_cast<const __nv_bfloat16*>(a.q) +
-                                 ((size_t)row.q_start * a.hq + (size_t)hk * G) * D + dl * VEC;
-#pragma unroll
-    for (int g = 0; g < GMAX; ++g) {
-        if (g < G) {
-            VecLoad<VEC>::load(qbase + (size_t)g * D, qf[g]);
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) qf[g][e] *= sl2;
-        } else {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) qf[g][e] = 0.f;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), kConsumerWarps);
         }
+        *abort_flag = 0;
+        fence_barrier_init();
     }
+    __syncthreads();
+
+    bool ok = true;
+    if (warp == kConsumerWarps) {
+        // ---------------------------------------------------------------- producer
+        // every block-table entry of the chunk once (lane p: pages p and p + 32)
+        const int32_t* table = a.block_table + (size_t)row.req * a.max_blocks;
+        const int32_t oob = (int32_t)(a.num_blocks * bs);  // a row past the cache: zero fill
+        const int32_t pg0 = lo / bs;
+        const int npages = (hi - 1) / bs - pg0 + 1;
+        for (int p = lane; p < npages; p += 32) {
+            const int32_t pg = pg0 + p;
+            const int32_t id = pg < a.max_blocks ? __ldg(table + pg) : -1;
+            int32_t y = oob;
+            if (id >= 0 && id < a.num_blocks) y = id * bs;
+            else report_status(a.status, PCP_ERR_RANGE);
+            page_row[p] = y;
+        }
+        __syncwarp();
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            for (int i = 0; i < nslab; ++i) {
+                const int st = i % kStages;
+                if (!(ok = mbar_wait(empty_bar(st), ((i / kStages) & 1) ^ 1, abort_flag))) break;
+                mbar_arrive_expect_tx(full_bar(st), C::kStageBytes);
+                const uint32_t dst = sbase + st * C::kStageBytes;
+                for (int b = 0; b < kSlab / box_rows; ++b) {
+                    const int32_t key = lo + i * kSlab + b * box_rows;
+                    int32_t y = oob;
+                    if (key < hi) {
+                        const int32_t base = page_row[key / bs - pg0];
+                        if (base != oob) y = base + (key % bs);
+                    }
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h) {
+                        tma_load_3d(dst + h * C::kHalfBytes + b * box_rows * 128, &tm_k, full_bar(st), h * 64, hk, y);
+                        tma_load_3d(dst + C::kSlabBytes + h * C::kHalfBytes + b * box_rows * 128, &tm_v,
+                                    full_bar(st), h * 64, hk, y);
+                    }
+                }
+            }
+            if (!ok) report_status(a.status, PCP_ERR_TIMEOUT);
+        }
+        __syncwarp();
+    }
+
+    const int half = lane / 16, dl = lane % 16;
     float m[GMAX], l[GMAX], acc[GMAX][VEC];
 #pragma unroll
     for (int g = 0; g < GMAX; ++g) {
@@ -97,113 +169,109 @@ __global__ void __launch_bounds__(kDecThreads)
 #pragma unroll
         for (int e = 0; e < VEC; ++e) acc[g][e] = 0.f;
     }
-    const int32_t* table = a.block_table + (size_t)row.req * a.max_blocks;
-    const __nv_bfloat16* kc = reinterpret_cast<const __nv_bfloat16*>(a.key_cache);
-    const __nv_bfloat16* vc = reinterpret_cast<const __nv_bfloat16*>(a.value_cache);
-    const int32_t stride = 8 * kUnroll;  // keys per CTA iteration over all half-warps
-    // The trip count depends on the warp only, never on the half-warp, so both
-    // halves always run the full-warp shuffles below together.
-    for (int32_t kw = lo + warp * 2; kw < hi; kw += stride) {
-        float kf[kUnroll][VEC], vf[kUnroll][VEC];
-        bool live[kUnroll];
+    if (warp < kConsumerWarps) {
+        // ---------------------------------------------------------------- consumers
+        const float sl2 = a.scale * kLog2e;
+        float qf[GMAX][VEC];
+        const __nv_bfloat16* qbase = reinterpret_cast<const __nv_bfloat16*>(a.q) +
+                                     ((size_t)row.q_start * a.hq + (size_t)hk * G) * D + dl * VEC;
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int32_t k = kw + half + 8 * u;
-            live[u] = false;
-            if (k < hi) {
-                const int32_t pg = k / bs;
-                const int32_t id = pg < a.max_blocks ? __ldg(table + pg) : -1;
-                if (id >= 0 && id < a.num_blocks) {
-                    const size_t off = (((size_t)id * bs + (k - pg * bs)) * a.hkv + hk) * D + dl * VEC;
-                    VecLoad<VEC>::load(kc + off, kf[u]);
-                    VecLoad<VEC>::load(vc + off, vf[u]);
-                    live[u] = true;
-                } else {
-                    report_status(a.status, PCP_ERR_RANGE);
+        for (int g = 0; g < GMAX; ++g) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                qf[g][e] = g < G ? __bfloat162float(qbase[(size_t)g * D + e]) * sl2 : 0.f;
+        }
+        for (int i = 0; i < nslab; ++i) {
+            const int st = i % kStages;
+            if (!(ok = mbar_wait_warp(full_bar(st), (i / kStages) & 1, abort_flag))) break;
+            const uint8_t* kslab = smem + st * C::kStageBytes;
+            const uint8_t* vslab = kslab + C::kSlabBytes;
+            // this half-warp's two keys of the slab: rows 4 w + half and 4 w + 2 + half
+            float s[2][GMAX];
+            float vf[2][VEC];
+            bool live[2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int kr = 4 * warp + 2 * t + half;
+                live[t] = lo + i * kSlab + kr < hi;
+                float kf[VEC];
+                load_row<VEC>(kslab, kr, dl * VEC, kf);
+                load_row<VEC>(vslab, kr, dl * VEC, vf[t]);
+                if (!live[t]) {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) vf[t][e] = 0.f;  // rows past the end may hold anything
+                }
+#pragma unroll
+                for (int g = 0; g < GMAX; ++g) {
+                    float d = 0.f;
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) d = fmaf(qf[g][e], kf[e], d);
+                    s[t][g] = d;
                 }
             }
-            if (!live[u]) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(st));
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) kf[u][e] = vf[u][e] = 0.f;
+            for (int g = 0; g < GMAX; ++g) {
+                if (g >= G) break;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    float d = s[t][g];
+                    d += __shfl_xor_sync(0xffffffffu, d, 8);
+                    d += __shfl_xor_sync(0xffffffffu, d, 4);
+                    d += __shfl_xor_sync(0xffffffffu, d, 2);
+                    d += __shfl_xor_sync(0xffffffffu, d, 1);
+                    s[t][g] = live[t] ? d : -INFINITY;
+                }
+                const float m_new = fmax3(m[g], s[0][g], s[1][g]);
+                const float mu = m_new == -INFINITY ? 0.f : m_new;  // no key yet: every weight is 0
+                const float alpha = fast_exp2(m[g] - mu);
+                const float p0 = fast_exp2(s[0][g] - mu), p1 = fast_exp2(s[1][g] - mu);
+                l[g] = l[g] * alpha + p0 + p1;
+                m[g] = m_new;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc[g][e] = fmaf(p1, vf[1][e], fmaf(p0, vf[0][e], acc[g][e] * alpha));
             }
         }
+        if (!ok) report_status(a.status, PCP_ERR_TIMEOUT);
+        // combine the two half-warps of each warp (lane i and lane i ^ 16 hold the same dims)
 #pragma unroll
         for (int g = 0; g < GMAX; ++g) {
             if (g >= G) break;
-            float s[kUnroll];
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                float d = 0.f;
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) d = fmaf(qf[g][e], kf[u][e], d);
-                d += __shfl_xor_sync(0xffffffffu, d, 8);
-                d += __shfl_xor_sync(0xffffffffu, d, 4);
-                d += __shfl_xor_sync(0xffffffffu, d, 2);
-                d += __shfl_xor_sync(0xffffffffu, d, 1);
-                s[u] = live[u] ? d : -INFINITY;
-            }
-            float mx = s[0];
-#pragma unroll
-            for (int u = 1; u < kUnroll; ++u) mx = fmaxf(mx, s[u]);
-            const float m_new = fmaxf(m[g], mx);
-            const float mu = m_new == -INFINITY ? 0.f : m_new;  // no key yet: every weight is 0
-            const float alpha = fast_exp2(m[g] - mu);
-            float p[kUnroll], ps = 0.f;
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                p[u] = fast_exp2(s[u] - mu);
-                ps += p[u];
-            }
-            l[g] = l[g] * alpha + ps;
-            m[g] = m_new;
+            const float mo = __shfl_xor_sync(0xffffffffu, m[g], 16);
+            const float lo2 = __shfl_xor_sync(0xffffffffu, l[g], 16);
+            const float M = fmaxf(m[g], mo);
+            const float fa = M == -INFINITY ? 0.f : fast_exp2(m[g] - M);
+            const float fb = M == -INFINITY ? 0.f : fast_exp2(mo - M);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
-                float x = acc[g][e] * alpha;
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) x = fmaf(p[u], vf[u][e], x);
-                acc[g][e] = x;
+                const float ao = __shfl_xor_sync(0xffffffffu, acc[g][e], 16);
+                acc[g][e] = fa * acc[g][e] + fb * ao;
             }
-        }
-    }
-    // combine the two half-warps of each warp (lane i and lane i ^ 16 hold the
-    // same dims), then the four warps of the CTA through shared memory
+            if (half == 0) {
+                if (dl == 0) {
+                    s_m[warp * GMAX + g] = M;
+                    s_l[warp * GMAX + g] = fa * l[g] + fb * lo2;
+                }
 #pragma unroll
-    for (int g = 0; g < GMAX; ++g) {
-        if (g >= G) break;
-        const float mo = __shfl_xor_sync(0xffffffffu, m[g], 16);
-        const float lo2 = __shfl_xor_sync(0xffffffffu, l[g], 16);
-        const float M = fmaxf(m[g], mo);
-        const float fa = M == -INFINITY ? 0.f : fast_exp2(m[g] - M);
-        const float fb = M == -INFINITY ? 0.f : fast_exp2(mo - M);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            const float ao = __shfl_xor_sync(0xffffffffu, acc[g][e], 16);
-            acc[g][e] = fa * acc[g][e] + fb * ao;
-        }
-        m[g] = M;
-        l[g] = fa * l[g] + fb * lo2;
-        if (half == 0) {
-            if (dl == 0) {
-                s_m[warp][g] = m[g];
-                s_l[warp][g] = l[g];
+                for (int e = 0; e < VEC; ++e) s_acc[(warp * GMAX + g) * D + dl * VEC + e] = acc[g][e];
             }
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) s_acc[warp][g][dl * VEC + e] = acc[g][e];
         }
     }
     __syncthreads();
+    // combine the consumer warps and write this split's partial
     for (int i = threadIdx.x; i < G * D; i += kDecThreads) {
         const int g = i / D, d = i % D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, s_m[w][g]);
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w * GMAX + g]);
         float L = 0.f, O = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const float f = fast_exp2(s_m[w][g] - M);
-                L += f * s_l[w][g];
-                O += f * s_acc[w][g][d];
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float f = fast_exp2(s_m[w * GMAX + g] - M);
+                L += f * s_l[w * GMAX + g];
+                O += f * s_acc[(w * GMAX + g) * D + d];
             }
         }
         const int h = hk * G + g;
@@ -278,9 +346,17 @@ __global__ void __launch_bounds__(256)
 template <int D, int GMAX>
 int launch_decode_dg(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
                      cudaStream_t stream) {
+    const int box_rows = a.block_size < kSlab ? a.block_size : kSlab;
+    CUtensorMap tk, tv;
+    if (!make_kv_map(&tk, a.key_cache, D, a.hkv, a.num_blocks * a.block_size, box_rows) ||
+        !make_kv_map(&tv, a.value_cache, D, a.hkv, a.num_blocks * a.block_size, box_rows))
+        return PCP_ERR_CUDA;
+    const int smem = DecCfg<D, GMAX>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, GMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
     dim3 grid(max_splits, a.hkv, a.num_rows);
-    decode_kernel<D, GMAX><<<grid, kDecThreads, 0, stream>>>(a, dec_out, dec_lse, max_splits);
-    cudaError_t e = cudaGetLastError();
+    decode_kernel<D, GMAX><<<grid, kDecThreads, smem, stream>>>(tk, tv, a, dec_out, dec_lse, max_splits, box_rows);
+    e = cudaGetLastError();
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
     decode_merge_kernel<D><<<dim3(a.num_rows, a.hq), D, 0, stream>>>(a, dec_out, dec_lse, max_splits);
     e = cudaGetLastError();

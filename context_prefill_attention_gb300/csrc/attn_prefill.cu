@@ -43,12 +43,25 @@ namespace {
 constexpr int kThreads = 384;  // 12 warps: two softmax warpgroups, producer, MMA, two spare
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kNK = 2;  // K stages
-constexpr int kNV = 2;  // V stages
+// Tuning knobs (compile-time; the defaults are the measured best on GB300).
+#ifndef PCP_PREFILL_K_STAGES
+#define PCP_PREFILL_K_STAGES 2
+#endif
+#ifndef PCP_PREFILL_V_STAGES
+#define PCP_PREFILL_V_STAGES 2
+#endif
+#ifndef PCP_POLY_EXP_EVERY
+// Off: on GB300 the exponential unit keeps up with the tensor cores, and the
+// polynomial only costs issue slots (measured: 1 pair in 4 -> 9% slower).
+#define PCP_POLY_EXP_EVERY 1000000
+#endif
+constexpr int kNK = PCP_PREFILL_K_STAGES;  // K stages
+constexpr int kNV = PCP_PREFILL_V_STAGES;  // V stages
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kPolyEvery = 4;  // one pair in four of an unmasked tile uses the polynomial exp2
+// one pair in kPolyEvery of a tile uses the polynomial exp2 (a large value turns it off)
+constexpr int kPolyEvery = PCP_POLY_EXP_EVERY;
 
 template <int D>
 struct Cfg {
@@ -397,9 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const float mu = (m == -INFINITY) ? 0.f : m;
-                // p = 2^(s * scale * log2 e - m), two lanes per instruction; every
-                // kPolyEvery-th pair goes to the FMA-pipe polynomial so the exponential
-                // unit is not the bottleneck (a masked key then gets ~1e-38, not 0).
+                // p = 2^(s * scale * log2 e - m), two lanes per instruction. With the
+                // polynomial knob on, every kPolyEvery-th pair goes to the FMA pipe (a
+                // masked key then gets ~1e-38, not 0); by default all use ex2.
                 // P is written back to TMEM in two halves to bound register pressure.
                 const float2 sl2v = make_float2(sl2, sl2), nmu = make_float2(-mu, -mu);
                 float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -681,6 +694,10 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     if (a.d == 64) return launch_prefill_d<64>(a, stream);
     if (a.d == 128) return launch_prefill_d<128>(a, stream);
     return PCP_ERR_UNSUPPORTED;
+}
+
+bool make_kv_map(CUtensorMap* m, const void* base, int D, int64_t mid, int64_t outer, int rows) {
+    return make_map(m, base, D, mid, outer, rows);
 }
 
 }  // namespace pcp

@@ -71,6 +71,10 @@ struct PrefillArgs {
     int32_t* status;
 };
 
+// TMA map of a bf16 tensor viewed as [outer][mid][D] with a box of 64 x 1 x rows
+// and 128-byte swizzle (Q: [T][Hq][D]; a paged cache: [blocks * bs][Hkv][D]).
+bool make_kv_map(CUtensorMap* m, const void* base, int D, int64_t mid, int64_t outer, int rows);
+
 int launch_schedule(const PrefillArgs& a, int32_t flags, Unit* units, Unit* units_sorted,
                     int32_t* header, int32_t* row_ok, int64_t max_units, cudaStream_t stream);
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
