@@ -8,11 +8,13 @@
 //  * split-KV: CTA (split, kv head, row) streams keys [512 s, 512 (s+1)) of
 //    one kv head for all G q heads of its group;
 //  * a producer warp reads the chunk's block-table entries once, then streams
-//    16-key slabs of K and V into an 8-stage shared-memory ring with TMA (the
+//    32-key slabs of K and V into a 4-stage shared-memory ring with TMA (the
 //    same swizzled 64-dim boxes as the prefill path, completion on mbarriers);
-//  * four consumer warps share each slab: 16 lanes per key, each lane one
-//    128-bit (D = 128) or 64-bit (D = 64) shared load of K and of V, fp32 dot
-//    products reduced over the 16 lanes, fp32 online softmax per q head;
+//  * four consumer warps share each slab, a half-warp per group of keys: each
+//    lane one 128-bit (D = 128) or 64-bit (D = 64) shared load per K and V row,
+//    packed fp32 dot products, a butterfly reduce-scatter over the 16 lanes so
+//    that each lane ends with one (key, head) score, one exponential per lane,
+//    fp32 online softmax per q head with lazy rescaling;
 //  * partial (out, lse) per split in the workspace, merged by log-sum-exp in
 //    decode_merge_kernel.
 // Also here: the LSE merge of the two prefill partials when the context and
@@ -30,8 +32,8 @@ namespace pcp {
 
 namespace {
 
-constexpr int kSlab = 16;          // keys per pipeline stage
-constexpr int kStages = 8;         // slabs in flight per CTA
+constexpr int kSlab = 32;          // keys per pipeline stage
+constexpr int kStages = 4;         // slabs in flight per CTA
 constexpr int kConsumerWarps = 4;
 constexpr int kDecThreads = 32 * (kConsumerWarps + 1);
 constexpr int kMaxPages = kDecodeChunk / 8;  // block-table entries of one chunk (block_size >= 8)
@@ -40,7 +42,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D, int GMAX>
 struct DecCfg {
-    static constexpr int kHalfBytes = kSlab * 128;                  // 16 rows x 64 dims (bf16)
+    static constexpr int kHalfBytes = kSlab * 128;                  // kSlab rows x 64 dims (bf16)
     static constexpr int kSlabBytes = (D / 64) * kHalfBytes;        // K (or V) of one slab
     static constexpr int kStageBytes = 2 * kSlabBytes;
     static constexpr int kBars = kStages * kStageBytes;
@@ -161,22 +163,28 @@ __global__ void __launch_bounds__(kDecThreads)
     }
 
     const int half = lane / 16, dl = lane % 16;
-    float m[GMAX], l[GMAX], acc[GMAX][VEC];
+    // Each half-warp handles KPI keys per step: its 16 lanes hold 8 (D = 128) or 4
+    // (D = 64) dims each, so every lane forms KPI x GP partial dot products; a
+    // butterfly reduce-scatter over the 16 lanes leaves lane dl with the full score
+    // of key dl / GP for head dl % GP (15 shuffles for all 16 scores).
+    constexpr int GP = GMAX;        // heads of a group, padded to a power of two
+    constexpr int KPI = 16 / GP;    // keys per half-warp and step
+    constexpr int NSUB = (kSlab + 8 * KPI - 1) / (8 * KPI);
+    const int g_own = dl % GP, kk_own = dl / GP;
+    float m_own = -INFINITY, l_part = 0.f;
+    float acc[GP][VEC];
 #pragma unroll
-    for (int g = 0; g < GMAX; ++g) {
-        m[g] = -INFINITY;
-        l[g] = 0.f;
+    for (int g = 0; g < GP; ++g)
 #pragma unroll
         for (int e = 0; e < VEC; ++e) acc[g][e] = 0.f;
-    }
     if (warp < kConsumerWarps) {
         // ---------------------------------------------------------------- consumers
         const float sl2 = a.scale * kLog2e;
-        float qf[GMAX][VEC];
+        float qf[GP][VEC];
         const __nv_bfloat16* qbase = reinterpret_cast<const __nv_bfloat16*>(a.q) +
                                      ((size_t)row.q_start * a.hq + (size_t)hk * G) * D + dl * VEC;
 #pragma unroll
-        for (int g = 0; g < GMAX; ++g) {
+        for (int g = 0; g < GP; ++g) {
 #pragma unroll
             for (int e = 0; e < VEC; ++e)
                 qf[g][e] = g < G ? __bfloat162float(qbase[(size_t)g * D + e]) * sl2 : 0.f;
@@ -186,72 +194,118 @@ __global__ void __launch_bounds__(kDecThreads)
             if (!(ok = mbar_wait_warp(full_bar(st), (i / kStages) & 1, abort_flag))) break;
             const uint8_t* kslab = smem + st * C::kStageBytes;
             const uint8_t* vslab = kslab + C::kSlabBytes;
-            // this half-warp's two keys of the slab: rows 4 w + half and 4 w + 2 + half
-            float s[2][GMAX];
-            float vf[2][VEC];
-            bool live[2];
+            const int32_t key_base = lo + i * kSlab;
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const int kr = 4 * warp + 2 * t + half;
-                live[t] = lo + i * kSlab + kr < hi;
-                float kf[VEC];
-                load_row<VEC>(kslab, kr, dl * VEC, kf);
-                load_row<VEC>(vslab, kr, dl * VEC, vf[t]);
-                if (!live[t]) {
+            for (int sub = 0; sub < NSUB; ++sub) {
+                const int base_r = sub * 8 * KPI + (warp * 2 + half) * KPI;
+                // partial dot products of this lane's dims: v[kk * GP + g]
+                float v[16];
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) vf[t][e] = 0.f;  // rows past the end may hold anything
+                for (int kk = 0; kk < KPI; ++kk) {
+                    const int r = base_r + kk;
+                    float kf[VEC];
+                    if (r < kSlab) {
+                        load_row<VEC>(kslab, r, dl * VEC, kf);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) kf[e] = 0.f;
+                    }
+#pragma unroll
+                    for (int g = 0; g < GP; ++g) {
+                        float2 d2 = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int e = 0; e < VEC; e += 2)
+                            d2 = ffma2(make_float2(qf[g][e], qf[g][e + 1]), make_float2(kf[e], kf[e + 1]), d2);
+                        v[kk * GP + g] = d2.x + d2.y;
+                    }
                 }
+                // reduce-scatter: after the step with offset o a lane keeps the half of its
+                // values selected by bit o of its lane index
 #pragma unroll
-                for (int g = 0; g < GMAX; ++g) {
-                    float d = 0.f;
+                for (int o = 8, n = 16; o >= 1; o >>= 1, n >>= 1) {
+                    const bool upper = (dl & o) != 0;
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) d = fmaf(qf[g][e], kf[e], d);
-                    s[t][g] = d;
+                    for (int t = 0; t < n / 2; ++t) {
+                        const float send = upper ? v[t] : v[t + n / 2];
+                        const float keep = upper ? v[t + n / 2] : v[t];
+                        v[t] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                    }
+                }
+                const int r_own = base_r + kk_own;
+                const bool live_own = g_own < G && r_own < kSlab && key_base + r_own < hi;
+                const float s_own = live_own ? v[0] : -INFINITY;
+                // running max of this head over the lanes holding it (lanes dl = g_own mod GP)
+                float mx = s_own;
+#pragma unroll
+                for (int o = GP; o < 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                const float m_new = fmaxf(m_own, mx);
+                // lazy rescaling: keep the old reference max unless the new one exceeds it by 2^8
+                const bool need = m_new > m_own + 8.0f;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float alpha = need ? fast_exp2(m_own - m_new) : 1.f;
+                    if (need) {
+                        m_own = m_new;
+                        l_part *= alpha;
+                    }
+#pragma unroll
+                    for (int g = 0; g < GP; ++g) {
+                        const float ag = __shfl_sync(0xffffffffu, alpha, half * 16 + g);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) acc[g][e] *= ag;
+                    }
+                }
+                const float mu = m_own == -INFINITY ? 0.f : m_own;  // no key yet: every weight is 0
+                const float p_own = fast_exp2(s_own - mu);
+                l_part += p_own;
+#pragma unroll
+                for (int kk = 0; kk < KPI; ++kk) {
+                    const int r = base_r + kk;
+                    float vf[VEC];
+                    if (r < kSlab && key_base + r < hi) {
+                        load_row<VEC>(vslab, r, dl * VEC, vf);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) vf[e] = 0.f;  // rows past the end may hold anything
+                    }
+#pragma unroll
+                    for (int g = 0; g < GP; ++g) {
+                        const float p = __shfl_sync(0xffffffffu, p_own, half * 16 + kk * GP + g);
+#pragma unroll
+                        for (int e = 0; e < VEC; e += 2) {
+                            const float2 r2 = ffma2(make_float2(p, p), make_float2(vf[e], vf[e + 1]),
+                                                    make_float2(acc[g][e], acc[g][e + 1]));
+                            acc[g][e] = r2.x;
+                            acc[g][e + 1] = r2.y;
+                        }
+                    }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar(st));
-#pragma unroll
-            for (int g = 0; g < GMAX; ++g) {
-                if (g >= G) break;
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    float d = s[t][g];
-                    d += __shfl_xor_sync(0xffffffffu, d, 8);
-                    d += __shfl_xor_sync(0xffffffffu, d, 4);
-                    d += __shfl_xor_sync(0xffffffffu, d, 2);
-                    d += __shfl_xor_sync(0xffffffffu, d, 1);
-                    s[t][g] = live[t] ? d : -INFINITY;
-                }
-                const float m_new = fmax3(m[g], s[0][g], s[1][g]);
-                const float mu = m_new == -INFINITY ? 0.f : m_new;  // no key yet: every weight is 0
-                const float alpha = fast_exp2(m[g] - mu);
-                const float p0 = fast_exp2(s[0][g] - mu), p1 = fast_exp2(s[1][g] - mu);
-                l[g] = l[g] * alpha + p0 + p1;
-                m[g] = m_new;
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) acc[g][e] = fmaf(p1, vf[1][e], fmaf(p0, vf[0][e], acc[g][e] * alpha));
-            }
         }
         if (!ok) report_status(a.status, PCP_ERR_TIMEOUT);
-        // combine the two half-warps of each warp (lane i and lane i ^ 16 hold the same dims)
+        // the sum of this lane's head over its lanes, then combine the two half-warps
+        // (lane i and lane i ^ 16 hold the same dims) and hand the warp's state over
 #pragma unroll
-        for (int g = 0; g < GMAX; ++g) {
-            if (g >= G) break;
-            const float mo = __shfl_xor_sync(0xffffffffu, m[g], 16);
-            const float lo2 = __shfl_xor_sync(0xffffffffu, l[g], 16);
-            const float M = fmaxf(m[g], mo);
-            const float fa = M == -INFINITY ? 0.f : fast_exp2(m[g] - M);
+        for (int o = GP; o < 16; o <<= 1) l_part += __shfl_xor_sync(0xffffffffu, l_part, o);
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            const float mg = __shfl_sync(0xffffffffu, m_own, half * 16 + g);
+            const float lg = __shfl_sync(0xffffffffu, l_part, half * 16 + g);
+            const float mo = __shfl_xor_sync(0xffffffffu, mg, 16);
+            const float lo2 = __shfl_xor_sync(0xffffffffu, lg, 16);
+            const float M = fmaxf(mg, mo);
+            const float fa = M == -INFINITY ? 0.f : fast_exp2(mg - M);
             const float fb = M == -INFINITY ? 0.f : fast_exp2(mo - M);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
                 const float ao = __shfl_xor_sync(0xffffffffu, acc[g][e], 16);
                 acc[g][e] = fa * acc[g][e] + fb * ao;
             }
-            if (half == 0) {
+            if (half == 0 && g < G) {
                 if (dl == 0) {
                     s_m[warp * GMAX + g] = M;
-                    s_l[warp * GMAX + g] = fa * l[g] + fb * lo2;
+                    s_l[warp * GMAX + g] = fa * lg + fb * lo2;
                 }
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) s_acc[(warp * GMAX + g) * D + dl * VEC + e] = acc[g][e];
@@ -368,6 +422,7 @@ template <int D>
 int launch_decode_d(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
                     cudaStream_t stream) {
     const int G = a.hq / a.hkv;
+    if (G <= 2) return launch_decode_dg<D, 2>(a, dec_out, dec_lse, max_splits, stream);
     if (G <= 4) return launch_decode_dg<D, 4>(a, dec_out, dec_lse, max_splits, stream);
     if (G <= 8) return launch_decode_dg<D, 8>(a, dec_out, dec_lse, max_splits, stream);
     if (G <= 16) return launch_decode_dg<D, 16>(a, dec_out, dec_lse, max_splits, stream);
