@@ -32,8 +32,11 @@ namespace pcp {
 
 namespace {
 
-constexpr int kSlab = 32;          // keys per pipeline stage
-constexpr int kStages = 4;         // slabs in flight per CTA
+#ifndef PCP_DECODE_STAGES
+#define PCP_DECODE_STAGES 4
+#endif
+constexpr int kSlab = 32;                  // keys per pipeline stage
+constexpr int kStages = PCP_DECODE_STAGES;  // slabs in flight per CTA
 constexpr int kConsumerWarps = 4;
 constexpr int kDecThreads = 32 * (kConsumerWarps + 1);
 constexpr int kMaxPages = kDecodeChunk / 8;  // block-table entries of one chunk (block_size >= 8)

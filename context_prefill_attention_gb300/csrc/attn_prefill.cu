@@ -467,16 +467,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
             }
             const size_t orow = ((size_t)tok * a.hq + h) * D;
+            // the whole O row into registers first, so the accumulator can be handed
+            // back to the MMA warp (next item) before the global stores
+            uint32_t orow_regs[D];
+            if (n > 0) {
+#pragma unroll
+                for (int c2 = 0; c2 < D / 32; ++c2)
+                    tmem_ld32(t_o + 32 * c2, *reinterpret_cast<uint32_t(*)[32]>(&orow_regs[32 * c2]));
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(o_free(g));
+            } else {
+#pragma unroll
+                for (int e = 0; e < D; ++e) orow_regs[e] = 0u;
+            }
 #pragma unroll
             for (int c2 = 0; c2 < D / 32; ++c2) {
-                uint32_t o[32];
-                if (n > 0) {
-                    tmem_ld32(t_o + 32 * c2, o);
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = 0u;
-                }
+                const uint32_t* o = &orow_regs[32 * c2];
                 if (valid) {
                     if (it.pass == 0) {
                         uint4* dst = reinterpret_cast<uint4*>(
@@ -502,10 +509,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (valid) {
                 float* lse_dst = it.pass == 0 ? a.lse : a.part_lse[it.pass - 1];
                 lse_dst[(size_t)h * a.total_q + tok] = lse_v;
-            }
-            if (n > 0) {
-                tc_fence_before();
-                mbar_arrive(o_free(g));
             }
         }
         if (!ok) report_status(a.status, PCP_ERR_TIMEOUT);

@@ -14,7 +14,10 @@ namespace pcp {
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 // Keys per split of the decode kernel.
-constexpr int kDecodeChunk = 512;
+#ifndef PCP_DECODE_CHUNK
+#define PCP_DECODE_CHUNK 1024  // measured: 1024 > 512 > 256 keys per split on the mixed workload
+#endif
+constexpr int kDecodeChunk = PCP_DECODE_CHUNK;
 
 // A unit of prefill work: one 128-token tile of one row, one pass
 // (0 = the whole key range, 1 = first partial, 2 = second partial), and the
