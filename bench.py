@@ -18,6 +18,7 @@ the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -74,6 +75,33 @@ def load_peaks():
         return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
                     bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
     return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+KERNEL_SOURCES = ("attn_prefill.cu", "pcp_device.cuh", "pcp_internal.h")
+
+
+def kernel_source_hash() -> str:
+    """Hash of the prefill kernel's sources, to tell whether a stored ncu
+    traffic figure still describes the kernel being timed."""
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "context_prefill_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload_name: str):
+    """DRAM bytes per launch of the prefill kernel from the ncu capture stored in
+    profiles/traffic.json, or None if it was taken on another workload or on
+    other kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        e = json.load(f).get("prefill_kernel", {})
+    if e.get("workload") == workload_name and e.get("source_hash") == kernel_source_hash():
+        return e.get("bytes_per_launch")
+    return None
 
 
 def plan_work(rows: np.ndarray, hq: int, hkv: int, d: int):
@@ -252,7 +280,8 @@ def run_gpu(args):
                    "frac_hbm_peak": None if dec_gbs is None else round(dec_gbs / peaks["hbm"], 4),
                    "bytes": work["decode_bytes"]},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16"],
-                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
+                     "traffic": measured_traffic(spec.name),
                      "kernel": "prefill_kernel", "peak_source": f"{peaks['source']} bf16 burst"},
         "e2e": {"value": round(ws * step_flop / (e2e * 1e-3) / 1e12, 3), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e, 4)},

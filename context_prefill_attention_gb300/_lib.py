@@ -28,12 +28,18 @@ PCP_SPLIT_DUAL_CHUNK = 1
 PCP_ATTN_SEPARATE_CONTEXT = 1
 PCP_ATTN_SPLIT_AT_ROW_START = 2
 
+
+def PCP_ATTN_KV_SHARDS(n: int) -> int:
+    """Flag: compute each prefill row as n partials over n contiguous key shards
+    (decode-context-parallel emulation) and merge them by LSE."""
+    return (int(n) & 0xFF) << 8
+
 ROW_FIELDS = ("req", "shard", "q_start", "q_len", "ctx_len", "kv_end", "causal_off", "is_decode")
 
 # every symbol include/pcp.h declares
 EXPORTS = ("pcp_build_row_plan", "pcp_mask_slots_for_shard", "pcp_kv_cache_write",
            "pcp_attn_workspace_size", "pcp_attn_varlen", "pcp_attn_varlen_noalloc", "pcp_lse_merge",
-           "pcp_set_profile_events",
+           "pcp_set_profile_events", "pcp_selftest_bounded_wait",
            "pcp_last_cuda_error", "pcp_status_string")
 
 _lib = None
@@ -78,6 +84,8 @@ def load(path: Optional[str] = None):
     lib.pcp_attn_varlen_noalloc.argtypes = [P, P, P, P, i32, i32, i64, i32, P, i32, i32, i32, i32, i32, f32,
                                             P, P, i32, P, P]
     lib.pcp_attn_varlen_noalloc.restype = ctypes.c_int
+    lib.pcp_selftest_bounded_wait.argtypes = [P, ctypes.c_uint32, P]
+    lib.pcp_selftest_bounded_wait.restype = ctypes.c_int
     lib.pcp_set_profile_events.argtypes = [P, P, P, P]
     lib.pcp_set_profile_events.restype = ctypes.c_int
     lib.pcp_last_cuda_error.argtypes = []

@@ -36,8 +36,8 @@ int num_sms() {
 WorkspaceLayout workspace_layout(int32_t num_rows, int32_t total_q, int32_t num_q_heads,
                                  int32_t head_dim, int32_t max_kv_len, int32_t flags) {
     WorkspaceLayout w{};
-    const bool separate = (flags & PCP_ATTN_SEPARATE_CONTEXT) != 0;
-    const int64_t passes = separate ? 2 : 1;
+    w.nparts = attn_partials(flags) > 0 ? attn_partials(flags) : 0;
+    const int64_t passes = w.nparts > 0 ? w.nparts : 1;
     w.max_units = passes * ((int64_t)(total_q + kBlockM - 1) / kBlockM + num_rows);
     w.max_splits = max_kv_len > 0 ? (max_kv_len + kDecodeChunk - 1) / kDecodeChunk : 1;
     size_t o = 0;
@@ -51,12 +51,10 @@ WorkspaceLayout workspace_layout(int32_t num_rows, int32_t total_q, int32_t num_
     o = align256(o + (size_t)w.max_units * sizeof(Unit));
     const size_t part = (size_t)total_q * num_q_heads * head_dim * sizeof(float);
     const size_t plse = (size_t)total_q * num_q_heads * sizeof(float);
-    for (int i = 0; i < 2; ++i) {
-        w.part_out[i] = o;
-        o = align256(o + (separate ? part : 0));
-        w.part_lse[i] = o;
-        o = align256(o + (separate ? plse : 0));
-    }
+    w.part_out = o;
+    o = align256(o + (size_t)w.nparts * part);
+    w.part_lse = o;
+    o = align256(o + (size_t)w.nparts * plse);
     const size_t dec = (size_t)num_rows * num_q_heads * w.max_splits;
     w.dec_out = o;
     o = align256(o + dec * head_dim * sizeof(float));
@@ -106,6 +104,7 @@ extern "C" int pcp_kv_cache_write(const void* k, const void* v, const int64_t* s
 extern "C" size_t pcp_attn_workspace_size(int32_t num_rows, int32_t total_q, int32_t num_q_heads,
                                           int32_t head_dim, int32_t max_kv_len, int32_t flags) {
     if (num_rows < 0 || total_q < 0 || num_q_heads < 1 || head_dim < 1 || max_kv_len < 0) return 0;
+    if (attn_partials(flags) < 0) return 0;
     return workspace_layout(num_rows, total_q, num_q_heads, head_dim, max_kv_len, flags).total;
 }
 
@@ -119,7 +118,7 @@ extern "C" int pcp_attn_varlen(const void* q, const void* key_cache, const void*
     if (num_rows < 0 || total_q < 0 || num_reqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || max_blocks_per_req < 0 ||
         num_blocks < 0 || block_size < 1)
         return PCP_ERR_ARG;
-    if (flags & ~(PCP_ATTN_SEPARATE_CONTEXT | PCP_ATTN_SPLIT_AT_ROW_START)) return PCP_ERR_ARG;
+    if (attn_partials(flags) < 0) return PCP_ERR_ARG;
     if (num_q_heads % num_kv_heads != 0) return PCP_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return PCP_ERR_UNSUPPORTED;
     if (block_size != 8 && block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
@@ -160,10 +159,9 @@ extern "C" int pcp_attn_varlen(const void* q, const void* key_cache, const void*
     a.scale = scale;
     a.out = out;
     a.lse = lse;
-    for (int i = 0; i < 2; ++i) {
-        a.part_out[i] = reinterpret_cast<float*>(ws + w.part_out[i]);
-        a.part_lse[i] = reinterpret_cast<float*>(ws + w.part_lse[i]);
-    }
+    a.part_out = reinterpret_cast<float*>(ws + w.part_out);
+    a.part_lse = reinterpret_cast<float*>(ws + w.part_lse);
+    a.nparts = w.nparts;
     a.row_ok = reinterpret_cast<const int32_t*>(ws + w.row_ok);
     a.units = reinterpret_cast<const Unit*>(ws + w.units_sorted);
     a.num_units = reinterpret_cast<const int32_t*>(ws + w.header);
@@ -183,7 +181,7 @@ extern "C" int pcp_attn_varlen(const void* q, const void* key_cache, const void*
     rc = launch_prefill(a, s);
     if (rc != PCP_OK) return rc;
     if (g_profile[1]) cudaEventRecord(g_profile[1], s);
-    if (flags & PCP_ATTN_SEPARATE_CONTEXT) rc = launch_separate_merge(a, s);
+    if (a.nparts > 0) rc = launch_separate_merge(a, s);
     return rc;
 }
 

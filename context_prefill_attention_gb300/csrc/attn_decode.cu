@@ -364,33 +364,42 @@ __global__ void __launch_bounds__(D)
     if (d == 0) a.lse[(size_t)h * a.total_q + t] = W > 0.f ? M + __logf(W) : -INFINITY;
 }
 
-// LSE merge of the two prefill partials of every non-decode row.
+// LSE merge of the nparts prefill partials of every non-decode row:
+// M = max lse_i, w_i = exp(lse_i - M), out = sum w_i out_i / sum w_i,
+// lse = M + log sum w_i; parts with lse = -inf weigh 0, all -inf give (0, -inf).
 __global__ void __launch_bounds__(256)
     separate_merge_kernel(PrefillArgs a) {
     if (!a.row_ok[blockIdx.y]) return;
     const pcp_row_t row = a.rows[blockIdx.y];
     if (row.is_decode) return;
     const int D = a.d, chunks = D / 4;
+    const size_t out_stride = (size_t)a.total_q * a.hq * D, lse_stride = (size_t)a.hq * a.total_q;
     const int64_t n = (int64_t)row.q_len * a.hq * chunks;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int c = (int)(i % chunks);
         const int64_t th = i / chunks;
         const int h = (int)(th % a.hq);
         const int32_t t = row.q_start + (int32_t)(th / a.hq);
-        const float la = a.part_lse[0][(size_t)h * a.total_q + t];
-        const float lb = a.part_lse[1][(size_t)h * a.total_q + t];
+        const size_t li = (size_t)h * a.total_q + t;
         const size_t o = ((size_t)t * a.hq + h) * D + 4 * c;
+        float M = -INFINITY;
+        for (int p = 0; p < a.nparts; ++p) M = fmaxf(M, a.part_lse[p * lse_stride + li]);
         float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
         float lse = -INFINITY;
-        if (!(la == -INFINITY && lb == -INFINITY)) {
-            const float M = fmaxf(la, lb);
-            const float wa = __expf(la - M), wb = __expf(lb - M);
-            const float inv = 1.f / (wa + wb);
-            const float4 xa = *reinterpret_cast<const float4*>(a.part_out[0] + o);
-            const float4 xb = *reinterpret_cast<const float4*>(a.part_out[1] + o);
-            r = make_float4((wa * xa.x + wb * xb.x) * inv, (wa * xa.y + wb * xb.y) * inv,
-                            (wa * xa.z + wb * xb.z) * inv, (wa * xa.w + wb * xb.w) * inv);
-            lse = M + __logf(wa + wb);
+        if (M != -INFINITY) {
+            float W = 0.f;
+            for (int p = 0; p < a.nparts; ++p) {
+                const float w = __expf(a.part_lse[p * lse_stride + li] - M);
+                const float4 x = *reinterpret_cast<const float4*>(a.part_out + p * out_stride + o);
+                r.x += w * x.x;
+                r.y += w * x.y;
+                r.z += w * x.z;
+                r.w += w * x.w;
+                W += w;
+            }
+            const float inv = 1.f / W;
+            r = make_float4(r.x * inv, r.y * inv, r.z * inv, r.w * inv);
+            lse = M + __logf(W);
         }
         uint2 w;
         w.x = pack_bf16x2(r.x, r.y);

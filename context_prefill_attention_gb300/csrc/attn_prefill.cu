@@ -498,7 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             dst[v4] = w;
                         }
                     } else {
-                        float4* dst = reinterpret_cast<float4*>(a.part_out[it.pass - 1] + orow + 32 * c2);
+                        float4* dst = reinterpret_cast<float4*>(
+                            a.part_out + (size_t)(it.pass - 1) * a.total_q * a.hq * D + orow + 32 * c2);
 #pragma unroll
                         for (int v4 = 0; v4 < 8; ++v4)
                             dst[v4] = make_float4(__uint_as_float(o[4 * v4 + 0]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
@@ -507,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (valid) {
-                float* lse_dst = it.pass == 0 ? a.lse : a.part_lse[it.pass - 1];
+                float* lse_dst = it.pass == 0 ? a.lse : a.part_lse + (size_t)(it.pass - 1) * a.hq * a.total_q;
                 lse_dst[(size_t)h * a.total_q + tok] = lse_v;
             }
         }
@@ -567,7 +568,8 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     const int64_t max_kv = (int64_t)a.max_blocks * bs;
     const bool separate = (flags & PCP_ATTN_SEPARATE_CONTEXT) != 0;
     const bool at_row_start = (flags & PCP_ATTN_SPLIT_AT_ROW_START) != 0;
-    const int passes = separate ? 2 : 1;
+    const int nparts = a.nparts;             // 0: fused; 2: context + new; n: n key shards
+    const int passes = nparts > 0 ? nparts : 1;
     int32_t base = 0;
     for (int32_t r0 = 0; r0 < num_rows; r0 += kSchedThreads) {
         const int32_t ri = r0 + threadIdx.x;
@@ -587,13 +589,21 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
         const int32_t off = base + block_exclusive_scan(cnt, warp_sums, &tot);
         for (int32_t u = 0; u < cnt; ++u) {
             if (off + u >= max_units) break;
-            const int32_t mt = u / passes, pass = separate ? 1 + u % passes : 0;
-            const int32_t split = at_row_start ? row.kv_end - row.q_len : row.ctx_len;
+            const int32_t mt = u / passes, pass = nparts > 0 ? 1 + u % passes : 0;
             Unit x;
             x.row = ri;
             x.mt_pass = mt | (pass << 24);
-            x.k_lo = pass == 2 ? split : 0;
-            x.k_hi = pass == 1 ? split : row.kv_end;
+            if (separate) {  // context [0, split) and new tokens [split, kv_end)
+                const int32_t split = at_row_start ? row.kv_end - row.q_len : row.ctx_len;
+                x.k_lo = pass == 2 ? split : 0;
+                x.k_hi = pass == 1 ? split : row.kv_end;
+            } else if (nparts > 0) {  // key shard pass - 1 of nparts: contiguous, floor bounds
+                x.k_lo = (int32_t)((int64_t)row.kv_end * (pass - 1) / nparts);
+                x.k_hi = (int32_t)((int64_t)row.kv_end * pass / nparts);
+            } else {
+                x.k_lo = 0;
+                x.k_hi = row.kv_end;
+            }
             units[off + u] = x;
         }
         base += tot;

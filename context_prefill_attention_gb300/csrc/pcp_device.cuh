@@ -66,9 +66,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete. Returns false (after
-// setting *abort) when it has not completed within kWaitTimeoutNs or when
-// another role of the CTA has already given up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+// setting *abort) when it has not completed within timeout_ns or when another
+// role of the CTA has already given up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint64_t timeout_ns = kWaitTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
@@ -76,7 +77,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        if (global_timer_ns() - t0 > timeout_ns) {
             *abort = 1;
             return false;
         }
@@ -85,8 +86,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 
 // The same wait for a whole warp: every lane polls, and the warp agrees on the
 // outcome so that it stays converged for warp-collective instructions.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort) {
-    const bool ok = mbar_wait(bar, parity, abort);
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort,
+                                               uint64_t timeout_ns = kWaitTimeoutNs) {
+    const bool ok = mbar_wait(bar, parity, abort, timeout_ns);
     return __all_sync(0xffffffffu, ok);
 }
 

@@ -35,14 +35,24 @@ struct WorkspaceLayout {
     size_t row_ok;        // int32[num_rows]: 1 for a row that passed the checks
     size_t units;         // Unit[max_units], unsorted
     size_t units_sorted;  // Unit[max_units], longest first
-    size_t part_out[2];   // fp32 [T][Hq][D] each (separate-context mode)
-    size_t part_lse[2];   // fp32 [Hq][T] each
+    size_t part_out;      // nparts x fp32 [T][Hq][D] (separate-context / KV-shard modes)
+    size_t part_lse;      // nparts x fp32 [Hq][T]
+    int32_t nparts;
     size_t dec_out;       // fp32 [num_rows][Hq][max_splits][D]
     size_t dec_lse;       // fp32 [num_rows][Hq][max_splits]
     size_t total;
     int64_t max_units;
     int32_t max_splits;
 };
+
+// Number of partial passes a flags word asks for (0: fused), or -1 if invalid.
+inline int32_t attn_partials(int32_t flags) {
+    const int32_t shards = (flags >> 8) & 0xFF;
+    const bool separate = (flags & PCP_ATTN_SEPARATE_CONTEXT) != 0;
+    if (flags & ~(PCP_ATTN_SEPARATE_CONTEXT | PCP_ATTN_SPLIT_AT_ROW_START | 0xFF00)) return -1;
+    if (shards == 1 || shards > 64 || (shards && separate)) return -1;
+    return separate ? 2 : shards;
+}
 
 WorkspaceLayout workspace_layout(int32_t num_rows, int32_t total_q, int32_t num_q_heads,
                                  int32_t head_dim, int32_t max_kv_len, int32_t flags);
@@ -66,8 +76,9 @@ struct PrefillArgs {
     float scale;
     void* out;
     float* lse;
-    float* part_out[2];
-    float* part_lse[2];
+    float* part_out;   // partial p (1-based pass p) at part_out + (p - 1) * total_q * hq * d
+    float* part_lse;   // ... at part_lse + (p - 1) * hq * total_q
+    int32_t nparts;    // 0: one fused pass straight into out / lse
     const int32_t* row_ok;
     const Unit* units;
     const int32_t* num_units;

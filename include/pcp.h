@@ -78,6 +78,11 @@ typedef struct CUstream_st* pcp_stream_t; /* == cudaStream_t */
                                         partials in the workspace and merge them by LSE */
 #define PCP_ATTN_SPLIT_AT_ROW_START 2 /* with SEPARATE_CONTEXT: split each row at its own
                                         start instead of at the cached prefix */
+/* Decode-context-parallel emulation: each prefill row is computed as n partials over n
+ * contiguous shards of its keys [0, kv_end) — what n DCP ranks holding those key shards
+ * would each compute — and the partials are merged by LSE in the same call
+ * (2 <= n <= 64; not combinable with PCP_ATTN_SEPARATE_CONTEXT). */
+#define PCP_ATTN_KV_SHARDS(n) (((n) & 0xFF) << 8)
 
 /* One row of the plan: a contiguous run of one request's new tokens that one
  * shard evaluates. All fields are int32.
@@ -188,8 +193,12 @@ size_t pcp_attn_workspace_size(int32_t num_rows, int32_t total_q, int32_t num_q_
  * flags: 0 computes every row in one online softmax; PCP_ATTN_SEPARATE_CONTEXT
  * computes the context part and the new-token part as two partial results in
  * the workspace and merges them by LSE (a part with no keys has lse = -inf and
- * out = 0); PCP_ATTN_SPLIT_AT_ROW_START moves the split point to the row start.
- * Supported: head_dim 64 or 128, block_size in {16, 32, 64, 128}, Hq % Hkv == 0.
+ * out = 0); PCP_ATTN_SPLIT_AT_ROW_START moves the split point to the row start;
+ * PCP_ATTN_KV_SHARDS(n) computes n partials over n contiguous key shards and
+ * merges them (decode rows are always split-KV internally; flags do not change
+ * their result). Every mode gives the same attention up to rounding.
+ * Supported: head_dim 64 or 128, block_size in {8, 16, 32, 64, 128},
+ * Hq % Hkv == 0 with Hq / Hkv <= 16.
  * Rows with an out-of-range page id are skipped in part and set *status =
  * PCP_ERR_RANGE; a device wait that runs out sets PCP_ERR_TIMEOUT.
  * Errors (nothing launched): PCP_ERR_ARG, PCP_ERR_ALIGN, PCP_ERR_UNSUPPORTED,
@@ -255,6 +264,17 @@ int pcp_lse_merge(const float* out_a, const float* lse_a, const float* out_b, co
  */
 int pcp_set_profile_events(void* prefill_begin, void* prefill_end, void* decode_begin,
                            void* decode_end);
+
+/*
+ * pcp_selftest_bounded_wait — device. A failure-detection self-test with no
+ * counterpart in the pages: one warp waits on an mbarrier phase that nothing
+ * completes, using the same bounded wait as the attention kernels, gives up
+ * after timeout_us microseconds and sets *status = PCP_ERR_TIMEOUT. It checks
+ * that a stuck pipeline ends with an error status and a usable context instead
+ * of a hang. status: device int32 (zero it first). timeout_us in [1, 1e6].
+ * Errors: PCP_ERR_ARG, PCP_ERR_CUDA.
+ */
+int pcp_selftest_bounded_wait(int32_t* status, uint32_t timeout_us, pcp_stream_t stream);
 
 /* The cudaError_t value of the last failed CUDA call in this thread (0 if none). */
 int pcp_last_cuda_error(void);

@@ -129,6 +129,11 @@ def test_attn_varlen_validates_before_launch(P):
     assert _attn(lib, q=None) == P.PCP_ERR_ARG
     assert _attn(lib, nrows=-1) == P.PCP_ERR_ARG
     assert _attn(lib, flags=8) == P.PCP_ERR_ARG
+    assert _attn(lib, flags=P.PCP_ATTN_KV_SHARDS(1)) == P.PCP_ERR_ARG
+    assert _attn(lib, flags=P.PCP_ATTN_KV_SHARDS(65)) == P.PCP_ERR_ARG
+    assert _attn(lib, flags=P.PCP_ATTN_SEPARATE_CONTEXT | P.PCP_ATTN_KV_SHARDS(2)) == P.PCP_ERR_ARG
+    assert P.pcp_attn_workspace_size(2, 100, 8, 128, 64, P.PCP_ATTN_KV_SHARDS(4)) > \
+        P.pcp_attn_workspace_size(2, 100, 8, 128, 64, P.PCP_ATTN_KV_SHARDS(2))
     assert _attn(lib, q=FAKE + 8) == P.PCP_ERR_ALIGN
     assert _attn(lib, ws=FAKE + 16) == P.PCP_ERR_ALIGN
     assert _attn(lib, wsb=100) == P.PCP_ERR_WORKSPACE

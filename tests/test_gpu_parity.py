@@ -94,6 +94,33 @@ def test_small_cases_match_oracle(name, flags):
     assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
 
 
+@pytest.mark.parametrize("shards", [2, 3, 5])
+@pytest.mark.parametrize("name", ["ragged_d128", "prefix", "mixed_decode", "gqa3_odd", "many_reqs", "bs32"])
+def test_kv_shard_partials_match_oracle(name, shards):
+    """Decode-context-parallel emulation: every row's keys in `shards` contiguous
+    shards, one partial each, merged by LSE — the same attention."""
+    import context_prefill_attention_gb300 as P
+    c = SMALL[name]
+    spec = W.custom_spec(c["q"], c["p"], num_q_heads=c["hq"], num_kv_heads=c["hkv"], head_dim=c["d"],
+                         block_size=c.get("bs", 16), num_shards=c.get("s", 2), split_mode=c.get("mode", 0),
+                         seed=hash(name) % 100000 + shards)
+    case = Case(spec, flags=P.PCP_ATTN_KV_SHARDS(shards))
+    out, lse = case.run()
+    eo, el = case.compare(out, lse)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+
+
+def test_workload3_kv_shards_matches_oracle():
+    import context_prefill_attention_gb300 as P
+    spec = W.workload_spec(3)
+    case = Case(spec, flags=P.PCP_ATTN_KV_SHARDS(4))
+    out, lse = case.run()
+    segs = shard_segments(case.plan["rows"])
+    tokens = W.sample_segments(segs, 48, spec.seed + 13).numpy()
+    eo, el = case.compare(out, lse, tokens)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+
+
 def test_separate_context_with_empty_prefix_merges_to_new_part():
     """Rows without a cached prefix have an empty context pass (lse = -inf);
     the merge must return the new-token part unchanged (the 'context pass
