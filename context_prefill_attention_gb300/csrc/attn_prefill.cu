@@ -55,6 +55,13 @@ constexpr int kMmaWarp = 9;
 // polynomial only costs issue slots (measured: 1 pair in 4 -> 9% slower).
 #define PCP_POLY_EXP_EVERY 1000000
 #endif
+#ifndef PCP_PV_SPLIT
+#define PCP_PV_SPLIT 0
+#endif
+// 1: O += P V is issued in two halves, the first as soon as the softmax has
+// written keys 0-63 of P; 0: one issue after all of P is written. Measured on
+// GB300: the split is 4-5 % slower (an extra handshake per tile), so it is off.
+constexpr bool kPvSplit = PCP_PV_SPLIT != 0;
 constexpr int kNK = PCP_PREFILL_K_STAGES;  // K stages
 constexpr int kNV = PCP_PREFILL_V_STAGES;  // V stages
 constexpr float kLog2e = 1.4426950408889634f;
@@ -72,9 +79,9 @@ struct Cfg {
     static constexpr int kK = kQ + 2 * kTileBytes;
     static constexpr int kV = kK + kNK * kTileBytes;
     static constexpr int kBar = kV + kNV * kTileBytes;
-    static constexpr int kNumBars = 2 + 2 * kNK + 2 * kNV + 8;
-    static constexpr int kMisc = kBar + kNumBars * 8;      // tmem address, abort flag
-    static constexpr int kSmem = kMisc + 16 + 1024;        // + alignment slack
+    static constexpr int kNumBars = 2 + 2 * kNK + 2 * kNV + 8 + 2;
+    static constexpr int kMisc = kBar + kNumBars * 8;      // tmem address, abort flag, item ring
+    static constexpr int kSmem = kMisc + 16 + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 512;
     __host__ __device__ static constexpr uint32_t tmem_s(int g) { return g ? 128u : 0u; }
     __host__ __device__ static constexpr uint32_t tmem_o(int g) { return g ? 256u + D : 256u; }
@@ -131,9 +138,9 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_smem, uint3
 // O (+)= P V: P from TMEM (bf16 pairs in the S columns), V MN-major in shared memory.
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_smem,
-                                         bool accumulate) {
+                                         bool accumulate, int ks_begin, int ks_end) {
 #pragma unroll
-    for (int ks = 0; ks < kBlockN / 16; ++ks) {
+    for (int ks = ks_begin; ks < ks_end; ++ks) {
         const uint64_t b = sdesc_sw128(v_smem + ks * 2048, Cfg<D>::kHalfBytes, 1024);
         mma_ts(tmem_o, tmem_p + ks * 8, b, Cfg<D>::kIdescO, (accumulate || ks > 0) ? 1u : 0u);
     }
@@ -160,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto p_full = [&](int g) { return bx + 16 + 8 * g; };
     auto o_done = [&](int g) { return bx + 32 + 8 * g; };
     auto o_free = [&](int g) { return bx + 48 + 8 * g; };
+    auto p_half = [&](int g) { return bx + 64 + 8 * g; };  // first 64 keys of P ready
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
 
@@ -179,6 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(p_full(g), 128);
             mbar_init(o_done(g), 1);
             mbar_init(o_free(g), 128);
+            mbar_init(p_half(g), 128);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -197,6 +206,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int32_t total_items = (*a.num_units) * slots_per_unit;
+    // Item of this CTA in round r: the longest-first list is dealt out in snake
+    // order (forward on even rounds, backward on odd ones), which balances the
+    // per-CTA totals far better than plain round robin, with no atomics.
+    auto item_of_round = [&](int32_t r) -> int32_t {
+        return r * (int32_t)gridDim.x + ((r & 1) ? (int32_t)(gridDim.x - 1 - blockIdx.x) : (int32_t)blockIdx.x);
+    };
     // Registers: the launch gives 168 per thread (384 threads); the producer /
     // MMA warpgroup gives back to 120 so the softmax warpgroups can hold a full
     // 128-column score row (192): 128 x 120 + 256 x 192 = 384 x 168. setmaxnreg
@@ -215,7 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t oob = (int32_t)(a.num_blocks * bs);  // a row past the cache: zero fill
         const int pages = kBlockN / bs;
         bool ok = true;
-        for (int32_t idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+        for (int32_t round = 0; ok; ++round) {
+            const int32_t idx = item_of_round(round);
+            if (idx >= total_items) break;
             const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, bs);
             if (it.n_tiles == 0) continue;
             if (c > 0 && !(ok = mbar_wait_warp(q_empty, (c - 1) & 1, abort_flag))) break;
@@ -266,7 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pph[2] = {0, 0}, nslot_items[2] = {0, 0};
         bool ok = true;
         const bool leader = lane == 0;
-        for (int32_t idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+        for (int32_t round = 0; ok; ++round) {
+            const int32_t idx = item_of_round(round);
+            if (idx >= total_items) break;
             const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, bs);
             const int n = it.n_tiles;
             if (n == 0) continue;
@@ -303,15 +322,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                 }
                 for (int g = 0; g < it.nslots && ok; ++g) {
-                    if (!(ok = mbar_wait_warp(p_full(g), pph[g], abort_flag))) break;
-                    pph[g] ^= 1;
+                    // O += P V in two halves: keys 0-63 as soon as the softmax has written
+                    // that half of P, keys 64-127 when all of P is there
+                    const int ks_mid = kPvSplit ? kBlockN / 32 : 0;
+                    if (!(ok = mbar_wait_warp(kPvSplit ? p_half(g) : p_full(g), pph[g], abort_flag))) break;
                     if (j == 0 && nslot_items[g] > 0) {
                         if (!(ok = mbar_wait_warp(o_free(g), (nslot_items[g] - 1) & 1, abort_flag))) break;
                     }
                     tc_fence_after();
+                    if (leader && ks_mid > 0)
+                        issue_pv<D>(tmem + C::tmem_o(g), tmem + C::tmem_s(g),
+                                    sbase + C::kV + vs * C::kTileBytes, j > 0, 0, ks_mid);
+                    if (kPvSplit) {
+                        if (!(ok = mbar_wait_warp(p_full(g), pph[g], abort_flag))) break;
+                        tc_fence_after();
+                    }
+                    pph[g] ^= 1;
                     if (leader)
                         issue_pv<D>(tmem + C::tmem_o(g), tmem + C::tmem_s(g),
-                                    sbase + C::kV + vs * C::kTileBytes, j > 0);
+                                    sbase + C::kV + vs * C::kTileBytes, j > 0, ks_mid, kBlockN / 16);
                     if (g == it.nslots - 1 && leader) mma_commit(v_empty(vs));
                     if (j + 1 < n) {
                         if (g == 0) {
@@ -352,7 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl2 = a.scale * kLog2e;
         uint32_t sph = 0, oph = 0;
         bool ok = true;
-        for (int32_t idx = blockIdx.x; idx < total_items && ok; idx += gridDim.x) {
+        for (int32_t round = 0; ok; ++round) {
+            const int32_t idx = item_of_round(round);
+            if (idx >= total_items) break;
             const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, bs);
             if (g >= it.nslots) continue;
             const int h = it.h0 + g;
@@ -410,10 +441,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const float mu = (m == -INFINITY) ? 0.f : m;
+                // O must be rescaled before the first half of this tile's PV runs (16
+                // columns at a time: the score row is still live in registers)
+                if (rescale) {
+#pragma unroll 1
+                    for (int c2 = 0; c2 < D / 16; ++c2) {
+                        uint32_t o[16];
+                        tmem_ld16(t_o + 16 * c2, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st16(t_o + 16 * c2, o);
+                    }
+                }
                 // p = 2^(s * scale * log2 e - m), two lanes per instruction. With the
                 // polynomial knob on, every kPolyEvery-th pair goes to the FMA pipe (a
                 // masked key then gets ~1e-38, not 0); by default all use ex2.
-                // P is written back to TMEM in two halves to bound register pressure.
+                // P goes back to TMEM in two halves (keys 0-63, then 64-127); the MMA warp
+                // starts O += P V on the first half while the second is computed.
                 const float2 sl2v = make_float2(sl2, sl2), nmu = make_float2(-mu, -mu);
                 float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f)};
@@ -435,26 +481,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p[c3] = pack_bf16x2(e.x, e.y);
                     }
                     tmem_st32(t_s + 32 * half, p);
+                    if (kPvSplit || half == 1) {
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(half == 0 ? p_half(g) : p_full(g));
+                    }
                 }
                 const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
                 const float2 a03 = fadd2(a01, a23);
-                const float rs = a03.x + a03.y;
-                if (rescale) {
-#pragma unroll
-                    for (int c2 = 0; c2 < D / 32; ++c2) {
-                        uint32_t o[32];
-                        tmem_ld32(t_o + 32 * c2, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(t_o + 32 * c2, o);
-                    }
-                }
-                l += rs;
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(p_full(g));
+                l += a03.x + a03.y;
             }
             if (!ok) break;
             // ---- epilogue: out = O / l, lse = ln 2 * (m + log2 l)

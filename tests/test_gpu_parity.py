@@ -3,6 +3,8 @@
 Bit-exact: cache contents. Floating point: max |out - oracle| <= 1e-2 and
 max |lse - oracle| <= 1e-3 over every compared (token, head).
 """
+import zlib
+
 import numpy as np
 import pytest
 import torch
@@ -87,7 +89,7 @@ def test_small_cases_match_oracle(name, flags):
     c = SMALL[name]
     spec = W.custom_spec(c["q"], c["p"], num_q_heads=c["hq"], num_kv_heads=c["hkv"], head_dim=c["d"],
                          block_size=c.get("bs", 16), num_shards=c.get("s", 2), split_mode=c.get("mode", 0),
-                         seed=hash(name) % 100000)
+                         seed=zlib.crc32(name.encode()) % 100000)
     case = Case(spec, flags=flags)
     out, lse = case.run()
     eo, el = case.compare(out, lse)
@@ -103,7 +105,7 @@ def test_kv_shard_partials_match_oracle(name, shards):
     c = SMALL[name]
     spec = W.custom_spec(c["q"], c["p"], num_q_heads=c["hq"], num_kv_heads=c["hkv"], head_dim=c["d"],
                          block_size=c.get("bs", 16), num_shards=c.get("s", 2), split_mode=c.get("mode", 0),
-                         seed=hash(name) % 100000 + shards)
+                         seed=zlib.crc32(name.encode()) % 100000 + shards)
     case = Case(spec, flags=P.PCP_ATTN_KV_SHARDS(shards))
     out, lse = case.run()
     eo, el = case.compare(out, lse)
@@ -232,3 +234,44 @@ def test_workload3_separate_context_matches_oracle():
     tokens = W.sample_segments(segs, 64, spec.seed + 12).numpy()
     eo, el = case.compare(out, lse, tokens)
     assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+
+
+# ------------------------------------------------------------ edge cases
+
+EDGE = {
+    "all_decode": dict(q=[1, 1, 1, 1, 1], p=[5, 900, 33, 1, 2048], hq=8, hkv=2, d=128),
+    "one_shard": dict(q=[300, 1, 77], p=[0, 40, 200], hq=4, hkv=2, d=128, s=1),
+    "request_without_new_tokens": dict(q=[0, 150, 0, 1], p=[64, 10, 30, 99], hq=4, hkv=2, d=128),
+    "gqa16": dict(q=[140, 1], p=[9, 300], hq=16, hkv=1, d=128),
+    "gqa16_d64": dict(q=[140, 1], p=[9, 300], hq=32, hkv=2, d=64),
+    "eight_shards_dual": dict(q=[1000], p=[3], hq=4, hkv=2, d=64, s=8, mode=1),
+    "tile_exact": dict(q=[256, 128], p=[128, 0], hq=4, hkv=2, d=128),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE))
+def test_edge_cases_match_oracle(name):
+    c = EDGE[name]
+    spec = W.custom_spec(c["q"], c["p"], num_q_heads=c["hq"], num_kv_heads=c["hkv"], head_dim=c["d"],
+                         block_size=c.get("bs", 16), num_shards=c.get("s", 2), split_mode=c.get("mode", 0),
+                         seed=zlib.crc32(name.encode()) % 100000)
+    case = Case(spec)
+    out, lse = case.run()
+    eo, el = case.compare(out, lse)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+
+
+def test_empty_plan_and_empty_batch_launch_nothing():
+    P = _P()
+    q = torch.zeros((4, 2, 128), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((2, 16, 1, 128), dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros((1, 2), dtype=torch.int32, device="cuda")
+    rows = torch.zeros((0, 8), dtype=torch.int32, device="cuda")
+    out = torch.full_like(q, 7.0)
+    lse = torch.full((2, 4), 7.0, device="cuda")
+    P.pcp_attn_varlen(q, kc, kc, bt, rows, 0.1, out=out, lse=lse,
+                      workspace=torch.empty(256, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.all(out.float() == 7.0) and torch.all(lse == 7.0)
+    plan = P.pcp_build_row_plan([0, 0], [3, 0], np.zeros((2, 1), np.int32), 16, 2)
+    assert plan["rows"].shape[0] == 0 and plan["slot_mapping"].shape[0] == 0
