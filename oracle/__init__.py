@@ -51,6 +51,16 @@ def _load():
         lib.oracle_attention.restype = i32
         lib.oracle_lse_merge.argtypes = [P, P, P, P, i64, i32, P, P]
         lib.oracle_lse_merge.restype = None
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = dbl
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_decode_array.argtypes = [P, i64, P]
+        lib.oracle_e4m3_decode_array.restype = None
+        lib.oracle_cache_write_fp8.argtypes = [P, P, i64, P, i64, i32, ctypes.c_float]
+        lib.oracle_cache_write_fp8.restype = i32
+        lib.oracle_attention_f64kv.argtypes = [i32, P, P, P, P, P, P, P, i32, i32, i32, dbl, P, i64, P, P]
+        lib.oracle_attention_f64kv.restype = i32
         _lib = lib
     return _lib
 
@@ -189,6 +199,61 @@ def lse_merge(out_a, lse_a, out_b, lse_b):
     lse = np.zeros(la.shape, dtype=np.float64)
     lib.oracle_lse_merge(_ptr(oa), _ptr(la), _ptr(ob), _ptr(lb), n, D, _ptr(out), _ptr(lse))
     return out, lse
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values of e4m3 codes (uint8 array, any shape) as float64; NaN codes give NaN."""
+    lib = _load()
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.zeros(c.shape, dtype=np.float64)
+    lib.oracle_e4m3_decode_array(_ptr(c), int(c.size), _ptr(out))
+    return out
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest e4m3 code of a float32 (ties to even, saturating at 448)."""
+    return int(_load().oracle_e4m3_encode(float(x)))
+
+
+def cache_write_fp8(src, slot, cache: np.ndarray, scale: float) -> int:
+    """FP8 cache write (see ``oracle_cache_write_fp8``): ``cache[slot[t]] =
+    e4m3(src[t] / scale)`` for ``slot[t] >= 0``, in place. ``cache`` is a uint8
+    numpy array ``[num_blocks, bs, H, D]``. Returns the C status."""
+    lib = _load()
+    s = _u16(src)
+    sl = np.ascontiguousarray(np.asarray(slot, dtype=np.int64))
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous
+    row = int(np.prod(s.shape[1:])) if s.ndim > 1 else 1
+    num_slots = cache.size // row
+    return int(lib.oracle_cache_write_fp8(_ptr(s), _ptr(sl), int(sl.shape[0]), _ptr(cache), num_slots, row,
+                                          float(scale)))
+
+
+def attention_f64kv(rows, q, kv_k, kv_v, kv_off, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                    scale: float, tokens, key_lo=None, key_hi=None, part: str = "fused"):
+    """``attention`` with every request's keys and values given as float64
+    arrays ``[L_total, Hkv, D]`` (for an FP8 cache: the codes' values times the
+    request's per-kv-head descale)."""
+    lib = _load()
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 8))
+    if key_lo is None or key_hi is None:
+        key_lo, key_hi = key_ranges(rows, part)
+    key_lo = np.ascontiguousarray(np.asarray(key_lo, dtype=np.int64))
+    key_hi = np.ascontiguousarray(np.asarray(key_hi, dtype=np.int64))
+    qa = _u16(q)
+    ka = np.ascontiguousarray(np.asarray(kv_k, dtype=np.float64))
+    va = np.ascontiguousarray(np.asarray(kv_v, dtype=np.float64))
+    off = np.ascontiguousarray(np.asarray(kv_off, dtype=np.int64))
+    tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+    n = int(tok.shape[0])
+    out = np.zeros((max(n, 1), num_q_heads, head_dim), dtype=np.float64)
+    lse = np.zeros((max(n, 1), num_q_heads), dtype=np.float64)
+    rc = lib.oracle_attention_f64kv(int(rows.shape[0]), _ptr(rows), _ptr(key_lo), _ptr(key_hi), _ptr(qa),
+                                    _ptr(ka), _ptr(va), _ptr(off), num_q_heads, num_kv_heads, head_dim,
+                                    float(scale), _ptr(tok), n, _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise OracleError(rc, "oracle_attention_f64kv")
+    return out[:n], lse[:n]
 
 
 def workload_kv(spec, device: str = "cpu"):

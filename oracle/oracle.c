@@ -19,6 +19,9 @@
  *    skipped, decode rows are written by rank 0 only; section "What made it
  *    removable": a row's seq_len is its end position, seq_len - query_len is the
  *    row start.
+ *  - "[MRv2] FlashAttention PCP support ...", the context-pass call: FP8 KV
+ *    cache descales of shape (num_seqs, num_kv_heads) built from the layer's
+ *    k/v scales; the e4m3 format itself is the OCP 8-bit floating point one.
  *
  * Every function here is pinned by CPU tests against brute force (a dense
  * numpy softmax), closed forms and the invariants the pages fix.
@@ -271,4 +274,146 @@ void oracle_lse_merge(const double* out_a, const double* lse_a, const double* ou
             o[d] = (wa * out_a[(size_t)i * D + d] + wb * out_b[(size_t)i * D + d]) / (wa + wb);
         lse[i] = m + log(wa + wb);
     }
+}
+
+/*
+ * FP8 (e4m3) KV cache ("[MRv2] FlashAttention PCP support for GQA on MRv2": the
+ * context-pass call carries FP8 descales of shape (num_seqs, num_kv_heads)
+ * and the layer's k/v scales).
+ *
+ * e4m3 as defined by the OCP 8-bit floating point format (the "fn" variant):
+ * 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0
+ * encodes subnormals m * 2^-9; there is no infinity, S.1111.111 is NaN, and the
+ * largest finite magnitude is 1.75 * 2^8 = 448.
+ */
+double oracle_e4m3_decode(uint8_t c) {
+    const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double mag = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+/* Round a float to the nearest e4m3 value, ties to even, magnitudes above 448
+ * saturating to 448 (NaN stays NaN). Found by exhaustive search over the 127
+ * non-negative finite codes: plain and obviously correct, not fast. */
+uint8_t oracle_e4m3_encode(float x) {
+    if (x != x) return 0x7F;
+    const uint8_t sign = (x < 0.0f || (x == 0.0f && signbit(x))) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;
+    uint8_t best = 0;
+    double best_err = a;  /* code 0 is +0 */
+    for (int c = 1; c <= 0x7E; ++c) {
+        const double v = oracle_e4m3_decode((uint8_t)c);
+        const double err = fabs(v - a);
+        /* strictly closer wins; on a tie the even code (mantissa lsb 0) wins */
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = (uint8_t)c;
+            best_err = err;
+        }
+    }
+    return sign | best;
+}
+
+/*
+ * FP8 cache write: code = e4m3(x / scale) with x the bf16 value and the
+ * division done in fp32 (correctly rounded), scale = k_scale for keys and
+ * v_scale for values; negative slots skipped; cache is [num_slots][row_elems]
+ * bytes. Returns ORC_ERR_RANGE for a slot past the end.
+ */
+int oracle_cache_write_fp8(const uint16_t* src, const int64_t* slot, int64_t num_tokens, uint8_t* cache,
+                           int64_t num_slots, int row_elems, float scale) {
+    int rc = ORC_OK;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t s = slot[t];
+        if (s < 0) continue;
+        if (s >= num_slots) { rc = ORC_ERR_RANGE; continue; }
+        for (int e = 0; e < row_elems; ++e) {
+            const float x = (float)bf16_to_double(src[(size_t)t * row_elems + e]);
+            const float q = x / scale;
+            cache[(size_t)s * row_elems + e] = oracle_e4m3_encode(q);
+        }
+    }
+    return rc;
+}
+
+/* out[i] = the e4m3 value of codes[i] (exact in double). */
+void oracle_e4m3_decode_array(const uint8_t* codes, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(codes[i]);
+}
+
+/* attend_token for keys and values given as doubles [L][Hkv][D]. */
+static void attend_token_f64(const uint16_t* q_tok, const double* k, const double* v, int64_t pos,
+                             int64_t k_lo, int64_t k_hi, int Hq, int Hkv, int D, double scale,
+                             double* out, double* lse, double* s_buf) {
+    int G = Hq / Hkv;
+    int64_t hi = k_hi < pos + 1 ? k_hi : pos + 1;
+    int64_t lo = k_lo > 0 ? k_lo : 0;
+    for (int h = 0; h < Hq; ++h) {
+        int hk = h / G;
+        double* o = out + (size_t)h * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        if (hi <= lo) { lse[h] = -INFINITY; continue; }
+        double m = -INFINITY;
+        for (int64_t kk = lo; kk < hi; ++kk) {
+            const double* kr = k + ((size_t)kk * Hkv + hk) * D;
+            const uint16_t* qr = q_tok + (size_t)h * D;
+            double s = 0.0;
+            for (int d = 0; d < D; ++d) s += bf16_to_double(qr[d]) * kr[d];
+            s *= scale;
+            s_buf[kk - lo] = s;
+            if (s > m) m = s;
+        }
+        double sum = 0.0;
+        for (int64_t kk = lo; kk < hi; ++kk) sum += exp(s_buf[kk - lo] - m);
+        double l = m + log(sum);
+        lse[h] = l;
+        for (int64_t kk = lo; kk < hi; ++kk) {
+            double w = exp(s_buf[kk - lo] - l);
+            const double* vr = v + ((size_t)kk * Hkv + hk) * D;
+            for (int d = 0; d < D; ++d) o[d] += w * vr[d];
+        }
+    }
+}
+
+/* oracle_attention with every request's keys and values given as doubles
+ * (for the FP8 cache: the dequantized codes). Same arguments otherwise. */
+int oracle_attention_f64kv(int num_rows, const int32_t* rows, const int64_t* key_lo, const int64_t* key_hi,
+                           const uint16_t* q, const double* kv_k, const double* kv_v, const int64_t* kv_off,
+                           int Hq, int Hkv, int D, double scale, const int64_t* tokens, int64_t n_tok,
+                           double* out, double* lse) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || D <= 0) return ORC_ERR_ARG;
+    int64_t max_len = 1;
+    for (int i = 0; i < num_rows; ++i) {
+        int64_t e = rows[(size_t)i * F_NFIELDS + F_KVEND];
+        if (e > max_len) max_len = e;
+    }
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* s_buf = (double*)malloc(sizeof(double) * (size_t)max_len);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < n_tok; ++i) {
+            int64_t t = tokens[i];
+            int found = -1;
+            for (int r = 0; r < num_rows; ++r) {
+                const int32_t* row = rows + (size_t)r * F_NFIELDS;
+                if (t >= row[F_QSTART] && t < (int64_t)row[F_QSTART] + row[F_QLEN]) { found = r; break; }
+            }
+            if (found < 0 || !s_buf) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            const int32_t* row = rows + (size_t)found * F_NFIELDS;
+            int64_t j = t - row[F_QSTART];
+            int64_t pos = (int64_t)row[F_KVEND] - row[F_QLEN] + j;
+            int64_t base = kv_off[row[F_REQ]];
+            attend_token_f64(q + (size_t)t * Hq * D, kv_k + (size_t)base * Hkv * D, kv_v + (size_t)base * Hkv * D,
+                             pos, key_lo[found], key_hi[found], Hq, Hkv, D, scale,
+                             out + (size_t)i * Hq * D, lse + (size_t)i * Hq, s_buf);
+        }
+        free(s_buf);
+    }
+    return bad ? ORC_ERR_ARG : ORC_OK;
 }
