@@ -59,8 +59,8 @@ def _load():
         lib.oracle_e4m3_decode_array.restype = None
         lib.oracle_cache_write_fp8.argtypes = [P, P, i64, P, i64, i32, ctypes.c_float]
         lib.oracle_cache_write_fp8.restype = i32
-        lib.oracle_attention_f64kv.argtypes = [i32, P, P, P, P, P, P, P, i32, i32, i32, dbl, P, i64, P, P]
-        lib.oracle_attention_f64kv.restype = i32
+        lib.oracle_attention_fp8kv.argtypes = [i32, P, P, P, P, P, P, P, P, P, i32, i32, i32, dbl, P, i64, P, P]
+        lib.oracle_attention_fp8kv.restype = i32
         _lib = lib
     return _lib
 
@@ -229,11 +229,13 @@ def cache_write_fp8(src, slot, cache: np.ndarray, scale: float) -> int:
                                           float(scale)))
 
 
-def attention_f64kv(rows, q, kv_k, kv_v, kv_off, num_q_heads: int, num_kv_heads: int, head_dim: int,
-                    scale: float, tokens, key_lo=None, key_hi=None, part: str = "fused"):
-    """``attention`` with every request's keys and values given as float64
-    arrays ``[L_total, Hkv, D]`` (for an FP8 cache: the codes' values times the
-    request's per-kv-head descale)."""
+def attention_fp8kv(rows, q, codes_k, codes_v, kv_off, k_descale, v_descale, num_q_heads: int,
+                    num_kv_heads: int, head_dim: int, scale: float, tokens, key_lo=None, key_hi=None,
+                    part: str = "fused"):
+    """``attention`` over an FP8 cache (see ``oracle_attention_fp8kv``): every
+    request's e4m3 key/value codes back to back (uint8 ``[L_total, Hkv, D]``,
+    request r from token ``kv_off[r]``) and float32 descales ``[num_reqs, Hkv]``;
+    key k of head g is value(code) * k_descale[r][g]."""
     lib = _load()
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 8))
     if key_lo is None or key_hi is None:
@@ -241,18 +243,20 @@ def attention_f64kv(rows, q, kv_k, kv_v, kv_off, num_q_heads: int, num_kv_heads:
     key_lo = np.ascontiguousarray(np.asarray(key_lo, dtype=np.int64))
     key_hi = np.ascontiguousarray(np.asarray(key_hi, dtype=np.int64))
     qa = _u16(q)
-    ka = np.ascontiguousarray(np.asarray(kv_k, dtype=np.float64))
-    va = np.ascontiguousarray(np.asarray(kv_v, dtype=np.float64))
+    ka = np.ascontiguousarray(np.asarray(codes_k, dtype=np.uint8))
+    va = np.ascontiguousarray(np.asarray(codes_v, dtype=np.uint8))
+    kd = np.ascontiguousarray(np.asarray(k_descale, dtype=np.float32))
+    vd = np.ascontiguousarray(np.asarray(v_descale, dtype=np.float32))
     off = np.ascontiguousarray(np.asarray(kv_off, dtype=np.int64))
     tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
     n = int(tok.shape[0])
     out = np.zeros((max(n, 1), num_q_heads, head_dim), dtype=np.float64)
     lse = np.zeros((max(n, 1), num_q_heads), dtype=np.float64)
-    rc = lib.oracle_attention_f64kv(int(rows.shape[0]), _ptr(rows), _ptr(key_lo), _ptr(key_hi), _ptr(qa),
-                                    _ptr(ka), _ptr(va), _ptr(off), num_q_heads, num_kv_heads, head_dim,
-                                    float(scale), _ptr(tok), n, _ptr(out), _ptr(lse))
+    rc = lib.oracle_attention_fp8kv(int(rows.shape[0]), _ptr(rows), _ptr(key_lo), _ptr(key_hi), _ptr(qa),
+                                    _ptr(ka), _ptr(va), _ptr(off), _ptr(kd), _ptr(vd), num_q_heads, num_kv_heads,
+                                    head_dim, float(scale), _ptr(tok), n, _ptr(out), _ptr(lse))
     if rc != 0:
-        raise OracleError(rc, "oracle_attention_f64kv")
+        raise OracleError(rc, "oracle_attention_fp8kv")
     return out[:n], lse[:n]
 
 

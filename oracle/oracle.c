@@ -294,25 +294,37 @@ double oracle_e4m3_decode(uint8_t c) {
 }
 
 /* Round a float to the nearest e4m3 value, ties to even, magnitudes above 448
- * saturating to 448 (NaN stays NaN). Found by exhaustive search over the 127
- * non-negative finite codes: plain and obviously correct, not fast. */
-uint8_t oracle_e4m3_encode(float x) {
+ * saturating to 448 (NaN stays NaN). The non-negative finite values, codes 0
+ * to 126, increase with the code (val[c] = value of code c), so the nearest
+ * one is found by bisection: lo = the last code whose value is <= |x|, then
+ * |x| is compared with the values of lo and lo + 1; an exact tie takes the even
+ * code (mantissa lsb 0). */
+static uint8_t encode_with(float x, const double* val) {
     if (x != x) return 0x7F;
     const uint8_t sign = (x < 0.0f || (x == 0.0f && signbit(x))) ? 0x80 : 0x00;
     const double a = fabs((double)x);
     if (a >= 448.0) return sign | 0x7E;
-    uint8_t best = 0;
-    double best_err = a;  /* code 0 is +0 */
-    for (int c = 1; c <= 0x7E; ++c) {
-        const double v = oracle_e4m3_decode((uint8_t)c);
-        const double err = fabs(v - a);
-        /* strictly closer wins; on a tie the even code (mantissa lsb 0) wins */
-        if (err < best_err || (err == best_err && (c & 1) == 0)) {
-            best = (uint8_t)c;
-            best_err = err;
-        }
+    int lo = 0, hi = 0x7E;  /* val[lo] <= a < val[hi] */
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) / 2;
+        if (val[mid] <= a) lo = mid; else hi = mid;
     }
-    return sign | best;
+    const double dlo = a - val[lo], dhi = val[hi] - a;
+    int c;
+    if (dlo < dhi) c = lo;
+    else if (dhi < dlo) c = hi;
+    else c = (lo & 1) == 0 ? lo : hi;
+    return sign | (uint8_t)c;
+}
+
+static void value_table(double* val) {
+    for (int c = 0; c <= 0x7E; ++c) val[c] = oracle_e4m3_decode((uint8_t)c);
+}
+
+uint8_t oracle_e4m3_encode(float x) {
+    double val[0x7F];
+    value_table(val);
+    return encode_with(x, val);
 }
 
 /*
@@ -324,6 +336,9 @@ uint8_t oracle_e4m3_encode(float x) {
 int oracle_cache_write_fp8(const uint16_t* src, const int64_t* slot, int64_t num_tokens, uint8_t* cache,
                            int64_t num_slots, int row_elems, float scale) {
     int rc = ORC_OK;
+    double val[0x7F];
+    value_table(val);
+#pragma omp parallel for schedule(static) reduction(min : rc)
     for (int64_t t = 0; t < num_tokens; ++t) {
         int64_t s = slot[t];
         if (s < 0) continue;
@@ -331,7 +346,7 @@ int oracle_cache_write_fp8(const uint16_t* src, const int64_t* slot, int64_t num
         for (int e = 0; e < row_elems; ++e) {
             const float x = (float)bf16_to_double(src[(size_t)t * row_elems + e]);
             const float q = x / scale;
-            cache[(size_t)s * row_elems + e] = oracle_e4m3_encode(q);
+            cache[(size_t)s * row_elems + e] = encode_with(q, val);
         }
     }
     return rc;
@@ -342,10 +357,11 @@ void oracle_e4m3_decode_array(const uint8_t* codes, int64_t n, double* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(codes[i]);
 }
 
-/* attend_token for keys and values given as doubles [L][Hkv][D]. */
-static void attend_token_f64(const uint16_t* q_tok, const double* k, const double* v, int64_t pos,
-                             int64_t k_lo, int64_t k_hi, int Hq, int Hkv, int D, double scale,
-                             double* out, double* lse, double* s_buf) {
+/* attend_token for an FP8 cache: key k of the request, kv head g, dim d is
+ * value(code_k[k][g][d]) * k_descale[g] (same for V); dec[c] is value(c). */
+static void attend_token_fp8(const uint16_t* q_tok, const uint8_t* k, const uint8_t* v, const float* kd,
+                             const float* vd, const double* dec, int64_t pos, int64_t k_lo, int64_t k_hi,
+                             int Hq, int Hkv, int D, double scale, double* out, double* lse, double* s_buf) {
     int G = Hq / Hkv;
     int64_t hi = k_hi < pos + 1 ? k_hi : pos + 1;
     int64_t lo = k_lo > 0 ? k_lo : 0;
@@ -356,10 +372,10 @@ static void attend_token_f64(const uint16_t* q_tok, const double* k, const doubl
         if (hi <= lo) { lse[h] = -INFINITY; continue; }
         double m = -INFINITY;
         for (int64_t kk = lo; kk < hi; ++kk) {
-            const double* kr = k + ((size_t)kk * Hkv + hk) * D;
+            const uint8_t* kr = k + ((size_t)kk * Hkv + hk) * D;
             const uint16_t* qr = q_tok + (size_t)h * D;
             double s = 0.0;
-            for (int d = 0; d < D; ++d) s += bf16_to_double(qr[d]) * kr[d];
+            for (int d = 0; d < D; ++d) s += bf16_to_double(qr[d]) * (dec[kr[d]] * (double)kd[hk]);
             s *= scale;
             s_buf[kk - lo] = s;
             if (s > m) m = s;
@@ -370,19 +386,22 @@ static void attend_token_f64(const uint16_t* q_tok, const double* k, const doubl
         lse[h] = l;
         for (int64_t kk = lo; kk < hi; ++kk) {
             double w = exp(s_buf[kk - lo] - l);
-            const double* vr = v + ((size_t)kk * Hkv + hk) * D;
-            for (int d = 0; d < D; ++d) o[d] += w * vr[d];
+            const uint8_t* vr = v + ((size_t)kk * Hkv + hk) * D;
+            for (int d = 0; d < D; ++d) o[d] += w * (dec[vr[d]] * (double)vd[hk]);
         }
     }
 }
 
-/* oracle_attention with every request's keys and values given as doubles
- * (for the FP8 cache: the dequantized codes). Same arguments otherwise. */
-int oracle_attention_f64kv(int num_rows, const int32_t* rows, const int64_t* key_lo, const int64_t* key_hi,
-                           const uint16_t* q, const double* kv_k, const double* kv_v, const int64_t* kv_off,
-                           int Hq, int Hkv, int D, double scale, const int64_t* tokens, int64_t n_tok,
-                           double* out, double* lse) {
+/* oracle_attention over an FP8 cache: every request's key and value codes
+ * back to back ([L][Hkv][D] bytes, request r from token kv_off[r]) and the
+ * descales k_descale, v_descale [num_reqs][Hkv]. Same arguments otherwise. */
+int oracle_attention_fp8kv(int num_rows, const int32_t* rows, const int64_t* key_lo, const int64_t* key_hi,
+                           const uint16_t* q, const uint8_t* kv_k, const uint8_t* kv_v, const int64_t* kv_off,
+                           const float* k_descale, const float* v_descale, int Hq, int Hkv, int D,
+                           double scale, const int64_t* tokens, int64_t n_tok, double* out, double* lse) {
     if (Hkv <= 0 || Hq % Hkv != 0 || D <= 0) return ORC_ERR_ARG;
+    double dec[256];
+    for (int c = 0; c < 256; ++c) dec[c] = oracle_e4m3_decode((uint8_t)c);
     int64_t max_len = 1;
     for (int i = 0; i < num_rows; ++i) {
         int64_t e = rows[(size_t)i * F_NFIELDS + F_KVEND];
@@ -408,10 +427,12 @@ int oracle_attention_f64kv(int num_rows, const int32_t* rows, const int64_t* key
             const int32_t* row = rows + (size_t)found * F_NFIELDS;
             int64_t j = t - row[F_QSTART];
             int64_t pos = (int64_t)row[F_KVEND] - row[F_QLEN] + j;
-            int64_t base = kv_off[row[F_REQ]];
-            attend_token_f64(q + (size_t)t * Hq * D, kv_k + (size_t)base * Hkv * D, kv_v + (size_t)base * Hkv * D,
-                             pos, key_lo[found], key_hi[found], Hq, Hkv, D, scale,
-                             out + (size_t)i * Hq * D, lse + (size_t)i * Hq, s_buf);
+            int32_t req = row[F_REQ];
+            int64_t base = kv_off[req];
+            attend_token_fp8(q + (size_t)t * Hq * D, kv_k + (size_t)base * Hkv * D, kv_v + (size_t)base * Hkv * D,
+                             k_descale + (size_t)req * Hkv, v_descale + (size_t)req * Hkv, dec, pos,
+                             key_lo[found], key_hi[found], Hq, Hkv, D, scale, out + (size_t)i * Hq * D,
+                             lse + (size_t)i * Hq, s_buf);
         }
         free(s_buf);
     }

@@ -8,9 +8,9 @@ than itself (CPU only).
   finite range, hand-worked ties (to even), the subnormal boundary, signed
   zero, and saturation at +-448 outside it (the saturating reading);
 * the FP8 cache write read back through the block table;
-* attention over float keys/values against a dense numpy softmax, and over
-  dequantised codes with per-(request, kv-head) descales against the same
-  dense softmax on the dequantised arrays.
+* attention over codes with per-(request, kv-head) descales against a dense
+  numpy softmax over the codes' values (decoded by PyTorch) times the
+  descales, and the descales' algebra.
 """
 import math
 
@@ -124,73 +124,79 @@ def _dense(Q, K, V, lo, hi, pos, scale, G):
     return out, lse
 
 
+def _torch_decode(codes: np.ndarray) -> np.ndarray:
+    """e4m3 values through PyTorch's float8_e4m3fn (independent of the oracle)."""
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _random_codes(rng, shape):
+    c = rng.integers(0, 0x7F, size=shape, dtype=np.uint8)          # 0 .. 126: finite magnitudes
+    return c | (rng.integers(0, 2, size=shape, dtype=np.uint8) << 7)
+
+
 @pytest.mark.parametrize("G", [1, 2, 4])
-def test_attention_f64kv_matches_dense(G):
+def test_attention_fp8kv_matches_dense(G):
+    """Two requests (one with a cached prefix), random codes and a different
+    descale per (request, kv head): every token of every part (fused, context,
+    new) against a dense softmax over the codes' values (decoded by PyTorch)
+    times the descales."""
     rng = np.random.default_rng(40 + G)
     Hkv, D = 2, 8
     Hq = G * Hkv
-    P, N = 9, 7
-    L = P + N
-    K = rng.standard_normal((L, Hkv, D)) * 1.7
-    V = rng.standard_normal((L, Hkv, D))
-    q = torch.from_numpy(rng.standard_normal((N, Hq, D)).astype(np.float32)).to(torch.bfloat16)
-    plan = oracle.row_plan([N], [P], np.arange(L, dtype=np.int32)[None, :], 1, 2, 0)
-    rows = plan["rows"]
-    tokens = np.arange(N)
+    lens = [(9, 7), (0, 11)]
+    ql = [n for _, n in lens]
+    nc = [p for p, _ in lens]
+    ck = [_random_codes(rng, (p + n, Hkv, D)) for p, n in lens]
+    cv = [_random_codes(rng, (p + n, Hkv, D)) for p, n in lens]
+    kd = rng.uniform(0.001, 0.02, size=(2, Hkv)).astype(np.float32)
+    vd = rng.uniform(0.001, 0.02, size=(2, Hkv)).astype(np.float32)
+    Lmax = max(p + n for p, n in lens)
+    bt = np.stack([np.arange(Lmax, dtype=np.int32) + r * Lmax for r in range(2)])
+    rows = oracle.row_plan(ql, nc, bt, 1, 2, 0)["rows"]
+    q = torch.from_numpy(rng.standard_normal((sum(ql), Hq, D)).astype(np.float32)).to(torch.bfloat16)
+    off = [0, lens[0][0] + lens[0][1]]
+    K = [_torch_decode(c) * kd[r][None, :, None].astype(np.float64) for r, c in enumerate(ck)]
+    V = [_torch_decode(c) * vd[r][None, :, None].astype(np.float64) for r, c in enumerate(cv)]
+    tokens = np.arange(sum(ql))
     for part in ("fused", "context", "new"):
         lo, hi = oracle.key_ranges(rows, part)
-        out, lse = oracle.attention_f64kv(rows, q, K, V, [0], Hq, Hkv, D, 0.3, tokens, key_lo=lo, key_hi=hi)
+        out, lse = oracle.attention_fp8kv(rows, q, np.concatenate(ck), np.concatenate(cv), off, kd, vd, Hq, Hkv, D,
+                                          0.3, tokens, key_lo=lo, key_hi=hi)
         for ri, r in enumerate(rows):
             j = np.arange(r[3])
             t = r[2] + j
             pos = r[5] - r[3] + j
-            ro, rl = _dense(q.to(torch.float64).numpy()[t], K, V, lo[ri], hi[ri], pos, 0.3, G)
-            np.testing.assert_allclose(out[t], ro, rtol=0, atol=1e-12)
+            ro, rl = _dense(q.to(torch.float64).numpy()[t], K[r[0]], V[r[0]], lo[ri], hi[ri], pos, 0.3, G)
+            np.testing.assert_allclose(out[t], ro, rtol=0, atol=1e-13)
             np.testing.assert_allclose(lse[t], rl, rtol=0, atol=1e-12)
 
 
-def test_attention_over_dequantised_codes_with_descales():
-    """Codes x per-(request, kv-head) descale, fed as float arrays, give the
-    dense softmax over the same dequantised keys and values; a descale of 2 on
-    V doubles the output and leaves the LSE alone, a descale on K scales the
-    scores."""
+def test_descale_algebra():
+    """A V descale of 2x doubles the output and leaves the LSE alone; a K
+    descale of 2x equals a softmax scale of 2x (factors of two: exact in fp32)."""
     rng = np.random.default_rng(77)
     Hkv, G, D = 2, 2, 16
     Hq = G * Hkv
-    lens = [(5, 6), (0, 9)]                          # (cached, new) per request
-    codes_k = [rng.integers(0, 0x7E, size=(p + n, Hkv, D), dtype=np.uint8) for p, n in lens]
-    codes_v = [rng.integers(0, 0x7E, size=(p + n, Hkv, D), dtype=np.uint8) for p, n in lens]
-    for c in codes_k + codes_v:                      # random signs
-        c |= (rng.integers(0, 2, size=c.shape, dtype=np.uint8) << 7)
-    kd = rng.uniform(0.001, 0.02, size=(len(lens), Hkv)).astype(np.float32)
-    vd = rng.uniform(0.001, 0.02, size=(len(lens), Hkv)).astype(np.float32)
-    K = [oracle.e4m3_decode(c) * kd[r][None, :, None].astype(np.float64) for r, c in enumerate(codes_k)]
-    V = [oracle.e4m3_decode(c) * vd[r][None, :, None].astype(np.float64) for r, c in enumerate(codes_v)]
-    ql = [n for _, n in lens]
-    nc = [p for p, _ in lens]
-    Lmax = max(p + n for p, n in lens)
-    bt = np.stack([np.arange(Lmax, dtype=np.int32) + r * Lmax for r in range(len(lens))])
-    plan = oracle.row_plan(ql, nc, bt, 1, 2, 1)
-    q = torch.from_numpy(rng.standard_normal((sum(ql), Hq, D)).astype(np.float32)).to(torch.bfloat16)
-    off = np.cumsum([0] + [k.shape[0] for k in K[:-1]])
-    tokens = np.arange(sum(ql))
-    out, lse = oracle.attention_f64kv(plan["rows"], q, np.concatenate(K), np.concatenate(V), off, Hq, Hkv, D,
-                                      0.25, tokens)
-    qo = 0
-    for r, (p, n) in enumerate(lens):
-        t = np.arange(qo, qo + n)
-        ro, rl = _dense(q.to(torch.float64).numpy()[t], K[r], V[r], 0, p + n, p + np.arange(n), 0.25, G)
-        np.testing.assert_allclose(out[t], ro, rtol=0, atol=1e-13)
-        np.testing.assert_allclose(lse[t], rl, rtol=0, atol=1e-12)
-        qo += n
-    out2, lse2 = oracle.attention_f64kv(plan["rows"], q, np.concatenate(K), 2 * np.concatenate(V), off, Hq, Hkv,
-                                        D, 0.25, tokens)
-    np.testing.assert_allclose(out2, 2 * out, rtol=0, atol=1e-13)
-    np.testing.assert_allclose(lse2, lse, rtol=0, atol=0)
-    # K descale 3x == softmax scale 3x
-    out3, lse3 = oracle.attention_f64kv(plan["rows"], q, 3 * np.concatenate(K), np.concatenate(V), off, Hq, Hkv,
-                                        D, 0.25, tokens)
-    out4, lse4 = oracle.attention_f64kv(plan["rows"], q, np.concatenate(K), np.concatenate(V), off, Hq, Hkv,
-                                        D, 0.75, tokens)
-    np.testing.assert_allclose(out3, out4, rtol=0, atol=1e-12)
-    np.testing.assert_allclose(lse3, lse4, rtol=0, atol=1e-12)
+    n = 13
+    ck = _random_codes(rng, (n, Hkv, D))
+    cv = _random_codes(rng, (n, Hkv, D))
+    kd = rng.uniform(0.001, 0.02, size=(1, Hkv)).astype(np.float32)
+    vd = rng.uniform(0.001, 0.02, size=(1, Hkv)).astype(np.float32)
+    rows = oracle.row_plan([n], [0], np.arange(n, dtype=np.int32)[None, :], 1, 1, 0)["rows"]
+    q = torch.from_numpy(rng.standard_normal((n, Hq, D)).astype(np.float32)).to(torch.bfloat16)
+    tok = np.arange(n)
+    o1, l1 = oracle.attention_fp8kv(rows, q, ck, cv, [0], kd, vd, Hq, Hkv, D, 0.25, tok)
+    o2, l2 = oracle.attention_fp8kv(rows, q, ck, cv, [0], kd, 2 * vd, Hq, Hkv, D, 0.25, tok)
+    np.testing.assert_allclose(o2, 2 * o1, rtol=0, atol=1e-15)
+    np.testing.assert_array_equal(l2, l1)
+    o3, l3 = oracle.attention_fp8kv(rows, q, ck, cv, [0], 2 * kd, vd, Hq, Hkv, D, 0.25, tok)
+    o4, l4 = oracle.attention_fp8kv(rows, q, ck, cv, [0], kd, vd, Hq, Hkv, D, 0.5, tok)
+    np.testing.assert_allclose(o3, o4, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l3, l4, rtol=0, atol=1e-12)
+
+
+def test_finite_codes_increase_with_the_code():
+    """The premise of the encoder's bisection: codes 0..126 are the
+    non-negative finite values in increasing order (PyTorch's table)."""
+    v = _torch_decode(np.arange(127, dtype=np.uint8))
+    assert np.all(np.diff(v) > 0)
