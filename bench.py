@@ -8,8 +8,11 @@ shard rows each plus 56 decode rows with U[1024,16384] keys, 32 q / 8 kv heads,
 D=128): the one workload on which both halves of the metric (prefill TFLOP/s
 and decode-row HBM GB/s) are defined.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5] [--kv-cache bf16|fp8]
     python bench.py --impl reference     # the CPU oracle on a bounded sample
+
+``--kv-cache fp8`` runs the same step over an FP8 (e4m3) paged cache (cache
+write with the layer scales, attention with per-(request, kv head) descales).
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (no data-path collective); rank 0 prints the line, value = all ranks' work /
@@ -104,10 +107,10 @@ def measured_traffic(workload_name: str):
     return None
 
 
-def plan_work(rows: np.ndarray, hq: int, hkv: int, d: int):
+def plan_work(rows: np.ndarray, hq: int, hkv: int, d: int, kv_bytes: int = 2):
     """Algorithmic work of a plan: prefill FLOPs (4 D Hq per unmasked query-key
     pair), decode FLOPs and decode bytes (K and V of every visible key once per
-    kv head, plus q, out and lse)."""
+    kv head at kv_bytes per element, plus q, out and lse)."""
     r = rows.astype(np.int64)
     ql, end = r[:, 3], r[:, 5]
     dec = r[:, 7] == 1
@@ -116,7 +119,7 @@ def plan_work(rows: np.ndarray, hq: int, hkv: int, d: int):
     dec_keys = int(end[dec].sum())
     n_dec = int(dec.sum())
     return dict(prefill_flop=4.0 * d * hq * pre_pairs, decode_flop=4.0 * d * hq * dec_keys,
-                decode_bytes=float(dec_keys * hkv * d * 2 * 2 + n_dec * (hq * d * 2 * 2 + hq * 4)),
+                decode_bytes=float(dec_keys * hkv * d * 2 * kv_bytes + n_dec * (hq * d * 2 * 2 + hq * 4)),
                 pairs=pre_pairs + dec_keys)
 
 
@@ -167,25 +170,29 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU arm
 
-def setup(workload: int, device: str, flags: int):
+def setup(workload: int, device: str, flags: int, kv_fp8: bool = False):
     import context_prefill_attention_gb300 as P
     P.load()
     spec = W.workload_spec(workload)
     bt, nb = W.block_tables(spec)
     shape = (nb, spec.block_size, spec.num_kv_heads, spec.head_dim)
-    kc = torch.zeros(shape, dtype=torch.bfloat16, device=device)
-    vc = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+    cache_dtype = torch.uint8 if kv_fp8 else torch.bfloat16
+    kc = torch.zeros(shape, dtype=cache_dtype, device=device)
+    vc = torch.zeros(shape, dtype=cache_dtype, device=device)
+    fp8_scales = (W.FP8_K_SCALE, W.FP8_V_SCALE) if kv_fp8 else None
     prefix = [r for r in range(spec.num_reqs) if spec.num_computed[r] > 0]
     for r in prefix:  # contexts an earlier step would have left in the cache
         P.write_positions(kc, vc, bt[r:r + 1].numpy(), [0], [W.request_tensor(spec, r, W.KIND_KP, device)],
-                          [W.request_tensor(spec, r, W.KIND_VP, device)], spec.block_size)
+                          [W.request_tensor(spec, r, W.KIND_VP, device)], spec.block_size,
+                          fp8_scales=fp8_scales)
     q = W.packed_new_tokens(spec, W.KIND_Q, device)
     k = W.packed_new_tokens(spec, W.KIND_K, device)
     v = W.packed_new_tokens(spec, W.KIND_V, device)
     step = P.PcpStep(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
                      block_size=spec.block_size, num_shards=spec.num_shards, split_mode=spec.split_mode,
                      max_tokens=spec.total_q, max_reqs=spec.num_reqs, max_kv_len=bt.shape[1] * spec.block_size,
-                     flags=flags, device=device)
+                     flags=flags, device=device, kv_cache_dtype="fp8" if kv_fp8 else "bf16",
+                     k_scale=W.FP8_K_SCALE, v_scale=W.FP8_V_SCALE)
     return P, spec, bt, bt.to(device), kc, vc, q, k, v, step
 
 
@@ -196,7 +203,9 @@ def run_gpu(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     device = f"cuda:{local}"
-    P, spec, bt, bt_dev, kc, vc, q, k, v, step = setup(args.workload, device, args.flags)
+    kv_fp8 = args.kv_cache == "fp8"
+    P, spec, bt, bt_dev, kc, vc, q, k, v, step = setup(args.workload, device, args.flags, kv_fp8)
+    workload_name = spec.name + ("-fp8kv" if kv_fp8 else "")
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
 
@@ -205,7 +214,7 @@ def run_gpu(args):
         return step.run(q, k, v, kc, vc, bt_dev, spec.scale, stream)
 
     plan = step.build_plan(spec.query_len, spec.num_computed, bt)
-    work = plan_work(plan["rows"], spec.num_q_heads, spec.num_kv_heads, spec.head_dim)
+    work = plan_work(plan["rows"], spec.num_q_heads, spec.num_kv_heads, spec.head_dim, 1 if kv_fp8 else 2)
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize()
@@ -269,10 +278,11 @@ def run_gpu(args):
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded torch.randn, bf16)",
-        "config": {"workload": spec.name, "rows": int(plan["rows"].shape[0]), "total_q": spec.total_q,
+        "config": {"workload": workload_name, "rows": int(plan["rows"].shape[0]), "total_q": spec.total_q,
                    "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
                    "head_dim": spec.head_dim, "block_size": spec.block_size, "num_shards": spec.num_shards,
-                   "flags": args.flags, "l2": "flushed (512 MiB write) between timed steps",
+                   "flags": args.flags, "kv_cache": "fp8-e4m3" if kv_fp8 else "bf16",
+                   "l2": "flushed (512 MiB write) between timed steps",
                    "parallelism": f"replicas x{ws}"},
         "prefill": {"tflops": round(achieved, 2), "ms": round(pre_avg, 4),
                     "frac_bf16_peak": round(achieved / peaks["bf16"], 4), "flop": work["prefill_flop"]},
@@ -281,7 +291,7 @@ def run_gpu(args):
                    "bytes": work["decode_bytes"]},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16"],
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
-                     "traffic": measured_traffic(spec.name),
+                     "traffic": measured_traffic(workload_name),
                      "kernel": "prefill_kernel", "peak_source": f"{peaks['source']} bf16 burst"},
         "e2e": {"value": round(ws * step_flop / (e2e * 1e-3) / 1e12, 3), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e, 4)},
@@ -289,7 +299,7 @@ def run_gpu(args):
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(spec, bt, target_s=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(spec, bt, target_s=args.cpu_seconds, kv_fp8=kv_fp8)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -299,9 +309,11 @@ def run_gpu(args):
 
 # ---------------------------------------------------------------- CPU oracle
 
-def _oracle_sample(spec, bt, target_s: float, seed: int):
+def _oracle_sample(spec, bt, target_s: float, seed: int, kv_fp8: bool = False):
     """Run the oracle on a seeded sample of the workload's query tokens, sized to
-    take about target_s seconds; returns (seconds, flop of the sample, description)."""
+    take about target_s seconds; returns (seconds, flop of the sample, description).
+    With kv_fp8 the oracle attends over its own e4m3 codes of the keys and values
+    (encoded before the timed calls) with the layer-scale descales."""
     import oracle
     rows = oracle.row_plan(spec.query_len, spec.num_computed, bt.numpy(), spec.block_size, spec.num_shards,
                            spec.split_mode)["rows"]
@@ -309,6 +321,21 @@ def _oracle_sample(spec, bt, target_s: float, seed: int):
     kfull, vfull = zip(*[W.full_kv(spec, r) for r in range(spec.num_reqs)])
     kv_off = np.cumsum([0] + [k.shape[0] for k in kfull[:-1]])
     kk, vv = torch.cat(kfull, 0), torch.cat(vfull, 0)
+    if kv_fp8:
+        ck = np.zeros(tuple(kk.shape), dtype=np.uint8)
+        cv = np.zeros(tuple(vv.shape), dtype=np.uint8)
+        slot = np.arange(kk.shape[0], dtype=np.int64)
+        oracle.cache_write_fp8(kk, slot, ck, W.FP8_K_SCALE)
+        oracle.cache_write_fp8(vv, slot, cv, W.FP8_V_SCALE)
+        kd, vd = (x.numpy() for x in W.fp8_descales(spec, "layer"))
+
+        def attend(tokens):
+            return oracle.attention_fp8kv(rows, q, ck, cv, kv_off, kd, vd, spec.num_q_heads, spec.num_kv_heads,
+                                          spec.head_dim, spec.scale, tokens)
+    else:
+        def attend(tokens):
+            return oracle.attention(rows, q, kk, vv, kv_off, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                                    spec.scale, tokens)
     rng = np.random.default_rng(seed)
     tok_rows = [(int(r[2]), int(r[3]), int(r[5])) for r in rows]   # (q_start, q_len, kv_end)
     all_tok = np.concatenate([np.arange(s, s + n) for s, n, _ in tok_rows])
@@ -318,8 +345,7 @@ def _oracle_sample(spec, bt, target_s: float, seed: int):
     while True:
         sel = order[:n]
         t0 = time.time()
-        oracle.attention(rows, q, kk, vv, kv_off, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.scale,
-                         all_tok[sel])
+        attend(all_tok[sel])
         dt = time.time() - t0
         flop = 4.0 * spec.head_dim * spec.num_q_heads * float(keys_of[sel].sum())
         if dt >= target_s * 0.5 or n >= all_tok.shape[0]:
@@ -327,10 +353,10 @@ def _oracle_sample(spec, bt, target_s: float, seed: int):
         n = min(all_tok.shape[0], int(n * max(2.0, min(16.0, target_s / max(dt, 1e-3)))))
 
 
-def cpu_baseline(spec, bt, target_s: float = 15.0):
+def cpu_baseline(spec, bt, target_s: float = 15.0, kv_fp8: bool = False):
     import oracle
     oracle.build()
-    dt, flop, desc = _oracle_sample(spec, bt, target_s, spec.seed + 99)
+    dt, flop, desc = _oracle_sample(spec, bt, target_s, spec.seed + 99, kv_fp8)
     threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
     return {"value": round(flop / dt / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": desc + f", fp64, {dt:.1f} s"}
@@ -373,6 +399,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", type=int, default=4)
     ap.add_argument("--flags", type=int, default=0)
+    ap.add_argument("--kv-cache", default="bf16", choices=["bf16", "fp8"])
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -8,7 +8,7 @@ from ._lib import (EXPORTS, PCP_ATTN_KV_SHARDS, PCP_ATTN_SEPARATE_CONTEXT, PCP_A
                    PCP_ERR_ALIGN,
                    PCP_ERR_ARG, PCP_ERR_CUDA, PCP_ERR_RANGE, PCP_ERR_TIMEOUT, PCP_ERR_UNSUPPORTED,
                    PCP_ERR_WORKSPACE, PCP_OK, PCP_SPLIT_CONTIGUOUS, PCP_SPLIT_DUAL_CHUNK, ROW_FIELDS,
-                   PcpError, load, pcp_attn_varlen, pcp_attn_varlen_noalloc, pcp_attn_workspace_size,
-                   pcp_build_row_plan,
-                   pcp_kv_cache_write, pcp_lse_merge, pcp_mask_slots_for_shard, pcp_set_profile_events)
+                   PcpError, load, pcp_attn_varlen, pcp_attn_varlen_fp8kv, pcp_attn_varlen_noalloc,
+                   pcp_attn_workspace_size, pcp_build_row_plan, pcp_kv_cache_write, pcp_kv_cache_write_fp8,
+                   pcp_lse_merge, pcp_mask_slots_for_shard, pcp_set_profile_events)
 from .step import PcpStep, write_positions  # noqa: F401

@@ -38,7 +38,8 @@ ROW_FIELDS = ("req", "shard", "q_start", "q_len", "ctx_len", "kv_end", "causal_o
 
 # every symbol include/pcp.h declares
 EXPORTS = ("pcp_build_row_plan", "pcp_mask_slots_for_shard", "pcp_kv_cache_write",
-           "pcp_attn_workspace_size", "pcp_attn_varlen", "pcp_attn_varlen_noalloc", "pcp_lse_merge",
+           "pcp_kv_cache_write_fp8", "pcp_attn_workspace_size", "pcp_attn_varlen", "pcp_attn_varlen_noalloc",
+           "pcp_attn_varlen_fp8kv", "pcp_lse_merge",
            "pcp_set_profile_events", "pcp_selftest_bounded_wait",
            "pcp_last_cuda_error", "pcp_status_string")
 
@@ -74,6 +75,11 @@ def load(path: Optional[str] = None):
     lib.pcp_mask_slots_for_shard.restype = ctypes.c_int
     lib.pcp_kv_cache_write.argtypes = [P, P, P, i32, P, P, i64, i32, i32, i32, P, P]
     lib.pcp_kv_cache_write.restype = ctypes.c_int
+    lib.pcp_kv_cache_write_fp8.argtypes = [P, P, P, i32, P, P, i64, i32, i32, i32, f32, f32, P, P]
+    lib.pcp_kv_cache_write_fp8.restype = ctypes.c_int
+    lib.pcp_attn_varlen_fp8kv.argtypes = [P, P, P, P, P, P, i32, i32, i64, i32, P, i32, i32, i32, i32, i32, f32,
+                                          P, P, P, sz, i32, P, P]
+    lib.pcp_attn_varlen_fp8kv.restype = ctypes.c_int
     lib.pcp_attn_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.pcp_attn_workspace_size.restype = sz
     lib.pcp_attn_varlen.argtypes = [P, P, P, P, i32, i32, i64, i32, P, i32, i32, i32, i32, i32, f32, P, P, P,
@@ -165,6 +171,20 @@ def pcp_kv_cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Ten
     _check(rc, "pcp_kv_cache_write")
 
 
+def pcp_kv_cache_write_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                           key_cache: torch.Tensor, value_cache: torch.Tensor, k_scale: float, v_scale: float,
+                           status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Scatter new bf16 K/V ``[T, Hkv, D]`` into FP8 (e4m3) caches ``[num_blocks, bs,
+    Hkv, D]`` (uint8) as e4m3(x / k_scale) and e4m3(x / v_scale)."""
+    lib = load()
+    T = int(k.shape[0])
+    nb, bs, hkv, d = (int(x) for x in key_cache.shape)
+    rc = lib.pcp_kv_cache_write_fp8(_t_ptr(k), _t_ptr(v), _t_ptr(slot_mapping), T, _t_ptr(key_cache),
+                                    _t_ptr(value_cache), nb, bs, hkv, d, float(k_scale), float(v_scale),
+                                    _t_ptr(status), _stream(stream))
+    _check(rc, "pcp_kv_cache_write_fp8")
+
+
 def pcp_attn_workspace_size(num_rows: int, total_q: int, num_q_heads: int, head_dim: int,
                             max_kv_len: int, flags: int = 0) -> int:
     return int(load().pcp_attn_workspace_size(num_rows, total_q, num_q_heads, head_dim, max_kv_len, flags))
@@ -196,6 +216,34 @@ def pcp_attn_varlen(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch
                              _t_ptr(workspace), int(workspace.numel() * workspace.element_size()), flags,
                              _t_ptr(status), _stream(stream))
     _check(rc, "pcp_attn_varlen")
+    return out, lse
+
+
+def pcp_attn_varlen_fp8kv(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                          k_descale: torch.Tensor, v_descale: torch.Tensor, block_table: torch.Tensor,
+                          rows: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
+                          lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                          flags: int = 0, status: Optional[torch.Tensor] = None, stream=None):
+    """:func:`pcp_attn_varlen` over FP8 (e4m3, uint8) caches with fp32 descales
+    ``[num_reqs, Hkv]`` on the device."""
+    lib = load()
+    T, hq, d = (int(x) for x in q.shape)
+    nb, bs, hkv, _ = (int(x) for x in key_cache.shape)
+    n_rows = int(rows.shape[0])
+    mb = int(block_table.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
+    need = pcp_attn_workspace_size(n_rows, T, hq, d, mb * bs, flags)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = lib.pcp_attn_varlen_fp8kv(_t_ptr(q), _t_ptr(key_cache), _t_ptr(value_cache), _t_ptr(k_descale),
+                                   _t_ptr(v_descale), _t_ptr(block_table), int(block_table.shape[0]), mb, nb, bs,
+                                   _t_ptr(rows), n_rows, T, hq, hkv, d, float(scale), _t_ptr(out), _t_ptr(lse),
+                                   _t_ptr(workspace), int(workspace.numel() * workspace.element_size()), flags,
+                                   _t_ptr(status), _stream(stream))
+    _check(rc, "pcp_attn_varlen_fp8kv")
     return out, lse
 
 

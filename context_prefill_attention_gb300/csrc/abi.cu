@@ -1,6 +1,7 @@
 // The C ABI of libpcp (declared in include/pcp.h): argument validation on the
 // host, workspace layout and the launch sequence of one attention call.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include <mutex>
@@ -101,6 +102,26 @@ extern "C" int pcp_kv_cache_write(const void* k, const void* v, const int64_t* s
                               num_blocks * block_size, status, reinterpret_cast<cudaStream_t>(stream));
 }
 
+extern "C" int pcp_kv_cache_write_fp8(const void* k, const void* v, const int64_t* slot_mapping,
+                                      int32_t num_tokens, void* key_cache, void* value_cache,
+                                      int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                      int32_t head_dim, float k_scale, float v_scale, int32_t* status,
+                                      pcp_stream_t stream) {
+    if (num_tokens < 0 || num_blocks < 0 || block_size < 1 || num_kv_heads < 1 || head_dim < 1)
+        return PCP_ERR_ARG;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite(k_scale) || !isfinite(v_scale)) return PCP_ERR_ARG;
+    if (num_tokens == 0) return PCP_OK;
+    if (!k || !v || !slot_mapping || !key_cache || !value_cache) return PCP_ERR_ARG;
+    if (((int64_t)head_dim * num_kv_heads) % 16 != 0) return PCP_ERR_UNSUPPORTED;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(key_cache) || !aligned16(value_cache) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PCP_ERR_ALIGN;
+    const int32_t vec_per_tok = (int32_t)((int64_t)head_dim * num_kv_heads / 16);
+    return launch_cache_write_fp8(k, v, slot_mapping, num_tokens, vec_per_tok, key_cache, value_cache,
+                                  num_blocks * block_size, k_scale, v_scale, status,
+                                  reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" size_t pcp_attn_workspace_size(int32_t num_rows, int32_t total_q, int32_t num_q_heads,
                                           int32_t head_dim, int32_t max_kv_len, int32_t flags) {
     if (num_rows < 0 || total_q < 0 || num_q_heads < 1 || head_dim < 1 || max_kv_len < 0) return 0;
@@ -108,13 +129,15 @@ extern "C" size_t pcp_attn_workspace_size(int32_t num_rows, int32_t total_q, int
     return workspace_layout(num_rows, total_q, num_q_heads, head_dim, max_kv_len, flags).total;
 }
 
-extern "C" int pcp_attn_varlen(const void* q, const void* key_cache, const void* value_cache,
-                               const int32_t* block_table, int32_t num_reqs,
-                               int32_t max_blocks_per_req, int64_t num_blocks, int32_t block_size, const pcp_row_t* rows,
-                               int32_t num_rows, int32_t total_q, int32_t num_q_heads,
-                               int32_t num_kv_heads, int32_t head_dim, float scale, void* out,
-                               float* lse, void* workspace, size_t workspace_bytes, int32_t flags,
-                               int32_t* status, pcp_stream_t stream) {
+namespace {
+// One attention call over a bf16 cache (k_descale == v_descale == nullptr) or
+// an FP8 one (both set).
+int attn_call(const void* q, const void* key_cache, const void* value_cache, const float* k_descale,
+              const float* v_descale, const int32_t* block_table, int32_t num_reqs,
+              int32_t max_blocks_per_req, int64_t num_blocks, int32_t block_size, const pcp_row_t* rows,
+              int32_t num_rows, int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
+              int32_t head_dim, float scale, void* out, float* lse, void* workspace,
+              size_t workspace_bytes, int32_t flags, int32_t* status, cudaStream_t s) {
     if (num_rows < 0 || total_q < 0 || num_reqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || max_blocks_per_req < 0 ||
         num_blocks < 0 || block_size < 1)
         return PCP_ERR_ARG;
@@ -139,7 +162,6 @@ extern "C" int pcp_attn_varlen(const void* q, const void* key_cache, const void*
         workspace_layout(num_rows, total_q, num_q_heads, head_dim, (int32_t)max_kv, flags);
     if (workspace_bytes < w.total) return PCP_ERR_WORKSPACE;
 
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     PrefillArgs a{};
     a.q = q;
@@ -166,6 +188,8 @@ extern "C" int pcp_attn_varlen(const void* q, const void* key_cache, const void*
     a.units = reinterpret_cast<const Unit*>(ws + w.units_sorted);
     a.num_units = reinterpret_cast<const int32_t*>(ws + w.header);
     a.status = status;
+    a.k_descale = k_descale;
+    a.v_descale = v_descale;
 
     int rc = launch_schedule(a, flags, reinterpret_cast<Unit*>(ws + w.units),
                              reinterpret_cast<Unit*>(ws + w.units_sorted),
@@ -183,6 +207,36 @@ extern "C" int pcp_attn_varlen(const void* q, const void* key_cache, const void*
     if (g_profile[1]) cudaEventRecord(g_profile[1], s);
     if (a.nparts > 0) rc = launch_separate_merge(a, s);
     return rc;
+}
+}  // namespace
+
+extern "C" int pcp_attn_varlen(const void* q, const void* key_cache, const void* value_cache,
+                               const int32_t* block_table, int32_t num_reqs,
+                               int32_t max_blocks_per_req, int64_t num_blocks, int32_t block_size,
+                               const pcp_row_t* rows, int32_t num_rows, int32_t total_q,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
+                               void* out, float* lse, void* workspace, size_t workspace_bytes,
+                               int32_t flags, int32_t* status, pcp_stream_t stream) {
+    return attn_call(q, key_cache, value_cache, nullptr, nullptr, block_table, num_reqs, max_blocks_per_req,
+                     num_blocks, block_size, rows, num_rows, total_q, num_q_heads, num_kv_heads, head_dim,
+                     scale, out, lse, workspace, workspace_bytes, flags, status,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int pcp_attn_varlen_fp8kv(const void* q, const void* key_cache, const void* value_cache,
+                                     const float* k_descale, const float* v_descale,
+                                     const int32_t* block_table, int32_t num_reqs, int32_t max_blocks_per_req,
+                                     int64_t num_blocks, int32_t block_size, const pcp_row_t* rows,
+                                     int32_t num_rows, int32_t total_q, int32_t num_q_heads,
+                                     int32_t num_kv_heads, int32_t head_dim, float scale, void* out,
+                                     float* lse, void* workspace, size_t workspace_bytes, int32_t flags,
+                                     int32_t* status, pcp_stream_t stream) {
+    if (num_rows > 0 && total_q > 0 && (!k_descale || !v_descale)) return PCP_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(k_descale) & 3u) || (reinterpret_cast<uintptr_t>(v_descale) & 3u))
+        return PCP_ERR_ALIGN;
+    return attn_call(q, key_cache, value_cache, k_descale, v_descale, block_table, num_reqs, max_blocks_per_req, num_blocks, block_size, rows, num_rows, total_q,
+                     num_q_heads, num_kv_heads, head_dim, scale, out, lse, workspace, workspace_bytes, flags,
+                     status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int pcp_set_profile_events(void* prefill_begin, void* prefill_end, void* decode_begin,

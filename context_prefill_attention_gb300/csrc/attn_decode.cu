@@ -16,7 +16,11 @@
 //    that each lane ends with one (key, head) score, one exponential per lane,
 //    fp32 online softmax per q head with lazy rescaling;
 //  * partial (out, lse) per split in the workspace, merged by log-sum-exp in
-//    decode_merge_kernel.
+//    decode_merge_kernel;
+//  * FP8 (e4m3) cache: the slabs hold the codes (rows of D bytes, unswizzled),
+//    each lane converts its 8 (D = 128) or 4 (D = 64) codes to fp32 after the
+//    shared load; the K descale folds into the query scale, the V descale into
+//    the split's output.
 // Also here: the LSE merge of the two prefill partials when the context and
 // new-token parts are computed separately.
 #include <cuda.h>
@@ -43,10 +47,11 @@ constexpr int kMaxPages = kDecodeChunk / 8;  // block-table entries of one chunk
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D, int GMAX>
+template <int D, int GMAX, bool F8 = false>
 struct DecCfg {
     static constexpr int kHalfBytes = kSlab * 128;                  // kSlab rows x 64 dims (bf16)
-    static constexpr int kSlabBytes = (D / 64) * kHalfBytes;        // K (or V) of one slab
+    // K (or V) of one slab: bf16 in D / 64 swizzled halves, or FP8 rows of D bytes
+    static constexpr int kSlabBytes = F8 ? kSlab * D : (D / 64) * kHalfBytes;
     static constexpr int kStageBytes = 2 * kSlabBytes;
     static constexpr int kBars = kStages * kStageBytes;
     static constexpr int kPages = kBars + 2 * kStages * 8;
@@ -56,8 +61,29 @@ struct DecCfg {
 
 // VEC consecutive bf16 of one key row, read from a 128-byte-swizzled slab:
 // row kr (0..15) of the slab, first dim e0 (a multiple of VEC).
-template <int VEC>
+template <int VEC, bool F8>
 __device__ __forceinline__ void load_row(const uint8_t* slab, int kr, int e0, float (&f)[VEC]) {
+    if constexpr (F8) {
+        // FP8 slab: row kr is VEC * 16 contiguous codes
+        const uint8_t* p = slab + kr * (VEC * 16) + e0;
+        if constexpr (VEC == 8) {
+            const uint2 u = *reinterpret_cast<const uint2*>(p);
+            float a[4], b[4];
+            e4m3x4_to_f32(u.x, a);
+            e4m3x4_to_f32(u.y, b);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                f[i] = a[i];
+                f[4 + i] = b[i];
+            }
+        } else {
+            float a[4];
+            e4m3x4_to_f32(*reinterpret_cast<const uint32_t*>(p), a);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) f[i] = a[i];
+        }
+        return;
+    }
     const int b = e0 * 2;
     const int half = b >> 7, bb = b & 127;
     const uint8_t* p = slab + half * (kSlab * 128) + kr * 128 + ((((bb >> 4) ^ (kr & 7)) << 4) | (bb & 15));
@@ -78,12 +104,12 @@ __device__ __forceinline__ void load_row(const uint8_t* slab, int kr, int e0, fl
     }
 }
 
-template <int D, int GMAX>
+template <int D, int GMAX, bool F8>
 __global__ void __launch_bounds__(kDecThreads)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   PrefillArgs a, float* __restrict__ dec_out, float* __restrict__ dec_lse, int max_splits,
                   int box_rows) {
-    using C = DecCfg<D, GMAX>;
+    using C = DecCfg<D, GMAX, F8>;
     constexpr int VEC = D / 16;
     const int split = blockIdx.x, hk = blockIdx.y, ri = blockIdx.z;
     if (!a.row_ok[ri]) return;
@@ -152,11 +178,17 @@ __global__ void __launch_bounds__(kDecThreads)
                         const int32_t base = page_row[key / bs - pg0];
                         if (base != oob) y = base + (key % bs);
                     }
+                    if constexpr (F8) {
+                        tma_load_3d(dst + b * box_rows * D, &tm_k, full_bar(st), 0, hk, y);
+                        tma_load_3d(dst + C::kSlabBytes + b * box_rows * D, &tm_v, full_bar(st), 0, hk, y);
+                    } else {
 #pragma unroll
-                    for (int h = 0; h < D / 64; ++h) {
-                        tma_load_3d(dst + h * C::kHalfBytes + b * box_rows * 128, &tm_k, full_bar(st), h * 64, hk, y);
-                        tma_load_3d(dst + C::kSlabBytes + h * C::kHalfBytes + b * box_rows * 128, &tm_v,
-                                    full_bar(st), h * 64, hk, y);
+                        for (int h = 0; h < D / 64; ++h) {
+                            tma_load_3d(dst + h * C::kHalfBytes + b * box_rows * 128, &tm_k, full_bar(st), h * 64,
+                                        hk, y);
+                            tma_load_3d(dst + C::kSlabBytes + h * C::kHalfBytes + b * box_rows * 128, &tm_v,
+                                        full_bar(st), h * 64, hk, y);
+                        }
                     }
                 }
             }
@@ -182,7 +214,8 @@ __global__ void __launch_bounds__(kDecThreads)
         for (int e = 0; e < VEC; ++e) acc[g][e] = 0.f;
     if (warp < kConsumerWarps) {
         // ---------------------------------------------------------------- consumers
-        const float sl2 = a.scale * kLog2e;
+        const float kd = F8 ? __ldg(a.k_descale + (size_t)row.req * a.hkv + hk) : 1.f;
+        const float sl2 = a.scale * kd * kLog2e;
         float qf[GP][VEC];
         const __nv_bfloat16* qbase = reinterpret_cast<const __nv_bfloat16*>(a.q) +
                                      ((size_t)row.q_start * a.hq + (size_t)hk * G) * D + dl * VEC;
@@ -208,7 +241,7 @@ __global__ void __launch_bounds__(kDecThreads)
                     const int r = base_r + kk;
                     float kf[VEC];
                     if (r < kSlab) {
-                        load_row<VEC>(kslab, r, dl * VEC, kf);
+                        load_row<VEC, F8>(kslab, r, dl * VEC, kf);
                     } else {
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) kf[e] = 0.f;
@@ -265,7 +298,7 @@ __global__ void __launch_bounds__(kDecThreads)
                     const int r = base_r + kk;
                     float vf[VEC];
                     if (r < kSlab && key_base + r < hi) {
-                        load_row<VEC>(vslab, r, dl * VEC, vf);
+                        load_row<VEC, F8>(vslab, r, dl * VEC, vf);
                     } else {
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) vf[e] = 0.f;  // rows past the end may hold anything
@@ -317,6 +350,7 @@ __global__ void __launch_bounds__(kDecThreads)
     }
     __syncthreads();
     // combine the consumer warps and write this split's partial
+    const float vd = F8 ? __ldg(a.v_descale + (size_t)row.req * a.hkv + hk) : 1.f;
     for (int i = threadIdx.x; i < G * D; i += kDecThreads) {
         const int g = i / D, d = i % D;
         float M = -INFINITY;
@@ -333,7 +367,7 @@ __global__ void __launch_bounds__(kDecThreads)
         }
         const int h = hk * G + g;
         const size_t slot = ((size_t)ri * a.hq + h) * max_splits + split;
-        dec_out[slot * D + d] = L > 0.f ? O / L : 0.f;
+        dec_out[slot * D + d] = L > 0.f ? O / L * vd : 0.f;
         if (d == 0) dec_lse[slot] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
     }
 }
@@ -409,25 +443,37 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-template <int D, int GMAX>
-int launch_decode_dg(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
-                     cudaStream_t stream) {
+template <int D, int GMAX, bool F8>
+int launch_decode_dgf(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
+                      cudaStream_t stream) {
     const int box_rows = a.block_size < kSlab ? a.block_size : kSlab;
+    const int64_t slots = a.num_blocks * a.block_size;
     CUtensorMap tk, tv;
-    if (!make_kv_map(&tk, a.key_cache, D, a.hkv, a.num_blocks * a.block_size, box_rows) ||
-        !make_kv_map(&tv, a.value_cache, D, a.hkv, a.num_blocks * a.block_size, box_rows))
-        return PCP_ERR_CUDA;
-    const int smem = DecCfg<D, GMAX>::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, GMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const bool maps = F8 ? make_kv_code_map(&tk, a.key_cache, D, a.hkv, slots, box_rows) &&
+                               make_kv_code_map(&tv, a.value_cache, D, a.hkv, slots, box_rows)
+                         : make_kv_map(&tk, a.key_cache, D, a.hkv, slots, box_rows) &&
+                               make_kv_map(&tv, a.value_cache, D, a.hkv, slots, box_rows);
+    if (!maps) return PCP_ERR_CUDA;
+    const int smem = DecCfg<D, GMAX, F8>::kSmem;
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_kernel<D, GMAX, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
     dim3 grid(max_splits, a.hkv, a.num_rows);
-    decode_kernel<D, GMAX><<<grid, kDecThreads, smem, stream>>>(tk, tv, a, dec_out, dec_lse, max_splits, box_rows);
+    decode_kernel<D, GMAX, F8><<<grid, kDecThreads, smem, stream>>>(tk, tv, a, dec_out, dec_lse, max_splits,
+                                                                    box_rows);
     e = cudaGetLastError();
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
     decode_merge_kernel<D><<<dim3(a.num_rows, a.hq), D, 0, stream>>>(a, dec_out, dec_lse, max_splits);
     e = cudaGetLastError();
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
     return PCP_OK;
+}
+
+template <int D, int GMAX>
+int launch_decode_dg(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
+                     cudaStream_t stream) {
+    return a.k_descale ? launch_decode_dgf<D, GMAX, true>(a, dec_out, dec_lse, max_splits, stream)
+                       : launch_decode_dgf<D, GMAX, false>(a, dec_out, dec_lse, max_splits, stream);
 }
 
 template <int D>

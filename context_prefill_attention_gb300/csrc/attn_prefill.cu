@@ -25,7 +25,13 @@
 //  * the two heads' MMAs interleave (S0 S1 | PV0 S0' PV1 S1' | ...) so each
 //    warpgroup's softmax overlaps the other head's MMAs;
 //  * every mbarrier wait is bounded: a wait that runs out sets PCP_ERR_TIMEOUT
-//    in the status word and the CTA winds down, freeing its TMEM.
+//    in the status word and the CTA winds down, freeing its TMEM;
+//  * FP8 (e4m3) cache: the producer's TMA brings the codes in (for D = 128 into
+//    the upper half of the stage they will be converted into, for D = 64 into
+//    a staging area), warps 10-11 convert them to bf16 in the 128-byte-swizzled
+//    layout the MMA reads (exact: every e4m3 value is a bf16 value), and the
+//    per-(request, kv head) descales fold into the softmax scale (K) and the
+//    epilogue's normalisation (V).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,9 +46,11 @@ namespace pcp {
 
 namespace {
 
-constexpr int kThreads = 384;  // 12 warps: two softmax warpgroups, producer, MMA, two spare
+constexpr int kThreads = 384;  // 12 warps: two softmax warpgroups, producer, MMA, two converters
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kConvWarp0 = 10;  // warps 10-11: FP8 code -> bf16 conversion (FP8 cache only)
+constexpr int kConvThreads = 64;
 // Tuning knobs (compile-time; the defaults are the measured best on GB300).
 #ifndef PCP_PREFILL_K_STAGES
 #define PCP_PREFILL_K_STAGES 2
@@ -70,7 +78,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // one pair in kPolyEvery of a tile uses the polynomial exp2 (a large value turns it off)
 constexpr int kPolyEvery = PCP_POLY_EXP_EVERY;
 
-template <int D>
+template <int D, bool F8 = false>
 struct Cfg {
     static constexpr int kHalves = D / 64;                 // 64-column (128-byte) sub-tiles
     static constexpr int kHalfBytes = 128 * 128;           // 128 rows x 128 bytes
@@ -78,8 +86,22 @@ struct Cfg {
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + 2 * kTileBytes;
     static constexpr int kV = kK + kNK * kTileBytes;
-    static constexpr int kBar = kV + kNV * kTileBytes;
-    static constexpr int kNumBars = 2 + 2 * kNK + 2 * kNV + 8 + 2;
+    // FP8 codes of one tile: 128 rows x D bytes. D = 128: in the upper half of
+    // the stage they are converted into (row r of the codes overlays row r of
+    // that half, so a row is read whole before it is written); D = 64: their own
+    // staging area after the V stages.
+    static constexpr int kCodeBytes = kBlockN * D;
+    static constexpr bool kInPlace = D == 128;
+    static constexpr int kCK = kV + kNV * kTileBytes;
+    static constexpr int kCV = kCK + (F8 && !kInPlace ? kNK * kCodeBytes : 0);
+    static constexpr int kBar = kCV + (F8 && !kInPlace ? kNV * kCodeBytes : 0);
+    __host__ __device__ static constexpr int code_k(int s) {
+        return kInPlace ? kK + s * kTileBytes + kHalfBytes : kCK + s * kCodeBytes;
+    }
+    __host__ __device__ static constexpr int code_v(int s) {
+        return kInPlace ? kV + s * kTileBytes + kHalfBytes : kCV + s * kCodeBytes;
+    }
+    static constexpr int kNumBars = 2 + 2 * kNK + 2 * kNV + 8 + 2 + (F8 ? kNK + kNV : 0);
     static constexpr int kMisc = kBar + kNumBars * 8;      // tmem address, abort flag, item ring
     static constexpr int kSmem = kMisc + 16 + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 512;
@@ -123,6 +145,46 @@ __device__ __forceinline__ Item decode_item(const Unit* units, int32_t idx, int3
     return it;
 }
 
+// One tile of FP8 codes (128 rows x D bytes, row-major) -> bf16 in the
+// 128-byte-swizzled K-major layout of a K or V stage (dims 64h..64h+63 of row
+// r in half h, 16-byte chunk c of that row at chunk c ^ (r & 7)). Run by the 64
+// converter threads (ct = 0..63): D / 16 threads per row, each converting 16
+// codes (one 16-byte load) into two 16-byte chunks. In place (D = 128) the codes
+// of row r sit where half 1 of row r goes; the threads of a row are in one warp
+// and all of them load before any of them stores.
+template <int D>
+__device__ __forceinline__ void convert_codes(const uint8_t* codes, uint8_t* dst, int ct) {
+    constexpr int kTpr = D / 16;             // threads per row
+    constexpr int kRpp = kConvThreads / kTpr;  // rows per pass
+    constexpr int kBatch = 4;                // rows per thread between warp barriers
+    const int t = ct % kTpr, rsub = ct / kTpr;
+    const int h = t / 4, c0 = 2 * (t % 4);
+    // threads of the second half store their odd chunk first, so the eight
+    // threads of a row hit eight different bank groups in each store
+    const int first = c0 + (t >= 4 ? 1 : 0), second = c0 + (t >= 4 ? 0 : 1);
+#pragma unroll 1
+    for (int r0 = 0; r0 < kBlockN; r0 += kRpp * kBatch) {
+        uint4 c[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b)
+            c[b] = *reinterpret_cast<const uint4*>(codes + (r0 + kRpp * b + rsub) * D + 16 * t);
+        __syncwarp();
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int r = r0 + kRpp * b + rsub;
+            const uint2 w0 = e4m3x4_to_bf16x4(c[b].x), w1 = e4m3x4_to_bf16x4(c[b].y);
+            const uint2 w2 = e4m3x4_to_bf16x4(c[b].z), w3 = e4m3x4_to_bf16x4(c[b].w);
+            const uint4 lo = make_uint4(w0.x, w0.y, w1.x, w1.y);  // dims 16t .. 16t+7
+            const uint4 hi = make_uint4(w2.x, w2.y, w3.x, w3.y);  // dims 16t+8 .. 16t+15
+            uint8_t* row = dst + h * (128 * 128) + r * 128;
+            const bool lo_first = first == c0;
+            *reinterpret_cast<uint4*>(row + ((first ^ (r & 7)) << 4)) = lo_first ? lo : hi;
+            *reinterpret_cast<uint4*>(row + ((second ^ (r & 7)) << 4)) = lo_first ? hi : lo;
+        }
+        __syncwarp();
+    }
+}
+
 // S = Q_slot K^T over D (K-major A and B, 128-byte swizzle).
 template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_smem, uint32_t k_smem) {
@@ -146,11 +208,11 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
     }
 }
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, PrefillArgs a) {
-    using C = Cfg<D>;
+    using C = Cfg<D, F8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -168,6 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto o_done = [&](int g) { return bx + 32 + 8 * g; };
     auto o_free = [&](int g) { return bx + 48 + 8 * g; };
     auto p_half = [&](int g) { return bx + 64 + 8 * g; };  // first 64 keys of P ready
+    // FP8: the codes of K / V stage s have landed
+    auto kc_full = [&](int s) { return bx + 80 + 8 * s; };
+    auto vc_full = [&](int s) { return bx + 80 + 8 * (kNK + s); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
 
@@ -180,8 +245,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
-        for (int s = 0; s < kNK; ++s) { mbar_init(k_full(s), 1); mbar_init(k_empty(s), 1); }
-        for (int s = 0; s < kNV; ++s) { mbar_init(v_full(s), 1); mbar_init(v_empty(s), 1); }
+        // FP8: a stage is full when both converter warps have arrived
+        const uint32_t fill_count = F8 ? kConvThreads / 32 : 1;
+        for (int s = 0; s < kNK; ++s) { mbar_init(k_full(s), fill_count); mbar_init(k_empty(s), 1); }
+        for (int s = 0; s < kNV; ++s) { mbar_init(v_full(s), fill_count); mbar_init(v_empty(s), 1); }
+        if (F8) {
+            for (int s = 0; s < kNK; ++s) mbar_init(kc_full(s), 1);
+            for (int s = 0; s < kNV; ++s) mbar_init(vc_full(s), 1);
+        }
         for (int g = 0; g < 2; ++g) {
             mbar_init(s_full(g), 1);
             mbar_init(p_full(g), 128);
@@ -257,24 +328,69 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int ks = kt % kNK;
                 if (!(ok = mbar_wait_warp(k_empty(ks), ((kt / kNK) & 1) ^ 1, abort_flag))) break;
-                if (lane == 0) mbar_arrive_expect_tx(k_full(ks), C::kTileBytes);
-                __syncwarp();
-                if (lane < pages)
-                    for (int h = 0; h < C::kHalves; ++h)
-                        tma_load_3d(sbase + C::kK + ks * C::kTileBytes + h * C::kHalfBytes + lane * bs * 128,
-                                    &tm_k, k_full(ks), h * 64, it.hk, y);
+                if constexpr (F8) {
+                    // codes: one box of bs rows x D bytes per page
+                    if (lane == 0) mbar_arrive_expect_tx(kc_full(ks), C::kCodeBytes);
+                    __syncwarp();
+                    if (lane < pages)
+                        tma_load_3d(sbase + C::code_k(ks) + lane * bs * D, &tm_k, kc_full(ks), 0, it.hk, y);
+                } else {
+                    if (lane == 0) mbar_arrive_expect_tx(k_full(ks), C::kTileBytes);
+                    __syncwarp();
+                    if (lane < pages)
+                        for (int h = 0; h < C::kHalves; ++h)
+                            tma_load_3d(sbase + C::kK + ks * C::kTileBytes + h * C::kHalfBytes + lane * bs * 128,
+                                        &tm_k, k_full(ks), h * 64, it.hk, y);
+                }
                 ++kt;
                 const int vs = vt % kNV;
                 if (!(ok = mbar_wait_warp(v_empty(vs), ((vt / kNV) & 1) ^ 1, abort_flag))) break;
-                if (lane == 0) mbar_arrive_expect_tx(v_full(vs), C::kTileBytes);
-                __syncwarp();
-                if (lane < pages)
-                    for (int h = 0; h < C::kHalves; ++h)
-                        tma_load_3d(sbase + C::kV + vs * C::kTileBytes + h * C::kHalfBytes + lane * bs * 128,
-                                    &tm_v, v_full(vs), h * 64, it.hk, y);
+                if constexpr (F8) {
+                    if (lane == 0) mbar_arrive_expect_tx(vc_full(vs), C::kCodeBytes);
+                    __syncwarp();
+                    if (lane < pages)
+                        tma_load_3d(sbase + C::code_v(vs) + lane * bs * D, &tm_v, vc_full(vs), 0, it.hk, y);
+                } else {
+                    if (lane == 0) mbar_arrive_expect_tx(v_full(vs), C::kTileBytes);
+                    __syncwarp();
+                    if (lane < pages)
+                        for (int h = 0; h < C::kHalves; ++h)
+                            tma_load_3d(sbase + C::kV + vs * C::kTileBytes + h * C::kHalfBytes + lane * bs * 128,
+                                        &tm_v, v_full(vs), h * 64, it.hk, y);
+                }
                 ++vt;
             }
             ++c;
+        }
+        if (!ok && lane == 0) report_status(a.status, PCP_ERR_TIMEOUT);
+    } else if (F8 && warp >= kConvWarp0) {
+        // ------------------------------------------------------------ FP8 converters
+        // Same walk over items and tiles as the producer: per K (then V) stage wait
+        // for the codes, convert them to bf16 in place, make the generic-proxy
+        // stores visible to the tensor cores' async proxy, then mark the stage full.
+        const int ct = threadIdx.x - kConvWarp0 * 32;
+        uint32_t kt = 0, vt = 0;
+        bool ok = true;
+        for (int32_t round = 0; ok; ++round) {
+            const int32_t idx = item_of_round(round);
+            if (idx >= total_items) break;
+            const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, bs);
+            for (int32_t j = 0; j < it.n_tiles && ok; ++j) {
+                const int ks = kt % kNK;
+                if (!(ok = mbar_wait_warp(kc_full(ks), (kt / kNK) & 1, abort_flag))) break;
+                convert_codes<D>(smem + C::code_k(ks), smem + C::kK + ks * C::kTileBytes, ct);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(k_full(ks));
+                ++kt;
+                const int vs = vt % kNV;
+                if (!(ok = mbar_wait_warp(vc_full(vs), (vt / kNV) & 1, abort_flag))) break;
+                convert_codes<D>(smem + C::code_v(vs), smem + C::kV + vs * C::kTileBytes, ct);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(v_full(vs));
+                ++vt;
+            }
         }
         if (!ok && lane == 0) report_status(a.status, PCP_ERR_TIMEOUT);
     } else if (warp == kMmaWarp) {
@@ -378,7 +494,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
         const uint32_t t_s = tmem + lane_base + C::tmem_s(g);
         const uint32_t t_o = tmem + lane_base + C::tmem_o(g);
-        const float sl2 = a.scale * kLog2e;
         uint32_t sph = 0, oph = 0;
         bool ok = true;
         for (int32_t round = 0; ok; ++round) {
@@ -387,6 +502,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, bs);
             if (g >= it.nslots) continue;
             const int h = it.h0 + g;
+            // FP8: the K descale scales every score (the V descale the output, below);
+            // it is re-read per tile (an L1 hit) rather than held across the loop,
+            // which keeps the score row within the register budget
+            const float* kd_ptr = F8 ? a.k_descale + (size_t)it.req * a.hkv + it.hk : nullptr;
             const bool valid = r < it.rows_valid;
             const int32_t pos = it.pos0 + min(r, it.rows_valid - 1);
             const int32_t tok = it.q_tok0 + r;
@@ -403,6 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
                 tmem_wait_ld();
                 float* sf = reinterpret_cast<float*>(s);
+                const float sl2 = F8 ? a.scale * __ldg(kd_ptr) * kLog2e : a.scale * kLog2e;
                 const int32_t key0 = it.kb + j * kBlockN;
                 const bool full = key0 >= it.k_lo && key0 + kBlockN <= it.k_hi &&
                                   key0 + kBlockN - 1 <= it.pos0;
@@ -494,7 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             // ---- epilogue: out = O / l, lse = ln 2 * (m + log2 l)
             const bool has = l > 0.f;
-            const float inv = has ? 1.f / l : 0.f;
+            const float vd = F8 ? __ldg(a.v_descale + (size_t)it.req * a.hkv + it.hk) : 1.f;
+            const float inv = has ? vd / l : 0.f;
             const float lse_v = has ? (m + __log2f(l)) * kLn2 : -INFINITY;
             if (n > 0) {
                 if (!(ok = mbar_wait_warp(o_done(g), oph, abort_flag))) break;
@@ -711,17 +832,35 @@ bool make_map(CUtensorMap* m, const void* base, int D, int64_t mid, int64_t oute
     return r == CUDA_SUCCESS;
 }
 
-template <int D>
+// 3-D byte view [outer][mid][D] of an FP8 cache with a box of {D, 1, rows},
+// no swizzle (a box row is D contiguous bytes: 64 or 128).
+bool make_code_map(CUtensorMap* m, const void* base, int D, int64_t mid, int64_t outer, int rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)mid, (cuuint64_t)outer};
+    cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)(D * mid)};
+    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D, bool F8>
 int launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
     CUtensorMap tq, tk, tv;
-    if (!make_map(&tq, a.q, D, a.hq, a.total_q, kBlockM) ||
-        !make_map(&tk, a.key_cache, D, a.hkv, a.num_blocks * a.block_size, a.block_size) ||
-        !make_map(&tv, a.value_cache, D, a.hkv, a.num_blocks * a.block_size, a.block_size))
-        return PCP_ERR_CUDA;
-    const int smem = Cfg<D>::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int64_t slots = a.num_blocks * a.block_size;
+    const bool maps = F8 ? make_code_map(&tk, a.key_cache, D, a.hkv, slots, a.block_size) &&
+                               make_code_map(&tv, a.value_cache, D, a.hkv, slots, a.block_size)
+                         : make_map(&tk, a.key_cache, D, a.hkv, slots, a.block_size) &&
+                               make_map(&tv, a.value_cache, D, a.hkv, slots, a.block_size);
+    if (!maps || !make_map(&tq, a.q, D, a.hq, a.total_q, kBlockM)) return PCP_ERR_CUDA;
+    const int smem = Cfg<D, F8>::kSmem;
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
-    prefill_kernel<D><<<num_sms(), kThreads, smem, stream>>>(tq, tk, tv, a);
+    prefill_kernel<D, F8><<<num_sms(), kThreads, smem, stream>>>(tq, tk, tv, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
     return PCP_OK;
@@ -739,13 +878,18 @@ int launch_schedule(const PrefillArgs& a, int32_t flags, Unit* units, Unit* unit
 }
 
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
-    if (a.d == 64) return launch_prefill_d<64>(a, stream);
-    if (a.d == 128) return launch_prefill_d<128>(a, stream);
+    const bool f8 = a.k_descale != nullptr;
+    if (a.d == 64) return f8 ? launch_prefill_d<64, true>(a, stream) : launch_prefill_d<64, false>(a, stream);
+    if (a.d == 128) return f8 ? launch_prefill_d<128, true>(a, stream) : launch_prefill_d<128, false>(a, stream);
     return PCP_ERR_UNSUPPORTED;
 }
 
 bool make_kv_map(CUtensorMap* m, const void* base, int D, int64_t mid, int64_t outer, int rows) {
     return make_map(m, base, D, mid, outer, rows);
+}
+
+bool make_kv_code_map(CUtensorMap* m, const void* base, int D, int64_t mid, int64_t outer, int rows) {
+    return make_code_map(m, base, D, mid, outer, rows);
 }
 
 }  // namespace pcp

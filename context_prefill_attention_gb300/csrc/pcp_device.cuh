@@ -302,4 +302,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// ---------------------------------------------------------------- FP8 (e4m3)
+
+// Four e4m3 codes (byte i of w = element i) -> their values as fp32. Every
+// e4m3 value (|x| <= 448, subnormals down to 2^-9) is exact in f16 and in f32,
+// so the two hardware conversions (e4m3x2 -> f16x2, f16 -> f32) are exact.
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float (&f)[4]) {
+    asm("{\n\t.reg .b16 c0, c1, a0, a1, a2, a3;\n\t.reg .b32 h0, h1;\n\t"
+        "mov.b32 {c0, c1}, %4;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h0, c0;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h1, c1;\n\t"
+        "mov.b32 {a0, a1}, h0;\n\t"
+        "mov.b32 {a2, a3}, h1;\n\t"
+        "cvt.f32.f16 %0, a0;\n\t"
+        "cvt.f32.f16 %1, a1;\n\t"
+        "cvt.f32.f16 %2, a2;\n\t"
+        "cvt.f32.f16 %3, a3;\n\t}"
+        : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3])
+        : "r"(w));
+}
+
+// Four e4m3 codes -> four bf16 (two packed pairs, element order kept); exact,
+// since every e4m3 value is a bf16 value.
+__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
+    float f[4];
+    e4m3x4_to_f32(w, f);
+    return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+}
+
+// Two floats -> two e4m3 codes (lo in the low byte), round to nearest even,
+// magnitudes beyond the largest finite value (448) saturate to it.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 }  // namespace pcp

@@ -83,11 +83,18 @@ struct PrefillArgs {
     const Unit* units;
     const int32_t* num_units;
     int32_t* status;
+    // FP8 (e4m3) cache: per-(request, kv head) descales [num_reqs][hkv]; both
+    // null for a bf16 cache
+    const float* k_descale;
+    const float* v_descale;
 };
 
 // TMA map of a bf16 tensor viewed as [outer][mid][D] with a box of 64 x 1 x rows
 // and 128-byte swizzle (Q: [T][Hq][D]; a paged cache: [blocks * bs][Hkv][D]).
 bool make_kv_map(CUtensorMap* m, const void* base, int D, int64_t mid, int64_t outer, int rows);
+// TMA map of an FP8 cache viewed as bytes [outer][mid][D] with a box of D x 1 x
+// rows, no swizzle.
+bool make_kv_code_map(CUtensorMap* m, const void* base, int D, int64_t mid, int64_t outer, int rows);
 
 int launch_schedule(const PrefillArgs& a, int32_t flags, Unit* units, Unit* units_sorted,
                     int32_t* header, int32_t* row_ok, int64_t max_units, cudaStream_t stream);
@@ -98,6 +105,10 @@ int launch_separate_merge(const PrefillArgs& a, cudaStream_t stream);
 int launch_cache_write(const void* k, const void* v, const int64_t* slot, int32_t num_tokens,
                        int32_t vec_per_tok, void* key_cache, void* value_cache, int64_t num_slots,
                        int32_t* status, cudaStream_t stream);
+// FP8 cache write: vec_per_tok = 16-element groups per token row.
+int launch_cache_write_fp8(const void* k, const void* v, const int64_t* slot, int32_t num_tokens,
+                           int32_t vec_per_tok, void* key_cache, void* value_cache, int64_t num_slots,
+                           float k_scale, float v_scale, int32_t* status, cudaStream_t stream);
 int launch_lse_merge(const float* out_a, const float* lse_a, const float* out_b, const float* lse_b,
                      void* out, float* lse, int32_t total_q, int32_t hq, int32_t d,
                      cudaStream_t stream);

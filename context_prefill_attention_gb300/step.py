@@ -9,6 +9,12 @@ A step ("Feat/pcp qwen36 hybrid", "Changes"; "[MRv2][PCP] Carry the row plan
    before attention on the same stream;
 4. ``pcp_attn_varlen``: prefill, context and decode rows in one call.
 
+With ``kv_cache_dtype="fp8"`` the cache holds e4m3 codes: step 3 is
+``pcp_kv_cache_write_fp8`` with the layer's k/v scales and step 4
+``pcp_attn_varlen_fp8kv`` with descales of shape (num_reqs, num_kv_heads),
+by default those scales broadcast ("[MRv2] FlashAttention PCP support ...",
+the context-pass call).
+
 This module only sequences those calls and owns the buffers (the reviewer's
 "use the workspace and pass out so we aren't allocating each step").
 """
@@ -27,7 +33,12 @@ class PcpStep:
 
     def __init__(self, *, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
                  num_shards: int, split_mode: int, max_tokens: int, max_reqs: int, max_kv_len: int,
-                 flags: int = 0, device: str = "cuda"):
+                 flags: int = 0, device: str = "cuda", kv_cache_dtype: str = "bf16", k_scale: float = 1.0,
+                 v_scale: float = 1.0):
+        if kv_cache_dtype not in ("bf16", "fp8"):
+            raise ValueError(f"kv_cache_dtype {kv_cache_dtype!r}: 'bf16' or 'fp8'")
+        self.kv_fp8 = kv_cache_dtype == "fp8"
+        self.k_scale, self.v_scale = float(k_scale), float(v_scale)
         self.hq, self.hkv, self.d = num_q_heads, num_kv_heads, head_dim
         self.bs, self.shards, self.split_mode, self.flags = block_size, num_shards, split_mode, flags
         self.device = torch.device(device)
@@ -43,6 +54,13 @@ class PcpStep:
         self.slot_dev = torch.empty(max(max_tokens, 1), dtype=torch.int64, device=self.device)
         self.rows_host = torch.empty((self.max_rows, 8), dtype=torch.int32, pin_memory=True)
         self.slot_host = torch.empty(max(max_tokens, 1), dtype=torch.int64, pin_memory=True)
+        # FP8 descales [max_reqs, Hkv]: the layer scales broadcast; a caller may overwrite them
+        self.k_descale = self.v_descale = None
+        if self.kv_fp8:
+            self.k_descale = torch.full((max(max_reqs, 1), num_kv_heads), self.k_scale, dtype=torch.float32,
+                                        device=self.device)
+            self.v_descale = torch.full((max(max_reqs, 1), num_kv_heads), self.v_scale, dtype=torch.float32,
+                                        device=self.device)
         self.plan = None
 
     def build_plan(self, query_len: Sequence[int], num_computed: Sequence[int], block_table_host) -> dict:
@@ -61,8 +79,12 @@ class PcpStep:
     def write_cache(self, k_new: torch.Tensor, v_new: torch.Tensor, key_cache: torch.Tensor,
                     value_cache: torch.Tensor, stream=None) -> None:
         T = int(k_new.shape[0])
-        L.pcp_kv_cache_write(k_new, v_new, self.slot_dev[:T], key_cache, value_cache, status=self.status,
-                             stream=stream)
+        if self.kv_fp8:
+            L.pcp_kv_cache_write_fp8(k_new, v_new, self.slot_dev[:T], key_cache, value_cache, self.k_scale,
+                                     self.v_scale, status=self.status, stream=stream)
+        else:
+            L.pcp_kv_cache_write(k_new, v_new, self.slot_dev[:T], key_cache, value_cache, status=self.status,
+                                 stream=stream)
 
     def attend(self, q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
                block_table_dev: torch.Tensor, scale: float, stream=None):
@@ -70,6 +92,12 @@ class PcpStep:
         n = int(self.plan["rows"].shape[0])
         out = self.out[:T]
         lse = self.lse_buf[:T * self.hq].view(self.hq, T)
+        if self.kv_fp8:
+            R = int(block_table_dev.shape[0])
+            return L.pcp_attn_varlen_fp8kv(q, key_cache, value_cache, self.k_descale[:R], self.v_descale[:R],
+                                           block_table_dev, self.rows_dev[:n], scale, out=out, lse=lse,
+                                           workspace=self.workspace, flags=self.flags, status=self.status,
+                                           stream=stream)
         return L.pcp_attn_varlen(q, key_cache, value_cache, block_table_dev, self.rows_dev[:n], scale,
                                  out=out, lse=lse, workspace=self.workspace, flags=self.flags,
                                  status=self.status, stream=stream)
@@ -90,10 +118,11 @@ class PcpStep:
 
 def write_positions(key_cache: torch.Tensor, value_cache: torch.Tensor, block_table_host,
                     start: Sequence[int], k_list, v_list, block_size: int,
-                    status: Optional[torch.Tensor] = None) -> None:
+                    status: Optional[torch.Tensor] = None, fp8_scales=None) -> None:
     """Write K/V rows of positions ``[start[r], start[r] + len)`` of every request
     into the paged cache, through the library's own plan (one shard) and cache
-    writer — what earlier steps of a real engine would have left in the cache."""
+    writer — what earlier steps of a real engine would have left in the cache.
+    ``fp8_scales=(k_scale, v_scale)`` writes an FP8 cache."""
     lens = [int(k.shape[0]) for k in k_list]
     if sum(lens) == 0:
         return
@@ -102,4 +131,7 @@ def write_positions(key_cache: torch.Tensor, value_cache: torch.Tensor, block_ta
     slot = torch.from_numpy(plan["slot_mapping"]).to(dev)
     k = torch.cat([x.to(dev) for x in k_list], 0)
     v = torch.cat([x.to(dev) for x in v_list], 0)
-    L.pcp_kv_cache_write(k, v, slot, key_cache, value_cache, status=status)
+    if fp8_scales is not None:
+        L.pcp_kv_cache_write_fp8(k, v, slot, key_cache, value_cache, fp8_scales[0], fp8_scales[1], status=status)
+    else:
+        L.pcp_kv_cache_write(k, v, slot, key_cache, value_cache, status=status)

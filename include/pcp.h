@@ -238,6 +238,45 @@ int pcp_attn_varlen_noalloc(const void* q, const void* key_cache, const void* va
                             int32_t flags, int32_t* status, pcp_stream_t stream);
 
 /*
+ * pcp_kv_cache_write_fp8 — device. pcp_kv_cache_write into an FP8 cache: one
+ * byte per element, the e4m3 code (OCP 8-bit floating point, no infinities,
+ * largest finite 448) of x / k_scale for keys and x / v_scale for values, the
+ * division correctly rounded in fp32, then rounded to nearest even and
+ * saturated at +-448. k_scale and v_scale are the layer's scales ("[MRv2]
+ * FlashAttention PCP support ...", the context-pass call: layer._k_scale,
+ * layer._v_scale), host floats, finite and > 0 (else PCP_ERR_ARG).
+ * key_cache, value_cache: [num_blocks][block_size][Hkv][D] bytes. Same slot,
+ * PAD and status rules as pcp_kv_cache_write. Supported: Hkv * D a multiple of
+ * 16. Errors: PCP_ERR_ARG, PCP_ERR_ALIGN, PCP_ERR_UNSUPPORTED, PCP_ERR_CUDA.
+ */
+int pcp_kv_cache_write_fp8(const void* k, const void* v, const int64_t* slot_mapping,
+                           int32_t num_tokens, void* key_cache, void* value_cache, int64_t num_blocks,
+                           int32_t block_size, int32_t num_kv_heads, int32_t head_dim, float k_scale,
+                           float v_scale, int32_t* status, pcp_stream_t stream);
+
+/*
+ * pcp_attn_varlen_fp8kv — device. pcp_attn_varlen over an FP8 (e4m3) paged
+ * cache with per-(request, kv head) descales ("[MRv2] FlashAttention PCP
+ * support ...", the context-pass call: descales of shape (num_seqs,
+ * num_kv_heads)). Key k of request r and kv head g is code_K[r][k][g][:] *
+ * k_descale[r][g], its value code_V[...] * v_descale[r][g]; q stays bf16 and
+ * the result is the same attention as pcp_attn_varlen over those keys and
+ * values (the codes are widened to bf16 exactly; the descales multiply the
+ * fp32 scores and outputs).
+ * key_cache, value_cache: [num_blocks][block_size][Hkv][D] bytes (as written
+ * by pcp_kv_cache_write_fp8); k_descale, v_descale: device fp32
+ * [num_reqs][Hkv]. Every other argument, check, flag and error is that of
+ * pcp_attn_varlen, with the same workspace size.
+ */
+int pcp_attn_varlen_fp8kv(const void* q, const void* key_cache, const void* value_cache,
+                          const float* k_descale, const float* v_descale, const int32_t* block_table,
+                          int32_t num_reqs, int32_t max_blocks_per_req, int64_t num_blocks,
+                          int32_t block_size, const pcp_row_t* rows, int32_t num_rows, int32_t total_q,
+                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
+                          void* out, float* lse, void* workspace, size_t workspace_bytes, int32_t flags,
+                          int32_t* status, pcp_stream_t stream);
+
+/*
  * pcp_lse_merge — device. Merge two partial results of the same queries by
  * log-sum-exp ("[MRv2] FlashAttention PCP support ...": (ctx_out, ctx_lse)
  * combined with the new-token pass; the per-step LSE-combine of the DCP

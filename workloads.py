@@ -24,6 +24,13 @@ the lengths and the block-table permutation; every tensor of request ``r``
 comes from its own generator seeded with ``tensor_seed(seed, r, kind)`` so a
 test can rebuild a single request without drawing the whole batch. Values are
 ``torch.randn`` in float32 rounded to bf16 (round to nearest even).
+
+FP8 (e4m3) cache inputs: the layer scales ``FP8_K_SCALE`` / ``FP8_V_SCALE``
+(the N(0, 1) values stay far inside 448 x scale) and, per workload, the
+descales of shape (num_reqs, num_kv_heads): the layer scales broadcast, or a
+seeded factor in [0.5, 1) times them per (request, kv head), so that the
+dequantised values stay N(0, 1)-sized like the bf16 inputs (the output is
+rounded to bf16, whose half-ulp reaches the 1e-2 bound at |out| = 5.12).
 """
 from __future__ import annotations
 
@@ -198,3 +205,24 @@ def sample_segments(segments: Sequence, per_segment: int, seed: int) -> torch.Te
     if not picks:
         return torch.empty(0, dtype=torch.int64)
     return torch.unique(torch.cat(picks)).to(torch.int64)
+
+
+# Layer scales of an FP8 (e4m3) cache: N(0, 1) K/V values of magnitude < 5 map to
+# codes of magnitude < 100 (K) and < 167 (V), inside e4m3's 448.
+FP8_K_SCALE = 0.05
+FP8_V_SCALE = 0.03
+
+
+def fp8_descales(spec: WorkloadSpec, mode: str = "layer"):
+    """(k_descale, v_descale), float32 [num_reqs, num_kv_heads] on the CPU:
+    ``layer`` broadcasts the layer scales; ``varied`` multiplies them by a
+    seeded factor in [0.5, 1) per (request, kv head)."""
+    R, H = spec.num_reqs, spec.num_kv_heads
+    if mode == "layer":
+        return torch.full((R, H), FP8_K_SCALE), torch.full((R, H), FP8_V_SCALE)
+    if mode != "varied":
+        raise ValueError(mode)
+    g = torch.Generator().manual_seed(tensor_seed(spec.seed, 0, 7))
+    kd = FP8_K_SCALE * (0.5 + 0.5 * torch.rand((R, H), generator=g))
+    vd = FP8_V_SCALE * (0.5 + 0.5 * torch.rand((R, H), generator=g))
+    return kd.to(torch.float32), vd.to(torch.float32)
