@@ -70,6 +70,17 @@ constexpr int kConvThreads = 64;
 // written keys 0-63 of P; 0: one issue after all of P is written. Measured on
 // GB300: the split is 4-5 % slower (an extra handshake per tile), so it is off.
 constexpr bool kPvSplit = PCP_PV_SPLIT != 0;
+#ifndef PCP_PREFILL_MAXFREE
+#define PCP_PREFILL_MAXFREE 1
+#endif
+// 1: once a row has a finite reference max, a tile's exponentials use it
+// directly (no row-max reduction before them); a tile whose row sum reaches
+// kMaxFreeLimit falls back to the exact path (max, rescale). 0: every tile
+// computes its row max first.
+constexpr bool kMaxFree = PCP_PREFILL_MAXFREE != 0;
+// p <= 2^64 keeps O (<= p x keys x |v|) and l far inside fp32 for any bf16 V of
+// moderate size and any sequence length this library accepts
+constexpr float kMaxFreeLimit = 18446744073709551616.0f;  // 2^64
 constexpr int kNK = PCP_PREFILL_K_STAGES;  // K stages
 constexpr int kNV = PCP_PREFILL_V_STAGES;  // V stages
 constexpr float kLog2e = 1.4426950408889634f;
@@ -516,23 +527,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sph ^= 1;
                 tc_fence_after();
                 uint32_t s[128];
-                tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-                tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-                tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-                tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-                tmem_wait_ld();
                 float* sf = reinterpret_cast<float*>(s);
                 const float sl2 = F8 ? a.scale * __ldg(kd_ptr) * kLog2e : a.scale * kLog2e;
                 const int32_t key0 = it.kb + j * kBlockN;
                 const bool full = key0 >= it.k_lo && key0 + kBlockN <= it.k_hi &&
                                   key0 + kBlockN - 1 <= it.pos0;
-                if (!full) {
-                    const int32_t lo = it.k_lo - key0;
-                    const int32_t hi = min(it.k_hi, pos + 1) - key0;
+                // S row of this thread into registers, keys outside [k_lo, min(k_hi, pos + 1)) at -inf
+                auto load_scores = [&]() {
+                    tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+                    tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+                    tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+                    tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+                    tmem_wait_ld();
+                    if (!full) {
+                        const int32_t lo = it.k_lo - key0;
+                        const int32_t hi = min(it.k_hi, pos + 1) - key0;
 #pragma unroll
-                    for (int c2 = 0; c2 < 128; ++c2)
-                        if (c2 < lo || c2 >= hi) sf[c2] = -INFINITY;
+                        for (int c2 = 0; c2 < 128; ++c2)
+                            if (c2 < lo || c2 >= hi) sf[c2] = -INFINITY;
+                    }
+                };
+                // p of a pair: ex2, or (polynomial knob) the FMA-pipe exp2 for every
+                // kPolyEvery-th pair (a masked key then gets ~1e-38, not 0)
+                auto exp_pair = [&](float2 x, int c2) -> float2 {
+                    if (c2 % kPolyEvery == kPolyEvery - 1) return exp2_poly2(x);
+                    return make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                };
+                load_scores();
+                // Fast path: every row of the warp already has a finite reference max m;
+                // p = 2^(s * scale * log2 e - m) straight away, no row max first. If a
+                // row's tile sum reaches 2^64 (its scores rose by ~64 in log2 units) the
+                // warp reloads S, which P has not yet overwritten, and takes the exact path.
+                bool exact = true;
+                if (kMaxFree && __all_sync(0xffffffffu, m != -INFINITY)) {
+                    const float2 sl2v = make_float2(sl2, sl2), nmu = make_float2(-m, -m);
+                    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                     make_float2(0.f, 0.f)};
+                    uint32_t p[64];
+#pragma unroll
+                    for (int c2 = 0; c2 < 64; ++c2) {
+                        const float2 e = exp_pair(ffma2(make_float2(sf[2 * c2], sf[2 * c2 + 1]), sl2v, nmu), c2);
+                        acc[c2 % 4] = fadd2(acc[c2 % 4], e);
+                        p[c2] = pack_bf16x2(e.x, e.y);
+                    }
+                    const float2 a03 = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+                    const float ts = a03.x + a03.y;
+                    if (!__any_sync(0xffffffffu, !(ts < kMaxFreeLimit))) {
+                        tmem_st32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+                        tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+                        tmem_wait_st();
+                        tc_fence_before();
+                        if (kPvSplit) mbar_arrive(p_half(g));
+                        mbar_arrive(p_full(g));
+                        l += ts;
+                        exact = false;
+                    } else {
+                        load_scores();
+                    }
                 }
+                if (!exact) continue;
                 // row max: eight independent chains of three-input maxima
                 float part[8];
 #pragma unroll
@@ -575,11 +628,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st16(t_o + 16 * c2, o);
                     }
                 }
-                // p = 2^(s * scale * log2 e - m), two lanes per instruction. With the
-                // polynomial knob on, every kPolyEvery-th pair goes to the FMA pipe (a
-                // masked key then gets ~1e-38, not 0); by default all use ex2.
-                // P goes back to TMEM in two halves (keys 0-63, then 64-127); the MMA warp
-                // starts O += P V on the first half while the second is computed.
+                // Exact path: p = 2^(s * scale * log2 e - m) with m this row's lazily
+                // updated max, two lanes per instruction. P goes back to TMEM in two
+                // halves (keys 0-63, then 64-127; with the PV-split knob the MMA warp
+                // starts O += P V on the first half while the second is computed).
                 const float2 sl2v = make_float2(sl2, sl2), nmu = make_float2(-mu, -mu);
                 float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f)};
@@ -589,14 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c3 = 0; c3 < 32; ++c3) {
                         const int c2 = half * 32 + c3;
-                        const float2 x = ffma2(make_float2(sf[2 * c2], sf[2 * c2 + 1]), sl2v, nmu);
-                        float2 e;
-                        if (c2 % kPolyEvery == kPolyEvery - 1) {
-                            e = exp2_poly2(x);
-                        } else {
-                            e.x = fast_exp2(x.x);
-                            e.y = fast_exp2(x.y);
-                        }
+                        const float2 e = exp_pair(ffma2(make_float2(sf[2 * c2], sf[2 * c2 + 1]), sl2v, nmu), c2);
                         acc[c2 % 4] = fadd2(acc[c2 % 4], e);
                         p[c3] = pack_bf16x2(e.x, e.y);
                     }

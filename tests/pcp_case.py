@@ -52,10 +52,11 @@ class Case:
 
     ``kv_fp8=True`` runs the FP8 cache path; ``descales="layer"`` uses the layer
     scales broadcast to (num_reqs, Hkv), ``descales="varied"`` a seeded
-    different descale per (request, kv head)."""
+    different descale per (request, kv head). ``inputs_hook(case)`` may modify
+    ``case.q``, ``case.kfull``, ``case.vfull`` before anything is written."""
 
     def __init__(self, spec: W.WorkloadSpec, flags: int = 0, device: str = "cuda", kv_fp8: bool = False,
-                 descales: str = "layer"):
+                 descales: str = "layer", inputs_hook=None):
         P = _pcp()
         self.spec, self.flags, self.device, self.kv_fp8 = spec, flags, device, kv_fp8
         self.bt, self.num_blocks = W.block_tables(spec)
@@ -65,6 +66,8 @@ class Case:
             self.kfull.append(k)
             self.vfull.append(v)
         self.q = W.packed_new_tokens(spec, W.KIND_Q)
+        if inputs_hook is not None:  # a test may reshape the seeded inputs (same tensors for both sides)
+            inputs_hook(self)
         P_ = spec.num_computed
         self.k_new = torch.cat([k[p:] for k, p in zip(self.kfull, P_)], 0)
         self.v_new = torch.cat([v[p:] for v, p in zip(self.vfull, P_)], 0)
