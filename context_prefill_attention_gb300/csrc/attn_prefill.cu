@@ -56,7 +56,7 @@ constexpr int kConvThreads = 64;
 #define PCP_PREFILL_K_STAGES 2
 #endif
 #ifndef PCP_PREFILL_V_STAGES
-#define PCP_PREFILL_V_STAGES 2
+#define PCP_PREFILL_V_STAGES 3
 #endif
 #ifndef PCP_POLY_EXP_EVERY
 // Off: on GB300 the exponential unit keeps up with the tensor cores, and the
@@ -404,36 +404,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (!ok && lane == 0) report_status(a.status, PCP_ERR_TIMEOUT);
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarp && lane == 0) {
         // ------------------------------------------------------------ MMA issuer
+        // Lane 0 alone runs this role. Measured on GB300: the same issue pattern
+        // run warp-wide (every lane waiting, a vote and a reconvergence around
+        // each batch issued by one lane) holds the tensor pipe to ~89 cycles per
+        // 128x128x16 MMA against ~70 from a single thread. The other lanes only
+        // take part in the TMEM allocation and release.
         uint32_t kt = 0, vt = 0, c = 0;
         uint32_t pph[2] = {0, 0}, nslot_items[2] = {0, 0};
         bool ok = true;
-        const bool leader = lane == 0;
         for (int32_t round = 0; ok; ++round) {
             const int32_t idx = item_of_round(round);
             if (idx >= total_items) break;
             const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, bs);
             const int n = it.n_tiles;
             if (n == 0) continue;
-            if (!(ok = mbar_wait_warp(q_full, c & 1, abort_flag))) break;
+            if (!(ok = mbar_wait(q_full, c & 1, abort_flag))) break;
             int ks = kt % kNK;
-            if (!(ok = mbar_wait_warp(k_full(ks), (kt / kNK) & 1, abort_flag))) break;
+            if (!(ok = mbar_wait(k_full(ks), (kt / kNK) & 1, abort_flag))) break;
             tc_fence_after();
-            if (leader) {
-                for (int g = 0; g < it.nslots; ++g) {
-                    issue_qk<D>(tmem + C::tmem_s(g), sbase + C::kQ + g * C::kTileBytes,
-                                sbase + C::kK + ks * C::kTileBytes);
-                    mma_commit(s_full(g));
-                }
-                mma_commit(k_empty(ks));
-                if (n == 1) mma_commit(q_empty);
+            for (int g = 0; g < it.nslots; ++g) {
+                issue_qk<D>(tmem + C::tmem_s(g), sbase + C::kQ + g * C::kTileBytes,
+                            sbase + C::kK + ks * C::kTileBytes);
+                mma_commit(s_full(g));
             }
-            __syncwarp();
+            mma_commit(k_empty(ks));
+            if (n == 1) mma_commit(q_empty);
             ++kt;
             for (int j = 0; j < n && ok; ++j) {
                 const int vs = vt % kNV;
-                if (!(ok = mbar_wait_warp(v_full(vs), (vt / kNV) & 1, abort_flag))) break;
+                if (!(ok = mbar_wait(v_full(vs), (vt / kNV) & 1, abort_flag))) break;
                 if (j == n - 1 && (it.k_end % bs) != 0) {
                     // Keys at or past k_end inside the last loaded page may never have been
                     // written: zero their V rows so that P = 0 cannot meet a NaN.
@@ -442,53 +443,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int nbytes = (r1 - rel) * 128;
                     for (int h = 0; h < C::kHalves; ++h) {
                         uint8_t* base = smem + C::kV + vs * C::kTileBytes + h * C::kHalfBytes + rel * 128;
-                        for (int off = lane * 16; off < nbytes; off += 32 * 16)
+                        for (int off = 0; off < nbytes; off += 16)
                             *reinterpret_cast<uint4*>(base + off) = make_uint4(0, 0, 0, 0);
                     }
                     fence_proxy_async_smem();
-                    __syncwarp();
                 }
                 for (int g = 0; g < it.nslots && ok; ++g) {
-                    // O += P V in two halves: keys 0-63 as soon as the softmax has written
-                    // that half of P, keys 64-127 when all of P is there
+                    // O += P V (with the PV-split knob: keys 0-63 as soon as the softmax has
+                    // written that half of P, keys 64-127 when all of P is there)
                     const int ks_mid = kPvSplit ? kBlockN / 32 : 0;
-                    if (!(ok = mbar_wait_warp(kPvSplit ? p_half(g) : p_full(g), pph[g], abort_flag))) break;
+                    if (!(ok = mbar_wait(kPvSplit ? p_half(g) : p_full(g), pph[g], abort_flag))) break;
                     if (j == 0 && nslot_items[g] > 0) {
-                        if (!(ok = mbar_wait_warp(o_free(g), (nslot_items[g] - 1) & 1, abort_flag))) break;
+                        if (!(ok = mbar_wait(o_free(g), (nslot_items[g] - 1) & 1, abort_flag))) break;
                     }
                     tc_fence_after();
-                    if (leader && ks_mid > 0)
+                    if (ks_mid > 0)
                         issue_pv<D>(tmem + C::tmem_o(g), tmem + C::tmem_s(g),
                                     sbase + C::kV + vs * C::kTileBytes, j > 0, 0, ks_mid);
                     if (kPvSplit) {
-                        if (!(ok = mbar_wait_warp(p_full(g), pph[g], abort_flag))) break;
+                        if (!(ok = mbar_wait(p_full(g), pph[g], abort_flag))) break;
                         tc_fence_after();
                     }
                     pph[g] ^= 1;
-                    if (leader)
-                        issue_pv<D>(tmem + C::tmem_o(g), tmem + C::tmem_s(g),
-                                    sbase + C::kV + vs * C::kTileBytes, j > 0, ks_mid, kBlockN / 16);
-                    if (g == it.nslots - 1 && leader) mma_commit(v_empty(vs));
+                    issue_pv<D>(tmem + C::tmem_o(g), tmem + C::tmem_s(g),
+                                sbase + C::kV + vs * C::kTileBytes, j > 0, ks_mid, kBlockN / 16);
+                    if (g == it.nslots - 1) mma_commit(v_empty(vs));
                     if (j + 1 < n) {
                         if (g == 0) {
                             ks = kt % kNK;
-                            if (!(ok = mbar_wait_warp(k_full(ks), (kt / kNK) & 1, abort_flag))) break;
+                            if (!(ok = mbar_wait(k_full(ks), (kt / kNK) & 1, abort_flag))) break;
                             tc_fence_after();
                         }
-                        if (leader) {
-                            issue_qk<D>(tmem + C::tmem_s(g), sbase + C::kQ + g * C::kTileBytes,
-                                        sbase + C::kK + ks * C::kTileBytes);
-                            mma_commit(s_full(g));
-                            if (g == it.nslots - 1) {
-                                mma_commit(k_empty(ks));
-                                if (j + 1 == n - 1) mma_commit(q_empty);
-                            }
+                        issue_qk<D>(tmem + C::tmem_s(g), sbase + C::kQ + g * C::kTileBytes,
+                                    sbase + C::kK + ks * C::kTileBytes);
+                        mma_commit(s_full(g));
+                        if (g == it.nslots - 1) {
+                            mma_commit(k_empty(ks));
+                            if (j + 1 == n - 1) mma_commit(q_empty);
+                            ++kt;
                         }
-                        if (g == it.nslots - 1) ++kt;
-                    } else if (leader) {
+                    } else {
                         mma_commit(o_done(g));
                     }
-                    __syncwarp();
                 }
                 ++vt;
             }
@@ -716,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) report_status(a.status, PCP_ERR_TIMEOUT);
     }
 
-    __syncwarp();  // the producer's lane 0 worked alone: reconverge before the CTA barrier
+    __syncwarp();  // lane 0 of the producer and of the MMA warp worked alone: reconverge first
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
