@@ -63,13 +63,6 @@ constexpr int kConvThreads = 64;
 // polynomial only costs issue slots (measured: 1 pair in 4 -> 9% slower).
 #define PCP_POLY_EXP_EVERY 1000000
 #endif
-#ifndef PCP_PV_SPLIT
-#define PCP_PV_SPLIT 0
-#endif
-// 1: O += P V is issued in two halves, the first as soon as the softmax has
-// written keys 0-63 of P; 0: one issue after all of P is written. Measured on
-// GB300: the split is 4-5 % slower (an extra handshake per tile), so it is off.
-constexpr bool kPvSplit = PCP_PV_SPLIT != 0;
 #ifndef PCP_PREFILL_MAXFREE
 #define PCP_PREFILL_MAXFREE 1
 #endif
@@ -112,7 +105,7 @@ struct Cfg {
     __host__ __device__ static constexpr int code_v(int s) {
         return kInPlace ? kV + s * kTileBytes + kHalfBytes : kCV + s * kCodeBytes;
     }
-    static constexpr int kNumBars = 2 + 2 * kNK + 2 * kNV + 8 + 2 + (F8 ? kNK + kNV : 0);
+    static constexpr int kNumBars = 2 + 2 * kNK + 2 * kNV + 8 + kNK + kNV;
     static constexpr int kMisc = kBar + kNumBars * 8;      // tmem address, abort flag, item ring
     static constexpr int kSmem = kMisc + 16 + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 512;
@@ -240,10 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto p_full = [&](int g) { return bx + 16 + 8 * g; };
     auto o_done = [&](int g) { return bx + 32 + 8 * g; };
     auto o_free = [&](int g) { return bx + 48 + 8 * g; };
-    auto p_half = [&](int g) { return bx + 64 + 8 * g; };  // first 64 keys of P ready
     // FP8: the codes of K / V stage s have landed
-    auto kc_full = [&](int s) { return bx + 80 + 8 * s; };
-    auto vc_full = [&](int s) { return bx + 80 + 8 * (kNK + s); };
+    auto kc_full = [&](int s) { return bx + 64 + 8 * s; };
+    auto vc_full = [&](int s) { return bx + 64 + 8 * (kNK + s); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
 
@@ -269,7 +261,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(p_full(g), 128);
             mbar_init(o_done(g), 1);
             mbar_init(o_free(g), 128);
-            mbar_init(p_half(g), 128);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -295,13 +286,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         return r * (int32_t)gridDim.x + ((r & 1) ? (int32_t)(gridDim.x - 1 - blockIdx.x) : (int32_t)blockIdx.x);
     };
     // Registers: the launch gives 168 per thread (384 threads); the producer /
-    // MMA warpgroup gives back to 120 so the softmax warpgroups can hold a full
-    // 128-column score row (192): 128 x 120 + 256 x 192 = 384 x 168. setmaxnreg
-    // sits at the top of each warpgroup's branch so that each role's code is
-    // compiled against its own register limit.
+    // MMA / converter warpgroup gives back to 104 so the softmax warpgroups can
+    // hold a full 128-column score row and the 64 packed P words of the max-free
+    // path (200): 128 x 104 + 256 x 200 = 384 x 168. setmaxnreg sits at the top
+    // of each warpgroup's branch so that each role's code is compiled against its
+    // own register limit.
 
     if (warp >= 8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 120;");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;");
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         // The whole warp runs the loop: lane p owns page p of every key tile. It
@@ -406,11 +398,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok && lane == 0) report_status(a.status, PCP_ERR_TIMEOUT);
     } else if (warp == kMmaWarp && lane == 0) {
         // ------------------------------------------------------------ MMA issuer
-        // Lane 0 alone runs this role. Measured on GB300: the same issue pattern
-        // run warp-wide (every lane waiting, a vote and a reconvergence around
-        // each batch issued by one lane) holds the tensor pipe to ~89 cycles per
-        // 128x128x16 MMA against ~70 from a single thread. The other lanes only
-        // take part in the TMEM allocation and release.
+        // Lane 0 alone runs this role, in a fixed order that staggers the two
+        // heads (S0 S1 | PV0 S0' PV1 S1' | ...) so each softmax warpgroup works
+        // while the other head's MMAs run. Measured on GB300: the same pattern run
+        // warp-wide (every lane waiting, a vote and a reconvergence around each
+        // batch) holds the tensor pipe to ~89 cycles per 128x128x16 MMA against
+        // ~70 from a single thread; one issuer thread per head (independent
+        // order) ran 11% slower end to end, the heads' softmaxes falling into
+        // step. The other lanes only take part in the TMEM allocation and release.
         uint32_t kt = 0, vt = 0, c = 0;
         uint32_t pph[2] = {0, 0}, nslot_items[2] = {0, 0};
         bool ok = true;
@@ -449,24 +444,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                 }
                 for (int g = 0; g < it.nslots && ok; ++g) {
-                    // O += P V (with the PV-split knob: keys 0-63 as soon as the softmax has
-                    // written that half of P, keys 64-127 when all of P is there)
-                    const int ks_mid = kPvSplit ? kBlockN / 32 : 0;
-                    if (!(ok = mbar_wait(kPvSplit ? p_half(g) : p_full(g), pph[g], abort_flag))) break;
+                    // O += P V once the softmax has written P
+                    if (!(ok = mbar_wait(p_full(g), pph[g], abort_flag))) break;
                     if (j == 0 && nslot_items[g] > 0) {
                         if (!(ok = mbar_wait(o_free(g), (nslot_items[g] - 1) & 1, abort_flag))) break;
                     }
                     tc_fence_after();
-                    if (ks_mid > 0)
-                        issue_pv<D>(tmem + C::tmem_o(g), tmem + C::tmem_s(g),
-                                    sbase + C::kV + vs * C::kTileBytes, j > 0, 0, ks_mid);
-                    if (kPvSplit) {
-                        if (!(ok = mbar_wait(p_full(g), pph[g], abort_flag))) break;
-                        tc_fence_after();
-                    }
                     pph[g] ^= 1;
                     issue_pv<D>(tmem + C::tmem_o(g), tmem + C::tmem_s(g),
-                                sbase + C::kV + vs * C::kTileBytes, j > 0, ks_mid, kBlockN / 16);
+                                sbase + C::kV + vs * C::kTileBytes, j > 0, 0, kBlockN / 16);
                     if (g == it.nslots - 1) mma_commit(v_empty(vs));
                     if (j + 1 < n) {
                         if (g == 0) {
@@ -494,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) report_status(a.status, PCP_ERR_TIMEOUT);
     }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 192;");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 200;");
         // ------------------------------------------------------------ softmax
         const int g = warp / 4;                 // head slot of this warpgroup
         const int r = threadIdx.x % 128;        // query row within the tile = TMEM lane
@@ -573,7 +559,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
                         tmem_wait_st();
                         tc_fence_before();
-                        if (kPvSplit) mbar_arrive(p_half(g));
                         mbar_arrive(p_full(g));
                         l += ts;
                         exact = false;
@@ -625,9 +610,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 // Exact path: p = 2^(s * scale * log2 e - m) with m this row's lazily
-                // updated max, two lanes per instruction. P goes back to TMEM in two
-                // halves (keys 0-63, then 64-127; with the PV-split knob the MMA warp
-                // starts O += P V on the first half while the second is computed).
+                // updated max, two lanes per instruction; P goes back to TMEM in two
+                // halves (keys 0-63, then 64-127).
                 const float2 sl2v = make_float2(sl2, sl2), nmu = make_float2(-mu, -mu);
                 float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f)};
@@ -642,10 +626,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p[c3] = pack_bf16x2(e.x, e.y);
                     }
                     tmem_st32(t_s + 32 * half, p);
-                    if (kPvSplit || half == 1) {
+                    if (half == 1) {
                         tmem_wait_st();
                         tc_fence_before();
-                        mbar_arrive(half == 0 ? p_half(g) : p_full(g));
+                        mbar_arrive(p_full(g));
                     }
                 }
                 const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
