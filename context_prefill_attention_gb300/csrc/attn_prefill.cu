@@ -189,27 +189,28 @@ __device__ __forceinline__ void convert_codes(const uint8_t* codes, uint8_t* dst
     }
 }
 
-// S = Q_slot K^T over D (K-major A and B, 128-byte swizzle).
+// S = Q_slot K^T over D (K-major A and B, 128-byte swizzle). q_desc / k_desc are
+// the descriptors of the tiles' first k-step; a later k-step only moves the start
+// address (the descriptor's low 14 bits, in 16-byte units), so each MMA costs one
+// add of a constant (the issuing thread's instruction count per MMA is on the
+// critical path of the tensor pipe).
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint64_t q_desc, uint64_t k_desc) {
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t off = (ks / 4) * Cfg<D>::kHalfBytes + (ks % 4) * 32;
-        const uint64_t a = sdesc_sw128(q_smem + off, 16, 1024);
-        const uint64_t b = sdesc_sw128(k_smem + off, 16, 1024);
-        mma_ss(tmem_s, a, b, Cfg<D>::kIdescS, ks > 0 ? 1u : 0u);
+        const uint32_t off = ((ks / 4) * Cfg<D>::kHalfBytes + (ks % 4) * 32) >> 4;
+        mma_ss(tmem_s, q_desc + off, k_desc + off, Cfg<D>::kIdescS, ks > 0 ? 1u : 0u);
     }
 }
 
-// O (+)= P V: P from TMEM (bf16 pairs in the S columns), V MN-major in shared memory.
+// O (+)= P V: P from TMEM (bf16 pairs in the S columns), V MN-major in shared
+// memory (v_desc: the descriptor of the tile's first 16 keys).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_smem,
-                                         bool accumulate, int ks_begin, int ks_end) {
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc, bool accumulate) {
 #pragma unroll
-    for (int ks = ks_begin; ks < ks_end; ++ks) {
-        const uint64_t b = sdesc_sw128(v_smem + ks * 2048, Cfg<D>::kHalfBytes, 1024);
-        mma_ts(tmem_o, tmem_p + ks * 8, b, Cfg<D>::kIdescO, (accumulate || ks > 0) ? 1u : 0u);
-    }
+    for (int ks = 0; ks < kBlockN / 16; ++ks)
+        mma_ts(tmem_o, tmem_p + ks * 8, v_desc + (uint32_t)(ks * 2048 >> 4), Cfg<D>::kIdescO,
+               (accumulate || ks > 0) ? 1u : 0u);
 }
 
 template <int D, bool F8>
@@ -409,6 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t kt = 0, vt = 0, c = 0;
         uint32_t pph[2] = {0, 0}, nslot_items[2] = {0, 0};
         bool ok = true;
+        // shared-memory descriptors of the first k-step of every Q, K and V tile
+        auto q_desc = [&](int g) { return sdesc_sw128(sbase + C::kQ + g * C::kTileBytes, 16, 1024); };
+        auto k_desc = [&](int s2) { return sdesc_sw128(sbase + C::kK + s2 * C::kTileBytes, 16, 1024); };
+        auto v_desc = [&](int s2) { return sdesc_sw128(sbase + C::kV + s2 * C::kTileBytes, C::kHalfBytes, 1024); };
+        const uint64_t qd0 = q_desc(0), qd1 = q_desc(1);
         for (int32_t round = 0; ok; ++round) {
             const int32_t idx = item_of_round(round);
             if (idx >= total_items) break;
@@ -420,8 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = mbar_wait(k_full(ks), (kt / kNK) & 1, abort_flag))) break;
             tc_fence_after();
             for (int g = 0; g < it.nslots; ++g) {
-                issue_qk<D>(tmem + C::tmem_s(g), sbase + C::kQ + g * C::kTileBytes,
-                            sbase + C::kK + ks * C::kTileBytes);
+                issue_qk<D>(tmem + C::tmem_s(g), g ? qd1 : qd0, k_desc(ks));
                 mma_commit(s_full(g));
             }
             mma_commit(k_empty(ks));
@@ -451,8 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     pph[g] ^= 1;
-                    issue_pv<D>(tmem + C::tmem_o(g), tmem + C::tmem_s(g),
-                                sbase + C::kV + vs * C::kTileBytes, j > 0, 0, kBlockN / 16);
+                    issue_pv<D>(tmem + C::tmem_o(g), tmem + C::tmem_s(g), v_desc(vs), j > 0);
                     if (g == it.nslots - 1) mma_commit(v_empty(vs));
                     if (j + 1 < n) {
                         if (g == 0) {
@@ -460,8 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!(ok = mbar_wait(k_full(ks), (kt / kNK) & 1, abort_flag))) break;
                             tc_fence_after();
                         }
-                        issue_qk<D>(tmem + C::tmem_s(g), sbase + C::kQ + g * C::kTileBytes,
-                                    sbase + C::kK + ks * C::kTileBytes);
+                        issue_qk<D>(tmem + C::tmem_s(g), g ? qd1 : qd0, k_desc(ks));
                         mma_commit(s_full(g));
                         if (g == it.nslots - 1) {
                             mma_commit(k_empty(ks));
