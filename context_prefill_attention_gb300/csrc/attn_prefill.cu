@@ -244,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = a.hq / a.hkv;
     const bool dual = (G % 2) == 0;
     const int slots_per_unit = dual ? a.hq / 2 : a.hq;
+    const int slots_per_item = dual ? 2 : 1;  // q heads per item (Item::nslots)
     const int32_t bs = a.block_size;
 
     if (threadIdx.x == 0) {
@@ -429,8 +430,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_qk<D>(tmem + C::tmem_s(g), g ? qd1 : qd0, k_desc(ks));
                 mma_commit(s_full(g));
             }
-            mma_commit(k_empty(ks));
-            if (n == 1) mma_commit(q_empty);
             ++kt;
             for (int j = 0; j < n && ok; ++j) {
                 const int vs = vt % kNV;
@@ -457,7 +456,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     pph[g] ^= 1;
                     issue_pv<D>(tmem + C::tmem_o(g), tmem + C::tmem_s(g), v_desc(vs), j > 0);
-                    if (g == it.nslots - 1) mma_commit(v_empty(vs));
                     if (j + 1 < n) {
                         if (g == 0) {
                             ks = kt % kNK;
@@ -466,11 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         issue_qk<D>(tmem + C::tmem_s(g), g ? qd1 : qd0, k_desc(ks));
                         mma_commit(s_full(g));
-                        if (g == it.nslots - 1) {
-                            mma_commit(k_empty(ks));
-                            if (j + 1 == n - 1) mma_commit(q_empty);
-                            ++kt;
-                        }
+                        if (g == it.nslots - 1) ++kt;
                     } else {
                         mma_commit(o_done(g));
                     }
@@ -491,6 +485,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t t_s = tmem + lane_base + C::tmem_s(g);
         const uint32_t t_o = tmem + lane_base + C::tmem_o(g);
         uint32_t sph = 0, oph = 0;
+        // The warpgroup of the last head slot releases the shared stages: S of tile j
+        // complete means every MMA issued before it is complete (K(j), V(j - 1) and,
+        // on the last tile, Q are free); O done frees the item's last V. Its thread 0
+        // arrives, so that the MMA issuer spends no commits on them.
+        const bool releaser = g == slots_per_item - 1;
+        uint32_t rel_k = 0, rel_v = 0;
         bool ok = true;
         for (int32_t round = 0; ok; ++round) {
             const int32_t idx = item_of_round(round);
@@ -510,6 +510,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < n && ok; ++j) {
                 if (!(ok = mbar_wait_warp(s_full(g), sph, abort_flag))) break;
                 sph ^= 1;
+                if (releaser) {
+                    if (r == 0) {
+                        mbar_arrive(k_empty(rel_k % kNK));
+                        if (j == n - 1) mbar_arrive(q_empty);
+                        if (j > 0) mbar_arrive(v_empty(rel_v % kNV));
+                    }
+                    ++rel_k;
+                    if (j > 0) ++rel_v;
+                }
                 tc_fence_after();
                 uint32_t s[128];
                 float* sf = reinterpret_cast<float*>(s);
@@ -648,6 +657,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (n > 0) {
                 if (!(ok = mbar_wait_warp(o_done(g), oph, abort_flag))) break;
                 oph ^= 1;
+                if (releaser) {
+                    if (r == 0) mbar_arrive(v_empty(rel_v % kNV));
+                    ++rel_v;
+                }
                 tc_fence_after();
             }
             const size_t orow = ((size_t)tok * a.hq + h) * D;
