@@ -8,8 +8,9 @@
 //  * split-KV: CTA (split, kv head, row) streams keys [512 s, 512 (s+1)) of
 //    one kv head for all G q heads of its group;
 //  * a producer warp reads the chunk's block-table entries once, then streams
-//    32-key slabs of K and V into a 4-stage shared-memory ring with TMA (the
-//    same swizzled 64-dim boxes as the prefill path, completion on mbarriers);
+//    32-key slabs of K and V into a 4-stage shared-memory ring with TMA: one
+//    unswizzled box per page (the head's D contiguous elements of each of its
+//    rows), completion on mbarriers;
 //  * four consumer warps share each slab, a half-warp per group of keys: each
 //    lane one 128-bit (D = 128) or 64-bit (D = 64) shared load per K and V row,
 //    packed fp32 dot products, a butterfly reduce-scatter over the 16 lanes so
@@ -17,10 +18,10 @@
 //    fp32 online softmax per q head with lazy rescaling;
 //  * partial (out, lse) per split in the workspace, merged by log-sum-exp in
 //    decode_merge_kernel;
-//  * FP8 (e4m3) cache: the slabs hold the codes (rows of D bytes, unswizzled),
-//    each lane converts its 8 (D = 128) or 4 (D = 64) codes to fp32 after the
-//    shared load; the K descale folds into the query scale, the V descale into
-//    the split's output.
+//  * FP8 (e4m3) cache: the slabs hold the codes (rows of D bytes), each lane
+//    converts its 8 (D = 128) or 4 (D = 64) codes to fp32 after the shared
+//    load; the K descale folds into the query scale, the V descale into the
+//    split's output.
 // Also here: the LSE merge of the two prefill partials when the context and
 // new-token parts are computed separately.
 #include <cuda.h>
@@ -49,9 +50,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D, int GMAX, bool F8 = false>
 struct DecCfg {
-    static constexpr int kHalfBytes = kSlab * 128;                  // kSlab rows x 64 dims (bf16)
-    // K (or V) of one slab: bf16 in D / 64 swizzled halves, or FP8 rows of D bytes
-    static constexpr int kSlabBytes = F8 ? kSlab * D : (D / 64) * kHalfBytes;
+    static constexpr int kRowBytes = F8 ? D : 2 * D;                // one key of one head
+    static constexpr int kSlabBytes = kSlab * kRowBytes;            // K (or V) of one slab
     static constexpr int kStageBytes = 2 * kSlabBytes;
     static constexpr int kBars = kStages * kStageBytes;
     static constexpr int kPages = kBars + 2 * kStages * 8;
@@ -59,12 +59,11 @@ struct DecCfg {
     static constexpr int kSmem = kComb + (2 * kConsumerWarps * GMAX + kConsumerWarps * GMAX * D) * 4 + 1024;
 };
 
-// VEC consecutive bf16 of one key row, read from a 128-byte-swizzled slab:
-// row kr (0..15) of the slab, first dim e0 (a multiple of VEC).
+// VEC consecutive elements (first dim e0) of row kr of a slab whose rows are
+// VEC * 16 elements (D), as fp32: bf16 widened by a shift, FP8 codes converted.
 template <int VEC, bool F8>
 __device__ __forceinline__ void load_row(const uint8_t* slab, int kr, int e0, float (&f)[VEC]) {
     if constexpr (F8) {
-        // FP8 slab: row kr is VEC * 16 contiguous codes
         const uint8_t* p = slab + kr * (VEC * 16) + e0;
         if constexpr (VEC == 8) {
             const uint2 u = *reinterpret_cast<const uint2*>(p);
@@ -82,25 +81,23 @@ __device__ __forceinline__ void load_row(const uint8_t* slab, int kr, int e0, fl
 #pragma unroll
             for (int i = 0; i < 4; ++i) f[i] = a[i];
         }
-        return;
-    }
-    const int b = e0 * 2;
-    const int half = b >> 7, bb = b & 127;
-    const uint8_t* p = slab + half * (kSlab * 128) + kr * 128 + ((((bb >> 4) ^ (kr & 7)) << 4) | (bb & 15));
-    if constexpr (VEC == 8) {
-        const uint4 u = *reinterpret_cast<const uint4*>(p);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            f[2 * i] = __uint_as_float(w[i] << 16);
-            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-        }
     } else {
-        const uint2 u = *reinterpret_cast<const uint2*>(p);
-        f[0] = __uint_as_float(u.x << 16);
-        f[1] = __uint_as_float(u.x & 0xFFFF0000u);
-        f[2] = __uint_as_float(u.y << 16);
-        f[3] = __uint_as_float(u.y & 0xFFFF0000u);
+        const uint8_t* p = slab + kr * (VEC * 32) + e0 * 2;
+        if constexpr (VEC == 8) {
+            const uint4 u = *reinterpret_cast<const uint4*>(p);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                f[2 * i] = __uint_as_float(w[i] << 16);
+                f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        } else {
+            const uint2 u = *reinterpret_cast<const uint2*>(p);
+            f[0] = __uint_as_float(u.x << 16);
+            f[1] = __uint_as_float(u.x & 0xFFFF0000u);
+            f[2] = __uint_as_float(u.y << 16);
+            f[3] = __uint_as_float(u.y & 0xFFFF0000u);
+        }
     }
 }
 
@@ -178,18 +175,8 @@ __global__ void __launch_bounds__(kDecThreads)
                         const int32_t base = page_row[key / bs - pg0];
                         if (base != oob) y = base + (key % bs);
                     }
-                    if constexpr (F8) {
-                        tma_load_3d(dst + b * box_rows * D, &tm_k, full_bar(st), 0, hk, y);
-                        tma_load_3d(dst + C::kSlabBytes + b * box_rows * D, &tm_v, full_bar(st), 0, hk, y);
-                    } else {
-#pragma unroll
-                        for (int h = 0; h < D / 64; ++h) {
-                            tma_load_3d(dst + h * C::kHalfBytes + b * box_rows * 128, &tm_k, full_bar(st), h * 64,
-                                        hk, y);
-                            tma_load_3d(dst + C::kSlabBytes + h * C::kHalfBytes + b * box_rows * 128, &tm_v,
-                                        full_bar(st), h * 64, hk, y);
-                        }
-                    }
+                    tma_load_3d(dst + b * box_rows * C::kRowBytes, &tm_k, full_bar(st), 0, hk, y);
+                    tma_load_3d(dst + C::kSlabBytes + b * box_rows * C::kRowBytes, &tm_v, full_bar(st), 0, hk, y);
                 }
             }
             if (!ok) report_status(a.status, PCP_ERR_TIMEOUT);
@@ -449,10 +436,9 @@ int launch_decode_dgf(const PrefillArgs& a, float* dec_out, float* dec_lse, int3
     const int box_rows = a.block_size < kSlab ? a.block_size : kSlab;
     const int64_t slots = a.num_blocks * a.block_size;
     CUtensorMap tk, tv;
-    const bool maps = F8 ? make_kv_code_map(&tk, a.key_cache, D, a.hkv, slots, box_rows) &&
-                               make_kv_code_map(&tv, a.value_cache, D, a.hkv, slots, box_rows)
-                         : make_kv_map(&tk, a.key_cache, D, a.hkv, slots, box_rows) &&
-                               make_kv_map(&tv, a.value_cache, D, a.hkv, slots, box_rows);
+    const int esize = F8 ? 1 : 2;
+    const bool maps = make_kv_row_map(&tk, a.key_cache, D, esize, a.hkv, slots, box_rows) &&
+                      make_kv_row_map(&tv, a.value_cache, D, esize, a.hkv, slots, box_rows);
     if (!maps) return PCP_ERR_CUDA;
     const int smem = DecCfg<D, GMAX, F8>::kSmem;
     cudaError_t e =

@@ -873,18 +873,19 @@ bool make_map(CUtensorMap* m, const void* base, int D, int64_t mid, int64_t oute
     return r == CUDA_SUCCESS;
 }
 
-// 3-D byte view [outer][mid][D] of an FP8 cache with a box of {D, 1, rows},
-// no swizzle (a box row is D contiguous bytes: 64 or 128).
-bool make_code_map(CUtensorMap* m, const void* base, int D, int64_t mid, int64_t outer, int rows) {
+// 3-D view [outer][mid][D] of a cache with elements of esize bytes (1: FP8 codes,
+// 2: bf16) and a box of {D, 1, rows}, no swizzle: a box row is one head's D
+// contiguous elements (64 to 256 bytes).
+bool make_row_map(CUtensorMap* m, const void* base, int D, int esize, int64_t mid, int64_t outer, int rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)mid, (cuuint64_t)outer};
-    cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)(D * mid)};
+    cuuint64_t strides[2] = {(cuuint64_t)D * esize, (cuuint64_t)(D * esize * mid)};
     cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)rows};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUtensorMapDataType dt = esize == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -892,8 +893,8 @@ template <int D, bool F8>
 int launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
     CUtensorMap tq, tk, tv;
     const int64_t slots = a.num_blocks * a.block_size;
-    const bool maps = F8 ? make_code_map(&tk, a.key_cache, D, a.hkv, slots, a.block_size) &&
-                               make_code_map(&tv, a.value_cache, D, a.hkv, slots, a.block_size)
+    const bool maps = F8 ? make_row_map(&tk, a.key_cache, D, 1, a.hkv, slots, a.block_size) &&
+                               make_row_map(&tv, a.value_cache, D, 1, a.hkv, slots, a.block_size)
                          : make_map(&tk, a.key_cache, D, a.hkv, slots, a.block_size) &&
                                make_map(&tv, a.value_cache, D, a.hkv, slots, a.block_size);
     if (!maps || !make_map(&tq, a.q, D, a.hq, a.total_q, kBlockM)) return PCP_ERR_CUDA;
@@ -929,8 +930,8 @@ bool make_kv_map(CUtensorMap* m, const void* base, int D, int64_t mid, int64_t o
     return make_map(m, base, D, mid, outer, rows);
 }
 
-bool make_kv_code_map(CUtensorMap* m, const void* base, int D, int64_t mid, int64_t outer, int rows) {
-    return make_code_map(m, base, D, mid, outer, rows);
+bool make_kv_row_map(CUtensorMap* m, const void* base, int D, int esize, int64_t mid, int64_t outer, int rows) {
+    return make_row_map(m, base, D, esize, mid, outer, rows);
 }
 
 }  // namespace pcp
