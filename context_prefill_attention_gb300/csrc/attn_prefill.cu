@@ -237,6 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // FP8: the codes of K / V stage s have landed
     auto kc_full = [&](int s) { return bx + 64 + 8 * s; };
     auto vc_full = [&](int s) { return bx + 64 + 8 * (kNK + s); };
+    // bf16: K(j) and V(j) land together on v_full(stage of V(j)), so the MMA
+    // issuer reads one barrier per tile for both (every barrier read by the issuer
+    // costs tensor-pipe time); FP8: the converters fill k_full and v_full apart
+    constexpr bool kMerged = !F8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
 
@@ -340,29 +344,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane < pages)
                         tma_load_3d(sbase + C::code_k(ks) + lane * bs * D, &tm_k, kc_full(ks), 0, it.hk, y);
                 } else {
-                    if (lane == 0) mbar_arrive_expect_tx(k_full(ks), C::kTileBytes);
+                    // K(j) and V(j) on one barrier: wait for both stages first
+                    const int vs = vt % kNV;
+                    if (!(ok = mbar_wait_warp(v_empty(vs), ((vt / kNV) & 1) ^ 1, abort_flag))) break;
+                    if (lane == 0) mbar_arrive_expect_tx(v_full(vs), 2 * C::kTileBytes);
                     __syncwarp();
                     if (lane < pages)
                         for (int h = 0; h < C::kHalves; ++h)
                             tma_load_3d(sbase + C::kK + ks * C::kTileBytes + h * C::kHalfBytes + lane * bs * 128,
-                                        &tm_k, k_full(ks), h * 64, it.hk, y);
+                                        &tm_k, v_full(vs), h * 64, it.hk, y);
                 }
                 ++kt;
                 const int vs = vt % kNV;
-                if (!(ok = mbar_wait_warp(v_empty(vs), ((vt / kNV) & 1) ^ 1, abort_flag))) break;
-                if constexpr (F8) {
-                    if (lane == 0) mbar_arrive_expect_tx(vc_full(vs), C::kCodeBytes);
-                    __syncwarp();
-                    if (lane < pages)
-                        tma_load_3d(sbase + C::code_v(vs) + lane * bs * D, &tm_v, vc_full(vs), 0, it.hk, y);
-                } else {
-                    if (lane == 0) mbar_arrive_expect_tx(v_full(vs), C::kTileBytes);
-                    __syncwarp();
+                if (!F8) {
                     if (lane < pages)
                         for (int h = 0; h < C::kHalves; ++h)
                             tma_load_3d(sbase + C::kV + vs * C::kTileBytes + h * C::kHalfBytes + lane * bs * 128,
                                         &tm_v, v_full(vs), h * 64, it.hk, y);
+                    ++vt;
+                    continue;
                 }
+                if (!(ok = mbar_wait_warp(v_empty(vs), ((vt / kNV) & 1) ^ 1, abort_flag))) break;
+                if (lane == 0) mbar_arrive_expect_tx(vc_full(vs), C::kCodeBytes);
+                __syncwarp();
+                if (lane < pages)
+                    tma_load_3d(sbase + C::code_v(vs) + lane * bs * D, &tm_v, vc_full(vs), 0, it.hk, y);
                 ++vt;
             }
             ++c;
@@ -424,7 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (n == 0) continue;
             if (!(ok = mbar_wait(q_full, c & 1, abort_flag))) break;
             int ks = kt % kNK;
-            if (!(ok = mbar_wait(k_full(ks), (kt / kNK) & 1, abort_flag))) break;
+            // K(0) (bf16: with V(0))
+            if (!(ok = kMerged ? mbar_wait(v_full(vt % kNV), (vt / kNV) & 1, abort_flag)
+                               : mbar_wait(k_full(ks), (kt / kNK) & 1, abort_flag)))
+                break;
             tc_fence_after();
             for (int g = 0; g < it.nslots; ++g) {
                 issue_qk<D>(tmem + C::tmem_s(g), g ? qd1 : qd0, k_desc(ks));
@@ -433,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++kt;
             for (int j = 0; j < n && ok; ++j) {
                 const int vs = vt % kNV;
-                if (!(ok = mbar_wait(v_full(vs), (vt / kNV) & 1, abort_flag))) break;
+                if (!kMerged && !(ok = mbar_wait(v_full(vs), (vt / kNV) & 1, abort_flag))) break;
                 if (j == n - 1 && (it.k_end % bs) != 0) {
                     // Keys at or past k_end inside the last loaded page may never have been
                     // written: zero their V rows so that P = 0 cannot meet a NaN.
@@ -458,8 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     issue_pv<D>(tmem + C::tmem_o(g), tmem + C::tmem_s(g), v_desc(vs), j > 0);
                     if (j + 1 < n) {
                         if (g == 0) {
+                            // K(j + 1) (bf16: with V(j + 1))
                             ks = kt % kNK;
-                            if (!(ok = mbar_wait(k_full(ks), (kt / kNK) & 1, abort_flag))) break;
+                            if (!(ok = kMerged ? mbar_wait(v_full((vt + 1) % kNV), ((vt + 1) / kNV) & 1, abort_flag)
+                                               : mbar_wait(k_full(ks), (kt / kNK) & 1, abort_flag)))
+                                break;
                             tc_fence_after();
                         }
                         issue_qk<D>(tmem + C::tmem_s(g), g ? qd1 : qd0, k_desc(ks));
