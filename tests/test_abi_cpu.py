@@ -163,3 +163,39 @@ def test_cache_write_and_merge_validate_before_launch(P):
     assert lib.pcp_lse_merge(V(FAKE + 4), V(FAKE), V(FAKE), V(FAKE + 512), V(FAKE), V(FAKE + 1024), 4, 2, 128,
                              None) == P.PCP_ERR_ALIGN
     assert lib.pcp_status_string(P.PCP_ERR_TIMEOUT) == b"device wait timed out"
+
+
+def _attn_fp8(lib, kd=FAKE, vd=FAKE, **kw):
+    args = dict(q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, nreq=1, mb=4, nb=64, bs=16, rows=FAKE, nrows=2, T=100,
+                hq=8, hkv=2, d=128, scale=0.1, out=FAKE, lse=FAKE, ws=FAKE, wsb=1 << 30, flags=0, status=None)
+    args.update(kw)
+    P_ = ctypes.c_void_p
+    return lib.pcp_attn_varlen_fp8kv(P_(args["q"]), P_(args["kc"]), P_(args["vc"]), P_(kd), P_(vd), P_(args["bt"]),
+                                     args["nreq"], args["mb"], args["nb"], args["bs"], P_(args["rows"]), args["nrows"],
+                                     args["T"], args["hq"], args["hkv"], args["d"], args["scale"], P_(args["out"]),
+                                     P_(args["lse"]), P_(args["ws"]), args["wsb"], args["flags"], args["status"],
+                                     None)
+
+
+def test_fp8_entry_points_validate_before_launch(P):
+    """Every call below fails a host check (or has nothing to do), so nothing
+    is launched on a fake pointer."""
+    lib = P.load()
+    V = ctypes.c_void_p
+    assert _attn_fp8(lib, kd=None) == P.PCP_ERR_ARG
+    assert _attn_fp8(lib, vd=None) == P.PCP_ERR_ARG
+    assert _attn_fp8(lib, kd=FAKE + 2) == P.PCP_ERR_ALIGN
+    assert _attn_fp8(lib, vd=FAKE + 1) == P.PCP_ERR_ALIGN
+    assert _attn_fp8(lib, d=96) == P.PCP_ERR_UNSUPPORTED
+    assert _attn_fp8(lib, flags=8) == P.PCP_ERR_ARG
+    assert _attn_fp8(lib, wsb=100) == P.PCP_ERR_WORKSPACE
+    assert _attn_fp8(lib, nrows=0, kd=None, vd=None) == P.PCP_OK
+    w = lib.pcp_kv_cache_write_fp8
+    args = (V(FAKE), V(FAKE), V(FAKE), 10, V(FAKE), V(FAKE), 8, 16, 2, 128)
+    for ks, vs in ((0.0, 1.0), (1.0, -2.0), (float("nan"), 1.0), (1.0, float("inf"))):
+        assert w(*args, ks, vs, None, None) == P.PCP_ERR_ARG
+    assert w(V(FAKE), V(FAKE), V(FAKE), 10, V(FAKE), V(FAKE), 8, 16, 1, 8, 1.0, 1.0, None, None) \
+        == P.PCP_ERR_UNSUPPORTED      # Hkv * D = 8 is not a multiple of 16
+    assert w(V(FAKE + 4), V(FAKE), V(FAKE), 10, V(FAKE), V(FAKE), 8, 16, 2, 128, 1.0, 1.0, None, None) \
+        == P.PCP_ERR_ALIGN
+    assert w(V(FAKE), V(FAKE), V(FAKE), 0, V(FAKE), V(FAKE), 8, 16, 2, 128, 1.0, 1.0, None, None) == P.PCP_OK
