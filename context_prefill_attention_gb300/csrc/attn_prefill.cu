@@ -938,10 +938,6 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     return PCP_ERR_UNSUPPORTED;
 }
 
-bool make_kv_map(CUtensorMap* m, const void* base, int D, int64_t mid, int64_t outer, int rows) {
-    return make_map(m, base, D, mid, outer, rows);
-}
-
 bool make_kv_row_map(CUtensorMap* m, const void* base, int D, int esize, int64_t mid, int64_t outer, int rows) {
     return make_row_map(m, base, D, esize, mid, outer, rows);
 }

@@ -89,9 +89,6 @@ struct PrefillArgs {
     const float* v_descale;
 };
 
-// TMA map of a bf16 tensor viewed as [outer][mid][D] with a box of 64 x 1 x rows
-// and 128-byte swizzle (Q: [T][Hq][D]; a paged cache: [blocks * bs][Hkv][D]).
-bool make_kv_map(CUtensorMap* m, const void* base, int D, int64_t mid, int64_t outer, int rows);
 // TMA map of a cache viewed as [outer][mid][D] elements of esize bytes (1: FP8
 // codes, 2: bf16) with a box of D x 1 x rows, no swizzle.
 bool make_kv_row_map(CUtensorMap* m, const void* base, int D, int esize, int64_t mid, int64_t outer, int rows);
