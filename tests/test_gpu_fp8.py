@@ -115,6 +115,8 @@ FP8_CASES = {
                       hq=8, hkv=4, d=128),
     "gqa16": dict(q=[140, 1], p=[9, 300], hq=16, hkv=1, d=128),
     "tile_exact": dict(q=[256, 128], p=[128, 0], hq=4, hkv=2, d=128),
+    "bs64": dict(q=[200, 1], p=[77, 300], hq=8, hkv=2, d=128, bs=64),
+    "gqa16_d64": dict(q=[140, 1, 1], p=[9, 300, 1200], hq=32, hkv=2, d=64),
 }
 
 
