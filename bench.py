@@ -83,13 +83,20 @@ def load_peaks():
 KERNEL_SOURCES = ("attn_prefill.cu", "pcp_device.cuh", "pcp_internal.h")
 
 
+def _code_only(text: str) -> str:
+    """Source text without // comments and blank lines (comment edits do not
+    change the compiled kernel)."""
+    lines = (line.split("//", 1)[0].rstrip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_source_hash() -> str:
-    """Hash of the prefill kernel's sources, to tell whether a stored ncu
-    traffic figure still describes the kernel being timed."""
+    """Hash of the prefill kernel's sources (code only), to tell whether a
+    stored ncu traffic figure still describes the kernel being timed."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "context_prefill_attention_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "context_prefill_attention_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

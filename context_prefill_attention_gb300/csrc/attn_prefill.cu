@@ -14,14 +14,20 @@
 //    pass, pair of q heads sharing one kv head), longest first;
 //  * warp 8 produces: TMA loads of the Q tiles and of K/V pages (one 3-D box
 //    of block_size keys x 64 dims per page and half head-dim) straight from the
-//    paged cache through the block table, 128-byte swizzled;
-//  * warp 9 issues tcgen05 MMAs from one lane: S = Q K^T into TMEM (A and B
-//    from shared memory), then O += P V with P read from TMEM (it overwrites S)
-//    and V from shared memory;
+//    paged cache through the block table, 128-byte swizzled; K(j) and V(j) land
+//    on one barrier;
+//  * lane 0 of warp 9 alone issues the tcgen05 MMAs: S = Q K^T into TMEM (A and
+//    B from shared memory), then O += P V with P read from TMEM (it overwrites
+//    S) and V from shared memory. The issuing thread is the throughput limit
+//    (each barrier read, commit or extra instruction there leaves the tensor
+//    pipe idle), so it reads one barrier per tile for K and V, builds its
+//    descriptors once per stage, and commits only S and O completions;
 //  * warps 0-3 and 4-7 are two softmax warpgroups, one per q head of the item,
-//    one thread per query row: they read S from TMEM, mask, keep the running
-//    max and sum, rescale O in TMEM when the max grows by more than 2^8, write
-//    P back as bf16, and finally normalise O and store out and lse;
+//    one thread per query row: they read S from TMEM, mask, exponentiate
+//    against the row's reference max without a max reduction first once it is
+//    known (falling back to an exact pass that rescales O in TMEM), write P
+//    back as bf16, and finally normalise O and store out and lse; the last
+//    head's warpgroup releases the K, V and Q stages;
 //  * the two heads' MMAs interleave (S0 S1 | PV0 S0' PV1 S1' | ...) so each
 //    warpgroup's softmax overlaps the other head's MMAs;
 //  * every mbarrier wait is bounded: a wait that runs out sets PCP_ERR_TIMEOUT
