@@ -117,7 +117,9 @@ def measured_traffic(workload_name: str):
 def plan_work(rows: np.ndarray, hq: int, hkv: int, d: int, kv_bytes: int = 2):
     """Algorithmic work of a plan: prefill FLOPs (4 D Hq per unmasked query-key
     pair), decode FLOPs and decode bytes (K and V of every visible key once per
-    kv head at kv_bytes per element, plus q, out and lse)."""
+    kv head at kv_bytes per element, plus q, out and lse), and the cache write's
+    bytes (every new token's bf16 K and V read, written at kv_bytes per element,
+    plus its 8-byte slot)."""
     r = rows.astype(np.int64)
     ql, end = r[:, 3], r[:, 5]
     dec = r[:, 7] == 1
@@ -125,8 +127,10 @@ def plan_work(rows: np.ndarray, hq: int, hkv: int, d: int, kv_bytes: int = 2):
     pre_pairs = int(pairs[~dec].sum())
     dec_keys = int(end[dec].sum())
     n_dec = int(dec.sum())
+    tokens = int(ql.sum())
     return dict(prefill_flop=4.0 * d * hq * pre_pairs, decode_flop=4.0 * d * hq * dec_keys,
                 decode_bytes=float(dec_keys * hkv * d * 2 * kv_bytes + n_dec * (hq * d * 2 * 2 + hq * 4)),
+                write_bytes=float(tokens * (hkv * d * 2 * (2 + kv_bytes) + 8)),
                 pairs=pre_pairs + dec_keys)
 
 
@@ -217,9 +221,16 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
 
-    def one_step():
+    def one_step(write_events=None):
+        # PcpStep.run's three steps, with optional events around the cache write
         step.build_plan(spec.query_len, spec.num_computed, bt)
-        return step.run(q, k, v, kc, vc, bt_dev, spec.scale, stream)
+        step.upload_plan(stream)
+        if write_events:
+            write_events[0].record(stream)
+        step.write_cache(k, v, kc, vc, stream)
+        if write_events:
+            write_events[1].record(stream)
+        return step.attend(q, kc, vc, bt_dev, spec.scale, stream)
 
     plan = step.build_plan(spec.query_len, spec.num_computed, bt)
     work = plan_work(plan["rows"], spec.num_q_heads, spec.num_kv_heads, spec.head_dim, 1 if kv_fp8 else 2)
@@ -229,7 +240,7 @@ def run_gpu(args):
     step.check_status()
 
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    ev = [[mk() for _ in range(6)] for _ in range(args.steps)]
+    ev = [[mk() for _ in range(8)] for _ in range(args.steps)]
     for e in ev:
         for x in e:
             x.record(stream)
@@ -241,7 +252,7 @@ def run_gpu(args):
             flush.fill_(i & 0xFF)  # L2 flush between timed steps, outside the timed window
             P.pcp_set_profile_events(ev[i][2], ev[i][3], ev[i][4], ev[i][5])
             ev[i][0].record(stream)
-            one_step()
+            one_step(ev[i][6:8])
             ev[i][1].record(stream)
         P.pcp_set_profile_events()
         torch.cuda.synchronize()
@@ -250,6 +261,7 @@ def run_gpu(args):
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     pre_ms = [e[2].elapsed_time(e[3]) for e in ev]
     dec_ms = [e[4].elapsed_time(e[5]) for e in ev]
+    write_ms = [e[6].elapsed_time(e[7]) for e in ev]
     total_ms = max_over_ranks(sum(step_ms), ws)
     ms = total_ms / args.steps
     step_flop = work["prefill_flop"] + work["decode_flop"]
@@ -282,6 +294,8 @@ def run_gpu(args):
     dec_avg = statistics.mean(dec_ms)
     achieved = work["prefill_flop"] / (pre_avg * 1e-3) / 1e12
     dec_gbs = work["decode_bytes"] / (dec_avg * 1e-3) / 1e9 if work["decode_bytes"] > 0 and dec_avg > 0 else None
+    write_avg = statistics.mean(write_ms)
+    write_gbs = work["write_bytes"] / (write_avg * 1e-3) / 1e9 if write_avg > 0 else None
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
@@ -297,6 +311,9 @@ def run_gpu(args):
         "decode": {"gbs": None if dec_gbs is None else round(dec_gbs, 1), "ms": round(dec_avg, 4),
                    "frac_hbm_peak": None if dec_gbs is None else round(dec_gbs / peaks["hbm"], 4),
                    "bytes": work["decode_bytes"]},
+        "cache_write": {"gbs": None if write_gbs is None else round(write_gbs, 1), "ms": round(write_avg, 4),
+                        "frac_hbm_peak": None if write_gbs is None else round(write_gbs / peaks["hbm"], 4),
+                        "bytes": work["write_bytes"]},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16"],
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
                      "traffic": measured_traffic(workload_name),

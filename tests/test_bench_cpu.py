@@ -48,6 +48,8 @@ def test_plan_work_matches_brute_force(case, kv_bytes):
     assert w["prefill_flop"] == 4.0 * D * hq * pre_pairs
     assert w["decode_flop"] == 4.0 * D * hq * dec_keys
     assert w["decode_bytes"] == dec_keys * hkv * D * kv_bytes * 2 + n_dec * (hq * D * 2 * 2 + hq * 4)
+    # cache write: each new token's K and V read as bf16 and written at kv_bytes, plus its slot
+    assert w["write_bytes"] == sum(case["q"]) * (2 * hkv * D * (2 + kv_bytes) + 8)
 
 
 def test_plan_work_on_the_bench_workload():
