@@ -182,6 +182,35 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU arm
 
+def merge_bytes(total_q: int, hq: int, d: int) -> float:
+    """Algorithmic bytes of one LSE merge of two fp32 partials [T, Hq, D] with
+    their lse [Hq, T] into bf16 out and fp32 lse."""
+    return float(total_q * hq * (2 * d * 4 + 2 * 4 + d * 2 + 4))
+
+
+def time_lse_merge(P, total_q: int, hq: int, d: int, device: str, stream, flush, iters: int = 5):
+    """pcp_lse_merge on seeded random partials of the step's [T, Hq, D] shape,
+    CUDA events on the launching stream, the L2 flushed before each launch;
+    returns the mean time in ms."""
+    g = torch.Generator(device=device).manual_seed(7)
+    oa, ob = (torch.randn((total_q, hq, d), generator=g, device=device) for _ in range(2))
+    la, lb = (torch.randn((hq, total_q), generator=g, device=device) for _ in range(2))
+    out = torch.empty((total_q, hq, d), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((hq, total_q), dtype=torch.float32, device=device)
+    for _ in range(3):
+        P.pcp_lse_merge(oa, la, ob, lb, out, lse, stream=stream)
+    times = []
+    for i in range(iters):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        P.pcp_lse_merge(oa, la, ob, lb, out, lse, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return statistics.mean(times)
+
+
 def setup(workload: int, device: str, flags: int, kv_fp8: bool = False):
     import context_prefill_attention_gb300 as P
     P.load()
@@ -289,6 +318,9 @@ def run_gpu(args):
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv)) + plan["rows"].nbytes + plan["slot_mapping"].nbytes
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
 
+    merge_ms = time_lse_merge(P, spec.total_q, spec.num_q_heads, spec.head_dim, device, stream, flush)
+    merge_b = merge_bytes(spec.total_q, spec.num_q_heads, spec.head_dim)
+
     peaks = load_peaks()
     pre_avg = statistics.mean(pre_ms)
     dec_avg = statistics.mean(dec_ms)
@@ -314,6 +346,9 @@ def run_gpu(args):
         "cache_write": {"gbs": None if write_gbs is None else round(write_gbs, 1), "ms": round(write_avg, 4),
                         "frac_hbm_peak": None if write_gbs is None else round(write_gbs / peaks["hbm"], 4),
                         "bytes": work["write_bytes"]},
+        "lse_merge": {"gbs": round(merge_b / (merge_ms * 1e-3) / 1e9, 1), "ms": round(merge_ms, 4),
+                      "frac_hbm_peak": round(merge_b / (merge_ms * 1e-3) / 1e9 / peaks["hbm"], 4),
+                      "bytes": merge_b, "timed": "pcp_lse_merge alone on the step's [T, Hq, D] partials"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16"],
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
                      "traffic": measured_traffic(workload_name),

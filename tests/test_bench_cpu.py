@@ -70,3 +70,10 @@ def test_stored_traffic_only_for_its_workload_and_sources(monkeypatch):
     # once the kernel sources change, the stored figure is no longer reported
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
     assert bench.measured_traffic(entry["workload"]) is None
+
+
+def test_merge_bytes_counts_both_partials_and_the_result():
+    T, hq, d = 37, 4, 128
+    read = 2 * (T * hq * d * 4) + 2 * (hq * T * 4)     # out_a, out_b fp32; lse_a, lse_b fp32
+    written = T * hq * d * 2 + hq * T * 4              # out bf16, lse fp32
+    assert bench.merge_bytes(T, hq, d) == read + written
