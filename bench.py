@@ -430,12 +430,13 @@ def run_reference(args):
     oracle.build()
     spec = W.workload_spec(args.workload)
     bt, _ = W.block_tables(spec)
+    kv_fp8 = args.kv_cache == "fp8"
     per_step = max(1.0, args.ref_seconds / (args.steps + args.warmup))
     for i in range(args.warmup):
-        _oracle_sample(spec, bt, per_step, spec.seed + 1000 + i)
+        _oracle_sample(spec, bt, per_step, spec.seed + 1000 + i, kv_fp8)
     tot_t, tot_f, desc = 0.0, 0.0, ""
     for i in range(args.steps):
-        dt, flop, desc = _oracle_sample(spec, bt, per_step, spec.seed + 2000 + i)
+        dt, flop, desc = _oracle_sample(spec, bt, per_step, spec.seed + 2000 + i, kv_fp8)
         tot_t += dt
         tot_f += flop
     value = tot_f / tot_t / 1e12
@@ -444,8 +445,9 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded torch.randn, bf16)",
-            "config": {"workload": spec.name, "total_q": spec.total_q, "num_q_heads": spec.num_q_heads,
-                       "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim},
+            "config": {"workload": spec.name + ("-fp8kv" if kv_fp8 else ""), "total_q": spec.total_q,
+                       "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
+                       "head_dim": spec.head_dim, "kv_cache": "fp8-e4m3" if kv_fp8 else "bf16"},
             "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": f"per step: {desc}"},
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -77,3 +77,36 @@ def test_merge_bytes_counts_both_partials_and_the_result():
     read = 2 * (T * hq * d * 4) + 2 * (hq * T * 4)     # out_a, out_b fp32; lse_a, lse_b fp32
     written = T * hq * d * 2 + hq * T * 4              # out bf16, lse fp32
     assert bench.merge_bytes(T, hq, d) == read + written
+
+
+def _run_bench(args, env_extra=None):
+    import subprocess
+    import sys
+    env = dict(os.environ, **(env_extra or {}))
+    return subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py")] + args, capture_output=True,
+                          text=True, timeout=300, env=env, cwd=bench.ROOT)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_reference_arm_prints_one_contract_line(kv):
+    """The reference arm (the oracle on the host cores) prints one JSON line with
+    the contract's keys, on the same metric and workload naming as the native arm."""
+    r = _run_bench(["--impl", "reference", "--workload", "1", "--steps", "1", "--warmup", "0",
+                    "--ref-seconds", "0.5", "--kv-cache", kv])
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["value"] > 0
+    assert line["config"]["workload"].endswith("-fp8kv") == (kv == "fp8")
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    r = _run_bench(["--impl", "reference", "--workload", "1", "--steps", "1", "--warmup", "0"],
+                   {"RANK": "1", "LOCAL_RANK": "1", "WORLD_SIZE": "2"})
+    assert r.returncode == 0 and not r.stdout.strip()
