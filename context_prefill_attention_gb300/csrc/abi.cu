@@ -18,6 +18,26 @@ thread_local cudaEvent_t g_profile[4] = {nullptr, nullptr, nullptr, nullptr};
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A device buffer as a byte range.
+struct Span {
+    const void* p;
+    size_t n;
+};
+
+// True when two byte ranges share a byte (an empty range shares none).
+inline bool overlap(Span a, Span b) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a.p), y = reinterpret_cast<uintptr_t>(b.p);
+    return a.n > 0 && b.n > 0 && x < y + b.n && y < x + a.n;
+}
+
+// True when an output range overlaps any of the ranges in ins[0, n) (kernels
+// read their inputs while other CTAs already write their outputs).
+inline bool overlaps_any(Span out, const Span* ins, int n) {
+    for (int i = 0; i < n; ++i)
+        if (overlap(out, ins[i])) return true;
+    return false;
+}
 }  // namespace
 
 void set_last_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
@@ -97,6 +117,12 @@ extern "C" int pcp_kv_cache_write(const void* k, const void* v, const int64_t* s
     if (!aligned16(k) || !aligned16(v) || !aligned16(key_cache) || !aligned16(value_cache) ||
         (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
         return PCP_ERR_ALIGN;
+    const size_t tok_bytes = (size_t)num_tokens * num_kv_heads * head_dim * 2;
+    const size_t cache_bytes = (size_t)num_blocks * block_size * num_kv_heads * head_dim * 2;
+    const Span ins[3] = {{k, tok_bytes}, {v, tok_bytes}, {slot_mapping, (size_t)num_tokens * 8}};
+    if (overlaps_any({key_cache, cache_bytes}, ins, 3) || overlaps_any({value_cache, cache_bytes}, ins, 3) ||
+        overlap({key_cache, cache_bytes}, {value_cache, cache_bytes}))
+        return PCP_ERR_ARG;
     const int32_t vec_per_tok = (int32_t)((int64_t)head_dim * 2 * num_kv_heads / 16);
     return launch_cache_write(k, v, slot_mapping, num_tokens, vec_per_tok, key_cache, value_cache,
                               num_blocks * block_size, status, reinterpret_cast<cudaStream_t>(stream));
@@ -116,6 +142,12 @@ extern "C" int pcp_kv_cache_write_fp8(const void* k, const void* v, const int64_
     if (!aligned16(k) || !aligned16(v) || !aligned16(key_cache) || !aligned16(value_cache) ||
         (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
         return PCP_ERR_ALIGN;
+    const size_t tok_bytes = (size_t)num_tokens * num_kv_heads * head_dim * 2;
+    const size_t cache_bytes = (size_t)num_blocks * block_size * num_kv_heads * head_dim;
+    const Span ins[3] = {{k, tok_bytes}, {v, tok_bytes}, {slot_mapping, (size_t)num_tokens * 8}};
+    if (overlaps_any({key_cache, cache_bytes}, ins, 3) || overlaps_any({value_cache, cache_bytes}, ins, 3) ||
+        overlap({key_cache, cache_bytes}, {value_cache, cache_bytes}))
+        return PCP_ERR_ARG;
     const int32_t vec_per_tok = (int32_t)((int64_t)head_dim * num_kv_heads / 16);
     return launch_cache_write_fp8(k, v, slot_mapping, num_tokens, vec_per_tok, key_cache, value_cache,
                                   num_blocks * block_size, k_scale, v_scale, status,
@@ -141,7 +173,7 @@ int attn_call(const void* q, const void* key_cache, const void* value_cache, con
     if (num_rows < 0 || total_q < 0 || num_reqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || max_blocks_per_req < 0 ||
         num_blocks < 0 || block_size < 1)
         return PCP_ERR_ARG;
-    if (attn_partials(flags) < 0) return PCP_ERR_ARG;
+    if (attn_partials(flags) < 0 || !isfinite(scale)) return PCP_ERR_ARG;
     if (num_q_heads % num_kv_heads != 0) return PCP_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return PCP_ERR_UNSUPPORTED;
     if (block_size != 8 && block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
@@ -161,6 +193,24 @@ int attn_call(const void* q, const void* key_cache, const void* value_cache, con
     const WorkspaceLayout w =
         workspace_layout(num_rows, total_q, num_q_heads, head_dim, (int32_t)max_kv, flags);
     if (workspace_bytes < w.total) return PCP_ERR_WORKSPACE;
+    {
+        const size_t esize = k_descale ? 1 : 2;
+        const size_t out_bytes = (size_t)total_q * num_q_heads * head_dim * 2;
+        const size_t lse_bytes = (size_t)total_q * num_q_heads * 4;
+        const size_t cache_bytes = (size_t)num_blocks * block_size * num_kv_heads * head_dim * esize;
+        const size_t descale_bytes = k_descale ? (size_t)num_reqs * num_kv_heads * 4 : 0;
+        const Span ins[8] = {{q, out_bytes},
+                             {key_cache, cache_bytes},
+                             {value_cache, cache_bytes},
+                             {block_table, (size_t)num_reqs * max_blocks_per_req * 4},
+                             {rows, (size_t)num_rows * sizeof(pcp_row_t)},
+                             {workspace, w.total},
+                             {k_descale, descale_bytes},
+                             {v_descale, descale_bytes}};
+        if (overlaps_any({out, out_bytes}, ins, 8) || overlaps_any({lse, lse_bytes}, ins, 8) ||
+            overlap({out, out_bytes}, {lse, lse_bytes}))
+            return PCP_ERR_ARG;
+    }
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     PrefillArgs a{};
@@ -255,11 +305,16 @@ extern "C" int pcp_lse_merge(const float* out_a, const float* lse_a, const float
     if (head_dim % 8 != 0) return PCP_ERR_UNSUPPORTED;
     if (total_q == 0) return PCP_OK;
     if (!out_a || !lse_a || !out_b || !lse_b || !out || !lse) return PCP_ERR_ARG;
-    if (lse == lse_a || lse == lse_b) return PCP_ERR_ARG;
     if (!aligned16(out_a) || !aligned16(out_b) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(lse_a) & 3u) || (reinterpret_cast<uintptr_t>(lse_b) & 3u) ||
         (reinterpret_cast<uintptr_t>(lse) & 3u))
         return PCP_ERR_ALIGN;
+    const size_t part_bytes = (size_t)total_q * num_q_heads * head_dim * 4;
+    const size_t lse_bytes = (size_t)total_q * num_q_heads * 4;
+    const Span ins[4] = {{out_a, part_bytes}, {out_b, part_bytes}, {lse_a, lse_bytes}, {lse_b, lse_bytes}};
+    const Span o = {out, part_bytes / 2};
+    if (overlaps_any(o, ins, 4) || overlaps_any({lse, lse_bytes}, ins, 4) || overlap(o, {lse, lse_bytes}))
+        return PCP_ERR_ARG;
     return launch_lse_merge(out_a, lse_a, out_b, lse_b, out, lse, total_q, num_q_heads, head_dim,
                             reinterpret_cast<cudaStream_t>(stream));
 }

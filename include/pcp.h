@@ -148,10 +148,12 @@ int pcp_mask_slots_for_shard(const int64_t* slot_mapping, const int8_t* owner_sh
  * pcp_has_prefill"). The write must precede the attention of the same step
  * ("What made it removable": the cache update is ordered before attention);
  * issuing both on one stream does that.
- * k, v, slot_mapping, key_cache, value_cache, status: device pointers.
+ * k, v, slot_mapping, key_cache, value_cache, status: device pointers;
+ * key_cache and value_cache overlap neither each other nor k, v or
+ * slot_mapping (PCP_ERR_ARG).
  * A slot >= num_blocks * block_size is skipped and sets *status = PCP_ERR_RANGE.
- * Supported: head_dim * 2 bytes a multiple of 16. Errors: PCP_ERR_ARG,
- * PCP_ERR_ALIGN, PCP_ERR_UNSUPPORTED, PCP_ERR_CUDA (launch failure).
+ * Supported: a token row of Hkv * head_dim * 2 bytes a multiple of 16. Errors:
+ * PCP_ERR_ARG, PCP_ERR_ALIGN, PCP_ERR_UNSUPPORTED, PCP_ERR_CUDA (launch failure).
  */
 int pcp_kv_cache_write(const void* k, const void* v, const int64_t* slot_mapping,
                        int32_t num_tokens, void* key_cache, void* value_cache, int64_t num_blocks,
@@ -197,6 +199,9 @@ size_t pcp_attn_workspace_size(int32_t num_rows, int32_t total_q, int32_t num_q_
  * PCP_ATTN_KV_SHARDS(n) computes n partials over n contiguous key shards and
  * merges them (decode rows are always split-KV internally; flags do not change
  * their result). Every mode gives the same attention up to rounding.
+ * scale: any finite float (PCP_ERR_ARG otherwise). out and lse overlap
+ * neither each other nor any input buffer (q, the caches, block_table, rows,
+ * the used workspace; PCP_ERR_ARG).
  * Supported: head_dim 64 or 128, block_size in {8, 16, 32, 64, 128},
  * Hq % Hkv == 0 with Hq / Hkv <= 16.
  * Rows with an out-of-range page id are skipped in part and set *status =
@@ -245,7 +250,7 @@ int pcp_attn_varlen_noalloc(const void* q, const void* key_cache, const void* va
  * saturated at +-448. k_scale and v_scale are the layer's scales ("[MRv2]
  * FlashAttention PCP support ...", the context-pass call: layer._k_scale,
  * layer._v_scale), host floats, finite and > 0 (else PCP_ERR_ARG).
- * key_cache, value_cache: [num_blocks][block_size][Hkv][D] bytes. Same slot,
+ * key_cache, value_cache: [num_blocks][block_size][Hkv][D] bytes. Same slot, overlap,
  * PAD and status rules as pcp_kv_cache_write. Supported: Hkv * D a multiple of
  * 16. Errors: PCP_ERR_ARG, PCP_ERR_ALIGN, PCP_ERR_UNSUPPORTED, PCP_ERR_CUDA.
  */
@@ -265,8 +270,9 @@ int pcp_kv_cache_write_fp8(const void* k, const void* v, const int64_t* slot_map
  * fp32 scores and outputs).
  * key_cache, value_cache: [num_blocks][block_size][Hkv][D] bytes (as written
  * by pcp_kv_cache_write_fp8); k_descale, v_descale: device fp32
- * [num_reqs][Hkv]. Every other argument, check, flag and error is that of
- * pcp_attn_varlen, with the same workspace size.
+ * [num_reqs][Hkv] (inputs: out and lse must not overlap them). Every other
+ * argument, check, flag and error is that of pcp_attn_varlen, with the same
+ * workspace size.
  */
 int pcp_attn_varlen_fp8kv(const void* q, const void* key_cache, const void* value_cache,
                           const float* k_descale, const float* v_descale, const int32_t* block_table,
@@ -285,8 +291,9 @@ int pcp_attn_varlen_fp8kv(const void* q, const void* key_cache, const void* valu
  *   out = (w_a out_a + w_b out_b) / (w_a + w_b), lse = m + log(w_a + w_b);
  * a part with lse = -inf contributes nothing; both -inf give out = 0, lse = -inf.
  * out_a, out_b: [total_q][Hq][D] fp32; lse_a, lse_b, lse: [Hq][total_q] fp32;
- * out: [total_q][Hq][D] bf16. All device pointers; lse must not alias lse_a or lse_b
- * (PCP_ERR_ARG). Errors: PCP_ERR_ARG, PCP_ERR_ALIGN, PCP_ERR_UNSUPPORTED (head_dim % 8 != 0),
+ * out: [total_q][Hq][D] bf16. All device pointers; out and lse overlap neither
+ * each other nor any of the four inputs (no in-place merge: PCP_ERR_ARG).
+ * Errors: PCP_ERR_ARG, PCP_ERR_ALIGN, PCP_ERR_UNSUPPORTED (head_dim % 8 != 0),
  * PCP_ERR_CUDA.
  */
 int pcp_lse_merge(const float* out_a, const float* lse_a, const float* out_b, const float* lse_b,

@@ -199,3 +199,56 @@ def test_fp8_entry_points_validate_before_launch(P):
     assert w(V(FAKE + 4), V(FAKE), V(FAKE), 10, V(FAKE), V(FAKE), 8, 16, 2, 128, 1.0, 1.0, None, None) \
         == P.PCP_ERR_ALIGN
     assert w(V(FAKE), V(FAKE), V(FAKE), 0, V(FAKE), V(FAKE), 8, 16, 2, 128, 1.0, 1.0, None, None) == P.PCP_OK
+
+
+GiB = 1 << 30
+BASE = 1 << 40          # distinct fake buffers, 1 GiB apart, never dereferenced
+
+
+def _distinct(**kw):
+    names = ["q", "kc", "vc", "bt", "rows", "out", "lse", "ws"]
+    d = {n: BASE + i * GiB for i, n in enumerate(names)}
+    d.update(kw)
+    return d
+
+
+def test_overlapping_outputs_and_non_finite_scale_are_refused(P):
+    """Every call below fails a host check, so nothing is launched on a fake
+    pointer. With distinct buffers a too-small workspace (the check just
+    before the overlap checks) is what fails; moving one output onto an input
+    turns that into PCP_ERR_ARG."""
+    lib = P.load()
+    V = ctypes.c_void_p
+    assert _attn(lib, wsb=100, **_distinct()) == P.PCP_ERR_WORKSPACE
+    for scale in (float("nan"), float("inf"), float("-inf")):
+        assert _attn(lib, scale=scale, **_distinct()) == P.PCP_ERR_ARG
+    out_bytes = 100 * 8 * 128 * 2
+    for kw in (dict(out=BASE), dict(out=BASE + 3 * GiB - 256),          # onto q; across the block table
+               dict(lse=BASE + 4 * GiB + 32), dict(out=BASE + 7 * GiB + 256),   # into rows; into the workspace
+               dict(lse=BASE + 5 * GiB + out_bytes - 4), dict(kc=BASE + 6 * GiB)):  # out/lse; lse on a cache
+        assert _attn(lib, **_distinct(**kw)) == P.PCP_ERR_ARG, kw
+    # the FP8 descales are inputs too
+    d = _distinct()
+    assert _attn_fp8(lib, kd=d["out"] + 64, **{k: v for k, v in d.items()}) == P.PCP_ERR_ARG
+    # cache write: the caches overlap neither each other nor k, v, slot_mapping
+    tok = 10 * 2 * 128 * 2
+
+    def write(k, v, slot, kc, vc):
+        return lib.pcp_kv_cache_write(V(k), V(v), V(slot), 10, V(kc), V(vc), 8, 16, 2, 128, None, None)
+    assert write(BASE, BASE + GiB, BASE + 2 * GiB, BASE + 3 * GiB, BASE + 3 * GiB) == P.PCP_ERR_ARG
+    assert write(BASE, BASE + GiB, BASE + 2 * GiB, BASE + tok - 16, BASE + 4 * GiB) == P.PCP_ERR_ARG
+    assert write(BASE, BASE + GiB, BASE + 2 * GiB, BASE + 3 * GiB, BASE + 2 * GiB + 64) == P.PCP_ERR_ARG
+    w8 = lib.pcp_kv_cache_write_fp8
+    assert w8(V(BASE), V(BASE + GiB), V(BASE + 2 * GiB), 10, V(BASE + 3 * GiB), V(BASE + 3 * GiB + 16), 8, 16, 2,
+              128, 1.0, 1.0, None, None) == P.PCP_ERR_ARG
+    # LSE merge: no in-place merge, no partial overlap of the lse arrays
+    T, H, D = 4, 2, 128
+    part, lse_b = T * H * D * 4, T * H * 4
+
+    def merge(oa, la, ob, lb, o, l):
+        return lib.pcp_lse_merge(V(oa), V(la), V(ob), V(lb), V(o), V(l), T, H, D, None)
+    a = [BASE + i * GiB for i in range(6)]
+    assert merge(a[0], a[1], a[2], a[3], a[0], a[5]) == P.PCP_ERR_ARG            # out onto out_a
+    assert merge(a[0], a[1], a[2], a[3], a[2] + part - 16, a[5]) == P.PCP_ERR_ARG  # out runs into out_b
+    assert merge(a[0], a[1], a[2], a[3], a[4], a[1] + 4) == P.PCP_ERR_ARG         # lse shifted onto lse_a
+    assert merge(a[0], a[1], a[2], a[3], a[4], a[4] + part // 2 - lse_b // 2) == P.PCP_ERR_ARG  # out / lse
