@@ -11,4 +11,4 @@ from ._lib import (EXPORTS, PCP_ATTN_KV_SHARDS, PCP_ATTN_SEPARATE_CONTEXT, PCP_A
                    PcpError, load, pcp_attn_varlen, pcp_attn_varlen_fp8kv, pcp_attn_varlen_noalloc,
                    pcp_attn_workspace_size, pcp_build_row_plan, pcp_kv_cache_write, pcp_kv_cache_write_fp8,
                    pcp_lse_merge, pcp_mask_slots_for_shard, pcp_set_profile_events)
-from .step import PcpStep, write_positions  # noqa: F401
+from .step import PcpStep, debug_plan, plan_summary, write_positions  # noqa: F401

@@ -20,6 +20,8 @@ This module only sequences those calls and owns the buffers (the reviewer's
 """
 from __future__ import annotations
 
+import os
+import sys
 from typing import Optional, Sequence
 
 import numpy as np
@@ -64,8 +66,11 @@ class PcpStep:
         self.plan = None
 
     def build_plan(self, query_len: Sequence[int], num_computed: Sequence[int], block_table_host) -> dict:
+        """Step 1. With ``PCP_DEBUG=1`` in the environment a summary of the plan
+        (:func:`plan_summary`) goes to stderr."""
         self.plan = L.pcp_build_row_plan(query_len, num_computed, block_table_host, self.bs, self.shards,
                                          self.split_mode, rows_capacity=self.max_rows)
+        debug_plan(self.plan, self.shards)
         return self.plan
 
     def upload_plan(self, stream=None) -> None:
@@ -114,6 +119,35 @@ class PcpStep:
         if s != 0:
             self.status.zero_()
             raise L.PcpError(s, "device status")
+
+
+def plan_summary(plan: dict, num_shards: int) -> str:
+    """A few lines on a row plan: rows and tokens per shard, prefill / decode /
+    prefix rows, the longest row and key range, and the slot mapping's PAD
+    count and range."""
+    rows = np.asarray(plan["rows"]).reshape(-1, len(L.ROW_FIELDS)).astype(np.int64)
+    slots = np.asarray(plan["slot_mapping"])
+    lines = [f"[pcp] plan: {rows.shape[0]} rows ({int((rows[:, 7] == 0).sum())} prefill, "
+             f"{int((rows[:, 7] == 1).sum())} decode), {int(rows[:, 3].sum())} tokens, {num_shards} shards"]
+    for s in range(num_shards):
+        r = rows[rows[:, 1] == s]
+        if r.shape[0] == 0:
+            lines.append(f"[pcp]   shard {s}: no rows")
+            continue
+        lines.append(f"[pcp]   shard {s}: {r.shape[0]} rows, {int(r[:, 3].sum())} tokens, q_len "
+                     f"{int(r[:, 3].min())}..{int(r[:, 3].max())}, kv_end max {int(r[:, 5].max())}, "
+                     f"{int((r[:, 4] > 0).sum())} with a cached prefix")
+    pad = int((slots < 0).sum())
+    live = slots[slots >= 0]
+    rng = f"[{int(live.min())}, {int(live.max())}]" if live.size else "[]"
+    lines.append(f"[pcp] slots: {slots.shape[0]} ({pad} PAD), range {rng}")
+    return "\n".join(lines)
+
+
+def debug_plan(plan: dict, num_shards: int) -> None:
+    """Print :func:`plan_summary` to stderr when ``PCP_DEBUG=1``."""
+    if os.environ.get("PCP_DEBUG", "") == "1":
+        print(plan_summary(plan, num_shards), file=sys.stderr, flush=True)
 
 
 def write_positions(key_cache: torch.Tensor, value_cache: torch.Tensor, block_table_host,

@@ -252,3 +252,22 @@ def test_overlapping_outputs_and_non_finite_scale_are_refused(P):
     assert merge(a[0], a[1], a[2], a[3], a[2] + part - 16, a[5]) == P.PCP_ERR_ARG  # out runs into out_b
     assert merge(a[0], a[1], a[2], a[3], a[4], a[1] + 4) == P.PCP_ERR_ARG         # lse shifted onto lse_a
     assert merge(a[0], a[1], a[2], a[3], a[4], a[4] + part // 2 - lse_b // 2) == P.PCP_ERR_ARG  # out / lse
+
+
+def test_debug_plan_summary(P, monkeypatch, capsys):
+    """PCP_DEBUG=1 prints the plan summary (rows and tokens per shard, decode
+    rows, PAD slots) to stderr; without it nothing is printed."""
+    bt = np.arange(200, dtype=np.int32).reshape(4, 50)
+    plan = P.pcp_build_row_plan([300, 1, 77, 0], [0, 500, 13, 4], bt, 16, 2)
+    text = P.plan_summary(plan, 2)
+    assert "5 rows (4 prefill, 1 decode), 378 tokens, 2 shards" in text
+    assert "shard 0: 3 rows, 189 tokens" in text and "shard 1: 2 rows, 189 tokens" in text
+    assert "378 (0 PAD)" in text
+    masked = dict(plan, slot_mapping=P.pcp_mask_slots_for_shard(plan["slot_mapping"], plan["owner_shard"], 1))
+    assert "378 (189 PAD)" in P.plan_summary(masked, 2)
+    monkeypatch.delenv("PCP_DEBUG", raising=False)
+    P.debug_plan(plan, 2)
+    assert capsys.readouterr().err == ""
+    monkeypatch.setenv("PCP_DEBUG", "1")
+    P.debug_plan(plan, 2)
+    assert capsys.readouterr().err.strip() == text
