@@ -121,6 +121,81 @@ def _check(rc: int, what: str):
         raise PcpError(rc, what)
 
 
+BF16 = (torch.bfloat16,)
+F32 = (torch.float32,)
+I32 = (torch.int32,)
+I64 = (torch.int64,)
+# an FP8 cache holds one e4m3 code per byte: raw bytes or PyTorch's e4m3 "fn" type
+FP8_CACHE = (torch.uint8,) + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ())
+
+
+def _is_device_tensor(t: torch.Tensor) -> bool:
+    return t.device.type == "cuda"
+
+
+def _dev(t, name: str, dtypes=None, shape=None, device=None) -> torch.Tensor:
+    """``t`` checked before its pointer crosses the ABI: a contiguous CUDA tensor
+    (the library takes device pointers), of one of ``dtypes``, of ``shape``
+    where given (-1 leaves a dimension free) and on ``device`` where given.
+    Raises TypeError / ValueError; nothing is launched."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {' or '.join(str(d) for d in dtypes)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if shape is not None and (t.dim() != len(shape) or
+                              any(want != -1 and want != got for want, got in zip(shape, t.shape))):
+        want = tuple("*" if x == -1 else x for x in shape)
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {want}")
+    if not _is_device_tensor(t):
+        raise ValueError(f"{name}: must be a CUDA tensor (the library takes device pointers), got {t.device}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, the other arguments are on {device}")
+    return t
+
+
+def _status(status, device) -> Optional[torch.Tensor]:
+    if status is None:
+        return None
+    _dev(status, "status", I32, device=device)
+    if status.numel() < 1:
+        raise ValueError("status: needs one int32 element")
+    return status
+
+
+def _check_write(k, v, slot_mapping, key_cache, value_cache, status, cache_dtypes):
+    _dev(key_cache, "key_cache", cache_dtypes, shape=(-1, -1, -1, -1))
+    dev = key_cache.device
+    nb, bs, hkv, d = (int(x) for x in key_cache.shape)
+    _dev(value_cache, "value_cache", cache_dtypes, shape=(nb, bs, hkv, d), device=dev)
+    _dev(k, "k", BF16, shape=(-1, hkv, d), device=dev)
+    T = int(k.shape[0])
+    _dev(v, "v", BF16, shape=(T, hkv, d), device=dev)
+    _dev(slot_mapping, "slot_mapping", I64, shape=(T,), device=dev)
+    _status(status, dev)
+    return T, nb, bs, hkv, d
+
+
+def _check_attn(q, key_cache, value_cache, block_table, rows, out, lse, workspace, status, cache_dtypes):
+    _dev(q, "q", BF16, shape=(-1, -1, -1))
+    dev = q.device
+    T, hq, d = (int(x) for x in q.shape)
+    _dev(key_cache, "key_cache", cache_dtypes, shape=(-1, -1, -1, d), device=dev)
+    nb, bs, hkv, _ = (int(x) for x in key_cache.shape)
+    _dev(value_cache, "value_cache", cache_dtypes, shape=(nb, bs, hkv, d), device=dev)
+    _dev(block_table, "block_table", I32, shape=(-1, -1), device=dev)
+    _dev(rows, "rows", I32, shape=(-1, len(ROW_FIELDS)), device=dev)
+    if out is not None:
+        _dev(out, "out", BF16, shape=(T, hq, d), device=dev)
+    if lse is not None:
+        _dev(lse, "lse", F32, shape=(hq, T), device=dev)
+    if workspace is not None:
+        _dev(workspace, "workspace", device=dev)
+    _status(status, dev)
+    return T, hq, d, nb, bs, hkv
+
+
 def pcp_build_row_plan(query_len, num_computed, block_table, block_size: int, num_shards: int,
                        split_mode: int = PCP_SPLIT_CONTIGUOUS, rows_capacity: Optional[int] = None):
     """Host row plan and slot mapping. Returns a dict of numpy arrays:
@@ -164,8 +239,7 @@ def pcp_kv_cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Ten
                        status: Optional[torch.Tensor] = None, stream=None) -> None:
     """Scatter new K/V ``[T, Hkv, D]`` into the paged caches ``[num_blocks, bs, Hkv, D]``."""
     lib = load()
-    T = int(k.shape[0])
-    nb, bs, hkv, d = (int(x) for x in key_cache.shape)
+    T, nb, bs, hkv, d = _check_write(k, v, slot_mapping, key_cache, value_cache, status, BF16)
     rc = lib.pcp_kv_cache_write(_t_ptr(k), _t_ptr(v), _t_ptr(slot_mapping), T, _t_ptr(key_cache),
                                 _t_ptr(value_cache), nb, bs, hkv, d, _t_ptr(status), _stream(stream))
     _check(rc, "pcp_kv_cache_write")
@@ -177,8 +251,7 @@ def pcp_kv_cache_write_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch
     """Scatter new bf16 K/V ``[T, Hkv, D]`` into FP8 (e4m3) caches ``[num_blocks, bs,
     Hkv, D]`` (uint8) as e4m3(x / k_scale) and e4m3(x / v_scale)."""
     lib = load()
-    T = int(k.shape[0])
-    nb, bs, hkv, d = (int(x) for x in key_cache.shape)
+    T, nb, bs, hkv, d = _check_write(k, v, slot_mapping, key_cache, value_cache, status, FP8_CACHE)
     rc = lib.pcp_kv_cache_write_fp8(_t_ptr(k), _t_ptr(v), _t_ptr(slot_mapping), T, _t_ptr(key_cache),
                                     _t_ptr(value_cache), nb, bs, hkv, d, float(k_scale), float(v_scale),
                                     _t_ptr(status), _stream(stream))
@@ -199,8 +272,8 @@ def pcp_attn_varlen(q: torch.Tensor, key_cache: torch.Tensor, value_cache: torch
     ``[n, 8]`` on the device; returns ``(out [T, Hq, D] bf16, lse [Hq, T] fp32)``.
     Pass ``out``/``lse``/``workspace`` to avoid allocating per call."""
     lib = load()
-    T, hq, d = (int(x) for x in q.shape)
-    nb, bs, hkv, d2 = (int(x) for x in key_cache.shape)
+    T, hq, d, nb, bs, hkv = _check_attn(q, key_cache, value_cache, block_table, rows, out, lse, workspace, status,
+                                        BF16)
     n_rows = int(rows.shape[0])
     mb = int(block_table.shape[1])
     if out is None:
@@ -227,8 +300,11 @@ def pcp_attn_varlen_fp8kv(q: torch.Tensor, key_cache: torch.Tensor, value_cache:
     """:func:`pcp_attn_varlen` over FP8 (e4m3, uint8) caches with fp32 descales
     ``[num_reqs, Hkv]`` on the device."""
     lib = load()
-    T, hq, d = (int(x) for x in q.shape)
-    nb, bs, hkv, _ = (int(x) for x in key_cache.shape)
+    T, hq, d, nb, bs, hkv = _check_attn(q, key_cache, value_cache, block_table, rows, out, lse, workspace, status,
+                                        FP8_CACHE)
+    R = int(block_table.shape[0])
+    _dev(k_descale, "k_descale", F32, shape=(R, hkv), device=q.device)
+    _dev(v_descale, "v_descale", F32, shape=(R, hkv), device=q.device)
     n_rows = int(rows.shape[0])
     mb = int(block_table.shape[1])
     if out is None:
@@ -256,8 +332,10 @@ def pcp_attn_varlen_noalloc(q: torch.Tensor, key_cache: torch.Tensor, value_cach
     scratch array (reserved on each GPU that loads the library) replaces the
     workspace. Calls on one device share that array: keep them on one stream."""
     lib = load()
-    T, hq, d = (int(x) for x in q.shape)
-    nb, bs, hkv, _ = (int(x) for x in key_cache.shape)
+    if out is None or lse is None:
+        raise ValueError("pcp_attn_varlen_noalloc: out and lse are required")
+    T, hq, d, nb, bs, hkv = _check_attn(q, key_cache, value_cache, block_table, rows, out, lse, None, status,
+                                        BF16)
     rc = lib.pcp_attn_varlen_noalloc(_t_ptr(q), _t_ptr(key_cache), _t_ptr(value_cache), _t_ptr(block_table),
                                      int(block_table.shape[0]), int(block_table.shape[1]), nb, bs, _t_ptr(rows),
                                      int(rows.shape[0]), T, hq, hkv, d, float(scale), _t_ptr(out), _t_ptr(lse),
@@ -270,11 +348,18 @@ def pcp_lse_merge(out_a: torch.Tensor, lse_a: torch.Tensor, out_b: torch.Tensor,
                   out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None, stream=None):
     """LSE merge of two fp32 partials ``[T, Hq, D]`` / ``[Hq, T]`` into bf16 out and fp32 lse."""
     lib = load()
+    _dev(out_a, "out_a", F32, shape=(-1, -1, -1))
+    dev = out_a.device
     T, hq, d = (int(x) for x in out_a.shape)
+    _dev(out_b, "out_b", F32, shape=(T, hq, d), device=dev)
+    _dev(lse_a, "lse_a", F32, shape=(hq, T), device=dev)
+    _dev(lse_b, "lse_b", F32, shape=(hq, T), device=dev)
     if out is None:
-        out = torch.empty(out_a.shape, dtype=torch.bfloat16, device=out_a.device)
+        out = torch.empty(out_a.shape, dtype=torch.bfloat16, device=dev)
     if lse is None:
         lse = torch.empty_like(lse_a)
+    _dev(out, "out", BF16, shape=(T, hq, d), device=dev)
+    _dev(lse, "lse", F32, shape=(hq, T), device=dev)
     rc = lib.pcp_lse_merge(_t_ptr(out_a), _t_ptr(lse_a), _t_ptr(out_b), _t_ptr(lse_b), _t_ptr(out), _t_ptr(lse),
                            T, hq, d, _stream(stream))
     _check(rc, "pcp_lse_merge")

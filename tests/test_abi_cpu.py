@@ -271,3 +271,142 @@ def test_debug_plan_summary(P, monkeypatch, capsys):
     monkeypatch.setenv("PCP_DEBUG", "1")
     P.debug_plan(plan, 2)
     assert capsys.readouterr().err.strip() == text
+
+
+def test_binding_refuses_host_and_malformed_tensors(P):
+    """The binding checks every tensor before its pointer crosses the ABI: a
+    host tensor (which the kernels would read as a device address), a wrong
+    dtype, a non-contiguous view or a wrong shape raises, and nothing is
+    called. (CUDA tensors are not available here: each check is reached with
+    host tensors, the device check last.)"""
+    import torch
+    from context_prefill_attention_gb300 import _lib as L
+    q = torch.zeros((10, 4, 128), dtype=torch.bfloat16)
+    kc = torch.zeros((2, 16, 2, 128), dtype=torch.bfloat16)
+    bt = torch.zeros((1, 2), dtype=torch.int32)
+    rows = torch.zeros((1, 8), dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        P.pcp_attn_varlen(q, kc, kc, bt, rows, 0.1)
+    with pytest.raises(TypeError, match="dtype"):
+        P.pcp_attn_varlen(q.float(), kc, kc, bt, rows, 0.1)
+    with pytest.raises(ValueError, match="contiguous"):
+        P.pcp_attn_varlen(q.transpose(0, 1), kc, kc, bt, rows, 0.1)
+    with pytest.raises(ValueError, match="shape"):
+        P.pcp_attn_varlen(q[0], kc, kc, bt, rows, 0.1)
+    with pytest.raises(ValueError, match="CUDA"):
+        P.pcp_attn_varlen_fp8kv(q, kc.view(torch.uint8)[..., :128], kc, None, None, bt, rows, 0.1)
+    with pytest.raises(ValueError, match="CUDA"):
+        P.pcp_attn_varlen_noalloc(q, kc, kc, bt, rows, 0.1, q, torch.zeros((4, 10)))
+    k = torch.zeros((5, 2, 128), dtype=torch.bfloat16)
+    slot = torch.zeros(5, dtype=torch.int64)
+    with pytest.raises(ValueError, match="CUDA"):
+        P.pcp_kv_cache_write(k, k, slot, kc, kc.clone())
+    with pytest.raises(TypeError, match="dtype"):
+        P.pcp_kv_cache_write_fp8(k, k, slot, kc, kc.clone(), 1.0, 1.0)      # a bf16 cache for the FP8 writer
+    with pytest.raises(ValueError, match="CUDA"):
+        P.pcp_lse_merge(torch.zeros((10, 4, 128)), torch.zeros((4, 10)), torch.zeros((10, 4, 128)),
+                        torch.zeros((4, 10)))
+    with pytest.raises(TypeError, match="torch.Tensor"):
+        P.pcp_lse_merge(np.zeros((10, 4, 128), np.float32), None, None, None)
+    # the shape rule: exact sizes, -1 free, the rank must match
+    t = torch.zeros((3, 8))
+    for shape in ((3, 9), (3,), (3, 8, 1), (-1, 7)):
+        with pytest.raises(ValueError, match="shape"):
+            L._dev(t, "t", shape=shape)
+    with pytest.raises(ValueError, match="CUDA"):
+        L._dev(t, "t", (torch.float32,), shape=(-1, 8))          # every other check passes
+
+
+class _FakeLib:
+    """Stands in for libpcp: records each call's arguments and returns PCP_OK
+    (so the binding's marshalling runs to the end with nothing launched)."""
+
+    def __init__(self, real):
+        self.calls = {}
+        self.real = real
+
+    def pcp_attn_workspace_size(self, *a):
+        return self.real.pcp_attn_workspace_size(*a)
+
+    def pcp_status_string(self, code):
+        return self.real.pcp_status_string(code)
+
+    def pcp_last_cuda_error(self):
+        return 0
+
+    def __getattr__(self, name):
+        def f(*args):
+            self.calls[name] = args
+            return 0
+        return f
+
+
+def test_binding_marshals_consistent_tensors_and_checks_every_argument(P, monkeypatch):
+    """Host tensors stand in for device ones (the device test is switched off
+    and the library replaced by a recorder, so nothing reaches a kernel): the
+    wrappers accept consistent arguments, pass the right sizes across the ABI,
+    and refuse each inconsistent one."""
+    import torch
+    from context_prefill_attention_gb300 import _lib as L
+    fake = _FakeLib(L.load())
+    monkeypatch.setattr(L, "_lib", fake)
+    monkeypatch.setattr(L, "_is_device_tensor", lambda t: True)
+    T, hq, hkv, D, nb, bs, R, mb, n = 10, 8, 2, 128, 6, 16, 3, 2, 4
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    q = torch.zeros((T, hq, D), dtype=bf)
+    kc, vc = torch.zeros((nb, bs, hkv, D), dtype=bf), torch.zeros((nb, bs, hkv, D), dtype=bf)
+    bt = torch.zeros((R, mb), dtype=i32)
+    rows = torch.zeros((n, 8), dtype=i32)
+    out, lse = torch.zeros((T, hq, D), dtype=bf), torch.zeros((hq, T), dtype=f32)
+    ws = torch.zeros(1 << 20, dtype=torch.uint8)
+    st = torch.zeros(1, dtype=i32)
+    P.pcp_attn_varlen(q, kc, vc, bt, rows, 0.1, out=out, lse=lse, workspace=ws, flags=1, status=st, stream=0)
+    a = fake.calls["pcp_attn_varlen"]
+    assert a[4:14] == (R, mb, nb, bs) + a[8:9] + (n, T, hq, hkv, D) and a[18] == ws.numel() and a[19] == 1
+    bad = [dict(out=torch.zeros((T, hq, 64), dtype=bf)), dict(lse=torch.zeros((T, hq), dtype=f32)),
+           dict(lse=torch.zeros((hq, T), dtype=bf)), dict(status=torch.zeros(1, dtype=torch.int64)),
+           dict(status=torch.zeros(0, dtype=i32))]
+    for kw in bad:
+        args = dict(out=out, lse=lse, workspace=ws, status=st, stream=0)
+        args.update(kw)
+        with pytest.raises((TypeError, ValueError)):
+            P.pcp_attn_varlen(q, kc, vc, bt, rows, 0.1, **args)
+    for k2, v2, b2, r2 in ((kc, vc[:, :8], bt, rows), (kc[..., :64].contiguous(), vc, bt, rows),
+                           (kc, vc, bt.long(), rows), (kc, vc, bt, rows[:, :7].contiguous()),
+                           (kc.view(torch.uint8)[..., :D].contiguous(), vc, bt, rows)):
+        with pytest.raises((TypeError, ValueError)):
+            P.pcp_attn_varlen(q, k2, v2, b2, r2, 0.1, stream=0)
+    # FP8 cache: uint8 codes and fp32 descales [R, Hkv]
+    kc8, vc8 = torch.zeros((nb, bs, hkv, D), dtype=torch.uint8), torch.zeros((nb, bs, hkv, D), dtype=torch.uint8)
+    kd, vd = torch.ones((R, hkv)), torch.ones((R, hkv))
+    P.pcp_attn_varlen_fp8kv(q, kc8, vc8, kd, vd, bt, rows, 0.1, stream=0)
+    a = fake.calls["pcp_attn_varlen_fp8kv"]
+    assert a[6:16] == (R, mb, nb, bs) + a[10:11] + (n, T, hq, hkv, D)
+    for kd2, vd2, c2 in ((kd[:2], vd, kc8), (kd, vd.double(), kc8), (kd, vd, kc)):
+        with pytest.raises((TypeError, ValueError)):
+            P.pcp_attn_varlen_fp8kv(q, c2, vc8, kd2, vd2, bt, rows, 0.1, stream=0)
+    # no-allocation entry point: out and lse required
+    P.pcp_attn_varlen_noalloc(q, kc, vc, bt, rows, 0.1, out, lse, stream=0)
+    assert fake.calls["pcp_attn_varlen_noalloc"][4:6] == (R, mb)
+    with pytest.raises(ValueError):
+        P.pcp_attn_varlen_noalloc(q, kc, vc, bt, rows, 0.1, None, lse, stream=0)
+    # cache writes
+    k, v = torch.zeros((T, hkv, D), dtype=bf), torch.zeros((T, hkv, D), dtype=bf)
+    slot = torch.zeros(T, dtype=torch.int64)
+    P.pcp_kv_cache_write(k, v, slot, kc, vc, status=st, stream=0)
+    assert fake.calls["pcp_kv_cache_write"][3:4] + fake.calls["pcp_kv_cache_write"][6:10] == (T, nb, bs, hkv, D)
+    P.pcp_kv_cache_write_fp8(k, v, slot, kc8, vc8, 0.5, 0.25, stream=0)
+    assert fake.calls["pcp_kv_cache_write_fp8"][10:12] == (0.5, 0.25)
+    for k2, v2, s2 in ((k[:, :1].contiguous(), v, slot), (k, v[:5], slot), (k, v, slot[:5]), (k, v, slot.int()),
+                       (k.float(), v, slot)):
+        with pytest.raises((TypeError, ValueError)):
+            P.pcp_kv_cache_write(k2, v2, s2, kc, vc, stream=0)
+    # LSE merge
+    oa, ob = torch.zeros((T, hq, D)), torch.zeros((T, hq, D))
+    la, lb = torch.zeros((hq, T)), torch.zeros((hq, T))
+    o, l_ = P.pcp_lse_merge(oa, la, ob, lb, stream=0)
+    assert o.dtype == bf and o.shape == (T, hq, D) and l_.shape == (hq, T)
+    assert fake.calls["pcp_lse_merge"][6:9] == (T, hq, D)
+    for args in ((oa, la, ob[:5], lb), (oa, la.t(), ob, lb), (oa, la, ob, lb.double()), (oa.bfloat16(), la, ob, lb)):
+        with pytest.raises((TypeError, ValueError)):
+            P.pcp_lse_merge(*args, stream=0)
