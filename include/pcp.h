@@ -199,6 +199,10 @@ size_t pcp_attn_workspace_size(int32_t num_rows, int32_t total_q, int32_t num_q_
  * PCP_ATTN_KV_SHARDS(n) computes n partials over n contiguous key shards and
  * merges them (decode rows are always split-KV internally; flags do not change
  * their result). Every mode gives the same attention up to rounding.
+ * Numerics: scores, softmax and sums in fp32, P rounded to bf16 for the
+ * P V product; the result is finite whenever every scale * q . k is finite in
+ * fp32 and |v| < 2^54 (the exponentials may run up to 2^64 against a stale
+ * row maximum before the exact rescaling path takes over).
  * scale: any finite float (PCP_ERR_ARG otherwise). out and lse overlap
  * neither each other nor any input buffer (q, the caches, block_table, rows,
  * the used workspace; PCP_ERR_ARG).
