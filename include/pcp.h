@@ -201,8 +201,9 @@ size_t pcp_attn_workspace_size(int32_t num_rows, int32_t total_q, int32_t num_q_
  * their result). Every mode gives the same attention up to rounding.
  * Numerics: scores, softmax and sums in fp32, P rounded to bf16 for the
  * P V product; the result is finite whenever every scale * q . k is finite in
- * fp32 and |v| < 2^54 (the exponentials may run up to 2^64 against a stale
- * row maximum before the exact rescaling path takes over).
+ * fp32 and ceil(keys / 128) * max |v| < 2^64, e.g. |v| < 2^54 at 131072 keys
+ * (a 128-key tile's exponentials may sum to 2^64 against a stale row maximum
+ * before the exact rescaling path takes over).
  * scale: any finite float (PCP_ERR_ARG otherwise). out and lse overlap
  * neither each other nor any input buffer (q, the caches, block_table, rows,
  * the used workspace; PCP_ERR_ARG).
