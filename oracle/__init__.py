@@ -7,8 +7,10 @@ library: the two meet only in the seeded inputs of ``workloads.py``.
 
 What each function follows is stated in ``oracle.c``. Every function is pinned
 by the CPU tests in ``tests/test_oracle_pins.py`` (dense brute force, closed
-forms, shard/merge invariants and the golden fixtures in ``tests/golden/``);
-no function here is "parity unpinned".
+forms, shard/merge invariants and the golden fixtures in ``tests/golden/``) and
+``tests/test_oracle_fp8_pins.py`` (the e4m3 codec against PyTorch's
+``float8_e4m3fn`` and hand-worked cases, FP8-cache attention against a dense
+softmax); no function here is "parity unpinned".
 """
 from __future__ import annotations
 
