@@ -131,13 +131,23 @@ __device__ __forceinline__ int32_t tiles_of(int32_t k_lo, int32_t k_end, int32_t
     return (k_end - kb + kBlockN - 1) / kBlockN;
 }
 
+// Item idx of the sorted unit list. A unit naming a row outside [0, num_rows)
+// (never written by the scheduler; a guard against a corrupted list) becomes an
+// empty item with no valid query row, which every role skips without a write.
 __device__ __forceinline__ Item decode_item(const Unit* units, int32_t idx, int32_t slots_per_unit,
                                             bool dual, int32_t G, const pcp_row_t* rows,
-                                            int32_t bs) {
+                                            int32_t num_rows, int32_t bs) {
     const Unit u = units[idx / slots_per_unit];
     const int32_t hs = idx % slots_per_unit;
-    const pcp_row_t r = rows[u.row];
     Item it;
+    if (u.row < 0 || u.row >= num_rows) {
+        it = Item{};
+        it.nslots = dual ? 2 : 1;
+        it.h0 = dual ? 2 * hs : hs;
+        it.hk = it.h0 / G;
+        return it;
+    }
+    const pcp_row_t r = rows[u.row];
     const int32_t mt = u.mt_pass & 0xFFFFFF;
     it.pass = u.mt_pass >> 24;
     it.req = r.req;
@@ -319,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int32_t round = 0; ok; ++round) {
             const int32_t idx = item_of_round(round);
             if (idx >= total_items) break;
-            const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, bs);
+            const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, a.num_rows, bs);
             if (it.n_tiles == 0) continue;
             if (c > 0 && !(ok = mbar_wait_warp(q_empty, (c - 1) & 1, abort_flag))) break;
             if (lane == 0) {
@@ -391,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int32_t round = 0; ok; ++round) {
             const int32_t idx = item_of_round(round);
             if (idx >= total_items) break;
-            const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, bs);
+            const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, a.num_rows, bs);
             for (int32_t j = 0; j < it.n_tiles && ok; ++j) {
                 const int ks = kt % kNK;
                 if (!(ok = mbar_wait_warp(kc_full(ks), (kt / kNK) & 1, abort_flag))) break;
@@ -431,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int32_t round = 0; ok; ++round) {
             const int32_t idx = item_of_round(round);
             if (idx >= total_items) break;
-            const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, bs);
+            const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, a.num_rows, bs);
             const int n = it.n_tiles;
             if (n == 0) continue;
             if (!(ok = mbar_wait(q_full, c & 1, abort_flag))) break;
@@ -513,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int32_t round = 0; ok; ++round) {
             const int32_t idx = item_of_round(round);
             if (idx >= total_items) break;
-            const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, bs);
+            const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, a.num_rows, bs);
             if (g >= it.nslots) continue;
             const int h = it.h0 + g;
             // FP8: the K descale scales every score (the V descale the output, below);
@@ -742,7 +752,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ scheduler
 
 constexpr int kSchedThreads = 1024;
+// Lists of up to kSortCap units are sorted exactly (bitonic, in shared memory);
+// longer ones by a counting sort over kCostBuckets cost classes (costs of
+// kCostBuckets - 1 key tiles or more share the first class).
 constexpr int kSortCap = 4096;
+constexpr int kCostBuckets = 2 * kSortCap;  // int32 counters in the same 32 KB as the sort keys
 
 __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* warp_sums, int32_t* total) {
     const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
@@ -770,6 +784,15 @@ __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* warp
     return before;
 }
 
+// Key tiles a unit's item walks (its cost in the schedule).
+__device__ __forceinline__ int32_t unit_cost(const Unit& u, const pcp_row_t* rows, int32_t bs) {
+    const pcp_row_t row = rows[u.row];
+    const int32_t mt = u.mt_pass & 0xFFFFFF;
+    const int32_t pos0 = row.kv_end - row.q_len + mt * kBlockM;
+    const int32_t rv = min(kBlockM, row.q_len - mt * kBlockM);
+    return tiles_of(u.k_lo, min(u.k_hi, pos0 + rv), bs);
+}
+
 // Check every row, then build the prefill work list: one unit per (valid
 // non-decode row, 128-token tile, pass), ordered by the number of key tiles,
 // longest first.
@@ -777,7 +800,8 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     schedule_kernel(PrefillArgs a, int32_t flags, Unit* units, Unit* sorted, int32_t* header,
                     int32_t* row_ok, int64_t max_units) {
     __shared__ int32_t warp_sums[32];
-    __shared__ unsigned long long keys[kSortCap];
+    // bitonic sort keys, or the counters of the counting sort
+    __shared__ __align__(16) unsigned long long keys[kSortCap];
     const pcp_row_t* rows = a.rows;
     const int32_t num_rows = a.num_rows, bs = a.block_size;
     const int64_t max_kv = (int64_t)a.max_blocks * bs;
@@ -825,22 +849,49 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     }
     const int32_t n = (int32_t)min((int64_t)base, max_units);
     if (threadIdx.x == 0) header[0] = n;
+    // every thread's units[] writes must be visible before any thread reads them
+    __syncthreads();
     if (n > kSortCap) {
-        for (int32_t i = threadIdx.x; i < n; i += kSchedThreads) sorted[i] = units[i];
+        // Counting sort, longest first: class c = kCostBuckets - 1 - min(cost,
+        // kCostBuckets - 1); count, exclusive scan, scatter. Units of one class
+        // land in any order (every item writes only its own outputs, so the
+        // order changes no result).
+        int32_t* cnt = reinterpret_cast<int32_t*>(keys);
+        for (int32_t i = threadIdx.x; i < kCostBuckets; i += kSchedThreads) cnt[i] = 0;
+        __syncthreads();
+        for (int32_t i = threadIdx.x; i < n; i += kSchedThreads) {
+            const int32_t c = kCostBuckets - 1 - min(unit_cost(units[i], rows, bs), kCostBuckets - 1);
+            atomicAdd(&cnt[c], 1);
+        }
+        __syncthreads();
+        constexpr int kPer = kCostBuckets / kSchedThreads;  // consecutive classes per thread
+        int32_t local[kPer], sum = 0;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            local[k] = cnt[threadIdx.x * kPer + k];
+            sum += local[k];
+        }
+        int32_t tot;
+        int32_t run = block_exclusive_scan(sum, warp_sums, &tot);
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            cnt[threadIdx.x * kPer + k] = run;
+            run += local[k];
+        }
+        __syncthreads();
+        for (int32_t i = threadIdx.x; i < n; i += kSchedThreads) {
+            const Unit u = units[i];
+            const int32_t c = kCostBuckets - 1 - min(unit_cost(u, rows, bs), kCostBuckets - 1);
+            sorted[atomicAdd(&cnt[c], 1)] = u;
+        }
         return;
     }
-    __syncthreads();
     int32_t pow2 = 1;
     while (pow2 < n) pow2 <<= 1;
     for (int32_t i = threadIdx.x; i < pow2; i += kSchedThreads) {
         unsigned long long key = ~0ull;
         if (i < n) {
-            const Unit u = units[i];
-            const pcp_row_t row = rows[u.row];
-            const int32_t mt = u.mt_pass & 0xFFFFFF;
-            const int32_t pos0 = row.kv_end - row.q_len + mt * kBlockM;
-            const int32_t rv = min(kBlockM, row.q_len - mt * kBlockM);
-            const int32_t cost = tiles_of(u.k_lo, min(u.k_hi, pos0 + rv), bs);
+            const int32_t cost = unit_cost(units[i], rows, bs);
             key = ((unsigned long long)(0x7FFFFFFF - cost) << 32) | (unsigned)i;
         }
         keys[i] = key;
