@@ -161,15 +161,17 @@ extern "C" size_t pcp_attn_workspace_size(int32_t num_rows, int32_t total_q, int
     return workspace_layout(num_rows, total_q, num_q_heads, head_dim, max_kv_len, flags).total;
 }
 
-namespace {
 // One attention call over a bf16 cache (k_descale == v_descale == nullptr) or
-// an FP8 one (both set).
-int attn_call(const void* q, const void* key_cache, const void* value_cache, const float* k_descale,
+// an FP8 one (both set). With a workspace provider, the workspace arguments are
+// ignored and, once every argument check has passed, the provider supplies the
+// workspace for the call's size.
+int pcp::attn_call(const void* q, const void* key_cache, const void* value_cache, const float* k_descale,
               const float* v_descale, const int32_t* block_table, int32_t num_reqs,
               int32_t max_blocks_per_req, int64_t num_blocks, int32_t block_size, const pcp_row_t* rows,
               int32_t num_rows, int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
               int32_t head_dim, float scale, void* out, float* lse, void* workspace,
-              size_t workspace_bytes, int32_t flags, int32_t* status, cudaStream_t s) {
+              size_t workspace_bytes, int32_t flags, int32_t* status, cudaStream_t s,
+              WorkspaceProvider provide) {
     if (num_rows < 0 || total_q < 0 || num_reqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || max_blocks_per_req < 0 ||
         num_blocks < 0 || block_size < 1)
         return PCP_ERR_ARG;
@@ -180,7 +182,11 @@ int attn_call(const void* q, const void* key_cache, const void* value_cache, con
         return PCP_ERR_UNSUPPORTED;
     if (num_q_heads / num_kv_heads > 16) return PCP_ERR_UNSUPPORTED;
     if (num_rows == 0 || total_q == 0) return PCP_OK;
-    if (!q || !key_cache || !value_cache || !block_table || !rows || !out || !lse || !workspace)
+    if (provide) {
+        workspace = nullptr;
+        workspace_bytes = 0;
+    }
+    if (!q || !key_cache || !value_cache || !block_table || !rows || !out || !lse || (!workspace && !provide))
         return PCP_ERR_ARG;
     if (!aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
@@ -192,6 +198,11 @@ int attn_call(const void* q, const void* key_cache, const void* value_cache, con
     if (max_kv > INT32_MAX) return PCP_ERR_ARG;
     const WorkspaceLayout w =
         workspace_layout(num_rows, total_q, num_q_heads, head_dim, (int32_t)max_kv, flags);
+    if (provide) {
+        const int rc = provide(w.total, &workspace, &workspace_bytes);
+        if (rc != PCP_OK) return rc;
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PCP_ERR_ALIGN;
+    }
     if (workspace_bytes < w.total) return PCP_ERR_WORKSPACE;
     {
         const size_t esize = k_descale ? 1 : 2;
@@ -258,7 +269,6 @@ int attn_call(const void* q, const void* key_cache, const void* value_cache, con
     if (a.nparts > 0) rc = launch_separate_merge(a, s);
     return rc;
 }
-}  // namespace
 
 extern "C" int pcp_attn_varlen(const void* q, const void* key_cache, const void* value_cache,
                                const int32_t* block_table, int32_t num_reqs,
@@ -270,7 +280,7 @@ extern "C" int pcp_attn_varlen(const void* q, const void* key_cache, const void*
     return attn_call(q, key_cache, value_cache, nullptr, nullptr, block_table, num_reqs, max_blocks_per_req,
                      num_blocks, block_size, rows, num_rows, total_q, num_q_heads, num_kv_heads, head_dim,
                      scale, out, lse, workspace, workspace_bytes, flags, status,
-                     reinterpret_cast<cudaStream_t>(stream));
+                     reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
 extern "C" int pcp_attn_varlen_fp8kv(const void* q, const void* key_cache, const void* value_cache,
@@ -286,7 +296,7 @@ extern "C" int pcp_attn_varlen_fp8kv(const void* q, const void* key_cache, const
         return PCP_ERR_ALIGN;
     return attn_call(q, key_cache, value_cache, k_descale, v_descale, block_table, num_reqs, max_blocks_per_req, num_blocks, block_size, rows, num_rows, total_q,
                      num_q_heads, num_kv_heads, head_dim, scale, out, lse, workspace, workspace_bytes, flags,
-                     status, reinterpret_cast<cudaStream_t>(stream));
+                     status, reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
 extern "C" int pcp_set_profile_events(void* prefill_begin, void* prefill_end, void* decode_begin,

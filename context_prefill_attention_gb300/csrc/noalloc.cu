@@ -7,18 +7,19 @@
 //
 // This entry point instead uses one fixed scratch array that lives in the
 // library's own device image: kStaticScratchBytes per GPU, reserved on every
-// GPU that loads this library until the process exits. It then runs exactly
-// the same launch sequence as pcp_attn_varlen (schedule, split-KV decode,
-// prefill, optional LSE merge) with that array as the workspace. The scratch
-// needs no clearing: every byte the kernels read is written earlier in the
-// same call. All calls on a device share the one array, so two calls whose
-// kernels overlap on the GPU (different streams without ordering between them,
-// or different host threads) race on it; order them on one stream.
+// GPU that loads this library until the process exits. It runs the same host
+// checks (in the same order) and the same launch sequence as pcp_attn_varlen
+// (schedule, split-KV decode, prefill, optional LSE merge) with that array as
+// the workspace. The scratch needs no clearing: every byte the kernels read is
+// written earlier in the same call. All calls on a device share the one array,
+// so two calls whose kernels overlap on the GPU (different streams without
+// ordering between them, or different host threads) race on it; order them on
+// one stream.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <mutex>
-
+#include "ctx_table.h"
 #include "pcp.h"
 #include "pcp_internal.h"
 
@@ -28,30 +29,58 @@ constexpr size_t kStaticScratchBytes = size_t(64) << 20;  // 64 MiB
 
 __device__ __align__(256) unsigned char g_scratch[kStaticScratchBytes];
 
-// Device address of g_scratch for each device (the host-side symbol is only a
-// stand-in and must never be passed to a kernel).
-void* g_scratch_addr[128] = {};
-std::mutex g_scratch_mu;
+// Device address of g_scratch per CUDA context (the host-side symbol is only a
+// stand-in and must never be passed to a kernel). Keyed by the context's ID, so
+// a context created after a device reset looks the address up again.
+pcp::CtxTable<32> g_scratch_addr;
 
-int scratch_for_current_device(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
-        pcp::set_last_cuda_error(e);
-        return PCP_ERR_CUDA;
-    }
-    if (dev < 0 || dev >= 128) return PCP_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_scratch);
+using PFN_ctxGetCurrent = CUresult (*)(CUcontext*);
+using PFN_ctxGetId = CUresult (*)(CUcontext, unsigned long long*);
+
+// A driver API function by name, or nullptr.
+void* driver_entry(const char* name) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return p;
+}
+
+// ID of the current context; false when no context is current yet or the
+// driver lacks the query.
+bool current_ctx_id(uint64_t* id) {
+    // resolved once (thread-safe static initialisation)
+    static const PFN_ctxGetCurrent get_current =
+        reinterpret_cast<PFN_ctxGetCurrent>(driver_entry("cuCtxGetCurrent"));
+    static const PFN_ctxGetId get_id = reinterpret_cast<PFN_ctxGetId>(driver_entry("cuCtxGetId"));
+    if (!get_current || !get_id) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    unsigned long long v = 0;
+    if (get_id(ctx, &v) != CUDA_SUCCESS) return false;
+    *id = v;
+    return true;
+}
+
+// The workspace provider of pcp_attn_varlen_noalloc: the scratch array of the
+// current device, if the call fits in it.
+int scratch_workspace(size_t need, void** ws, size_t* bytes) {
+    if (need > kStaticScratchBytes) return PCP_ERR_WORKSPACE;
+    uint64_t id = 0;
+    bool have_id = current_ctx_id(&id);
+    void* p = have_id ? g_scratch_addr.find(id) : nullptr;
+    if (!p) {
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
         if (e != cudaSuccess || p == nullptr) {
             pcp::set_last_cuda_error(e);
             return PCP_ERR_CUDA;
         }
-        g_scratch_addr[dev] = p;
+        if (!have_id) have_id = current_ctx_id(&id);  // the lookup made the context current
+        if (have_id) g_scratch_addr.put(id, p);
     }
-    *out = g_scratch_addr[dev];
+    *ws = p;
+    *bytes = kStaticScratchBytes;
     return PCP_OK;
 }
 
@@ -64,16 +93,8 @@ extern "C" int pcp_attn_varlen_noalloc(const void* q, const void* key_cache, con
                                        int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
                                        int32_t head_dim, float scale, void* out, float* lse,
                                        int32_t flags, int32_t* status, pcp_stream_t stream) {
-    if (max_blocks_per_req < 0 || block_size < 1) return PCP_ERR_ARG;
-    const int64_t max_kv = (int64_t)max_blocks_per_req * block_size;
-    if (max_kv > INT32_MAX) return PCP_ERR_ARG;
-    const size_t need = pcp_attn_workspace_size(num_rows, total_q, num_q_heads, head_dim, (int32_t)max_kv, flags);
-    if (need == 0) return PCP_ERR_ARG;
-    if (need > kStaticScratchBytes) return PCP_ERR_WORKSPACE;
-    void* scratch = nullptr;
-    const int rc = scratch_for_current_device(&scratch);
-    if (rc != PCP_OK) return rc;
-    return pcp_attn_varlen(q, key_cache, value_cache, block_table, num_reqs, max_blocks_per_req, num_blocks,
-                           block_size, rows, num_rows, total_q, num_q_heads, num_kv_heads, head_dim, scale, out,
-                           lse, scratch, kStaticScratchBytes, flags, status, stream);
+    return pcp::attn_call(q, key_cache, value_cache, nullptr, nullptr, block_table, num_reqs, max_blocks_per_req,
+                          num_blocks, block_size, rows, num_rows, total_q, num_q_heads, num_kv_heads, head_dim,
+                          scale, out, lse, nullptr, 0, flags, status, reinterpret_cast<cudaStream_t>(stream),
+                          scratch_workspace);
 }

@@ -93,6 +93,23 @@ struct PrefillArgs {
 // codes, 2: bf16) with a box of D x 1 x rows, no swizzle.
 bool make_kv_row_map(CUtensorMap* m, const void* base, int D, int esize, int64_t mid, int64_t outer, int rows);
 
+// Supplies the workspace of an attention call that has passed every argument
+// check: at least `need` bytes, 256-byte aligned. Returns PCP_OK after setting
+// *ws and *bytes, or the status the call returns.
+using WorkspaceProvider = int (*)(size_t need, void** ws, size_t* bytes);
+
+// The body of pcp_attn_varlen (k_descale = v_descale = nullptr) and
+// pcp_attn_varlen_fp8kv: host checks, then the launches on stream s. With a
+// provider the workspace arguments are ignored and the provider's workspace is
+// used (pcp_attn_varlen_noalloc).
+int attn_call(const void* q, const void* key_cache, const void* value_cache, const float* k_descale,
+              const float* v_descale, const int32_t* block_table, int32_t num_reqs,
+              int32_t max_blocks_per_req, int64_t num_blocks, int32_t block_size, const pcp_row_t* rows,
+              int32_t num_rows, int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
+              int32_t head_dim, float scale, void* out, float* lse, void* workspace,
+              size_t workspace_bytes, int32_t flags, int32_t* status, cudaStream_t s,
+              WorkspaceProvider provide);
+
 int launch_schedule(const PrefillArgs& a, int32_t flags, Unit* units, Unit* units_sorted,
                     int32_t* header, int32_t* row_ok, int64_t max_units, cudaStream_t stream);
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream);

@@ -231,14 +231,19 @@ int pcp_attn_varlen(const void* q, const void* key_cache, const void* value_cach
  * workspace arguments: the library supplies a fixed 64 MiB scratch array that
  * every GPU loading the library reserves until the process exits, and the
  * call allocates nothing.
- * Same arguments, semantics, checks and errors as pcp_attn_varlen, plus
- * PCP_ERR_WORKSPACE when pcp_attn_workspace_size(num_rows, total_q, Hq, D,
- * max_blocks_per_req * block_size, flags) exceeds 64 MiB (nothing launched).
- * The first call on a device looks up the array's device address with that
- * device current (cudaGetSymbolAddress); make that first call before any
- * stream capture. All calls on a device share the array: calls whose kernels
- * may overlap on the GPU (other streams or threads) race on it — serialise
- * them on one stream.
+ * Same arguments, semantics, checks (in the same order) and errors as
+ * pcp_attn_varlen; where that call would check the workspace size, this one
+ * returns PCP_ERR_WORKSPACE (nothing launched) when
+ * pcp_attn_workspace_size(num_rows, total_q, Hq, D, max_blocks_per_req *
+ * block_size, flags) exceeds 64 MiB, and PCP_ERR_CUDA when the array's device
+ * address cannot be looked up.
+ * The first call in a CUDA context looks up the array's device address with
+ * that context current (cudaGetSymbolAddress) and keeps it for that context;
+ * make that first call before any stream capture. A device reset ends the
+ * context, and the first call in the next one looks the address up again.
+ * All calls on a device share the array: calls whose kernels may overlap on
+ * the GPU (other streams or threads) race on it — serialise them on one
+ * stream.
  */
 int pcp_attn_varlen_noalloc(const void* q, const void* key_cache, const void* value_cache,
                             const int32_t* block_table, int32_t num_reqs, int32_t max_blocks_per_req,
