@@ -2,11 +2,12 @@
 
 A step is the whole hot path over one batch: the host row plan, its upload,
 the KV-cache write of the new tokens, and attention of every row (prefill,
-cached-prefix context and decode rows) through the C ABI. The default workload
-is the mixed prefill + decode batch (8 prompts of U[1024,8192] tokens in 2
-shard rows each plus 56 decode rows with U[1024,16384] keys, 32 q / 8 kv heads,
-D=128): the one workload on which both halves of the metric (prefill TFLOP/s
-and decode-row HBM GB/s) are defined.
+cached-prefix context and decode rows) through the C ABI. The default workload is the mixed prefill + decode batch (8 prompts
+of U[1024,8192] tokens in 2 shard rows each plus 56 decode rows with
+U[1024,16384] keys, 32 q / 8 kv heads, D=128): the one workload on which both
+halves of the metric (prefill TFLOP/s and decode-row HBM GB/s) are defined,
+each timed with CUDA events around its own kernel inside the step; the other
+four workloads follow in "workloads".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5] [--kv-cache bf16|fp8]
     python bench.py --impl reference     # the CPU oracle on a bounded sample
@@ -135,49 +136,100 @@ def plan_work(rows: np.ndarray, hq: int, hkv: int, d: int, kv_bytes: int = 2):
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 20 ms) of SM clock and throttle reasons while
-    the timed steps run."""
+    """SM clock, power and clock-event reasons while the timed steps run: read
+    from NVML (ctypes, libnvidia-ml) every millisecond, so a timed region of a
+    few tens of milliseconds still holds tens of samples; without NVML,
+    nvidia-smi every 20 ms. Reading clocks changes no setting."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40}
 
-    def __init__(self, index: int):
-        self.index, self.samples, self.proc = index, [], None
+    def __init__(self, index: int, period_s: float = 0.001):
+        self.index, self.period = index, period_s
+        self.samples, self.proc, self.nvml, self.thread = [], None, None, None
+        self.stop = threading.Event()
+        self.source = "none"
+
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            return None
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        lib.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+        return lib, h, reasons
+
+    def _nvml_loop(self):
+        import ctypes
+        lib, h, reasons = self.nvml
+        clk, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            ok = lib.nvmlDeviceGetClockInfo(h, ctypes.c_int(1), ctypes.byref(clk)) == 0
+            lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+            if reasons(h, ctypes.byref(rs)) != 0:
+                rs.value = 0
+            if ok:
+                self.samples.append((float(clk.value), self.max_mhz, pw.value / 1000.0, int(rs.value)))
+            time.sleep(self.period)
 
     def __enter__(self):
+        try:
+            self.nvml = self._nvml_open()
+        except Exception:
+            self.nvml = None
+        if self.nvml is not None:
+            self.source = "nvml 1 ms"
+            self.thread = threading.Thread(target=self._nvml_loop, daemon=True)
+            self.thread.start()
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread = threading.Thread(target=self._smi_read, daemon=True)
             self.thread.start()
+            self.source = "nvidia-smi 20 ms"
         except Exception:
             self.proc = None
         return self
 
-    def _read(self):
+    def _smi_read(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 8:
-                self.samples.append(parts)
+            if len(parts) >= 8 and parts[0].replace(".", "").isdigit():
+                bits = sum(self.REASON_BITS[n] for i, n in enumerate(names) if parts[4 + i].lower() == "active")
+                mx = float(parts[1]) if parts[1].replace(".", "").isdigit() else 0.0
+                self.samples.append((float(parts[0]), mx, 0.0, bits))
 
     def __exit__(self, *a):
+        self.stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
 
     def summary(self):
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
-        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[4 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.samples)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [x[0] for x in self.samples]
+        reasons = sorted({n for x in self.samples for n, b in self.REASON_BITS.items() if x[3] & b})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(x[1] for x in self.samples),
+                "reasons": reasons, "samples": len(self.samples), "source": self.source,
+                "power_w_max": round(max(x[2] for x in self.samples), 1)}
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -211,6 +263,168 @@ def time_lse_merge(P, total_q: int, hq: int, d: int, device: str, stream, flush,
     return statistics.mean(times)
 
 
+def config_of(spec, n_rows: int, flags: int, kv_fp8: bool) -> dict:
+    """The workload description both arms print (same keys, same values)."""
+    return {"workload": spec.name + ("-fp8kv" if kv_fp8 else ""), "rows": int(n_rows), "total_q": spec.total_q,
+            "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
+            "block_size": spec.block_size, "num_shards": spec.num_shards, "flags": int(flags),
+            "kv_cache": "fp8-e4m3" if kv_fp8 else "bf16"}
+
+
+def _mk(timing: bool = True):
+    return torch.cuda.Event(enable_timing=timing)
+
+
+def _live_events(n: int, stream):
+    """n timing events whose CUDA events exist (torch creates one at its first
+    record), so that their handles can be given to the library."""
+    ev = [_mk() for _ in range(n)]
+    for e in ev:
+        e.record(stream)
+    return ev
+
+
+def time_rows(P, step, q, kc, vc, bt_dev, rows_np, scale, stream, flush, iters: int = 5):
+    """pcp_attn_varlen over a subset of the plan's rows (same data, same
+    workspace), the L2 flushed before each call. Returns the mean ms of the
+    prefill kernel and of the decode kernels (split-KV pass and merge)."""
+    rows = torch.from_numpy(np.ascontiguousarray(rows_np)).to(q.device)
+    T, hq = q.shape[0], q.shape[1]
+    out = step.out[:T]
+    lse = step.lse_buf[:T * hq].view(hq, T)
+
+    def call():
+        if step.kv_fp8:
+            R = int(bt_dev.shape[0])
+            P.pcp_attn_varlen_fp8kv(q, kc, vc, step.k_descale[:R], step.v_descale[:R], bt_dev, rows, scale,
+                                    out=out, lse=lse, workspace=step.workspace, flags=step.flags,
+                                    status=step.status, stream=stream)
+        else:
+            P.pcp_attn_varlen(q, kc, vc, bt_dev, rows, scale, out=out, lse=lse, workspace=step.workspace,
+                              flags=step.flags, status=step.status, stream=stream)
+
+    for _ in range(2):
+        call()
+    pre, dec = [], []
+    for i in range(iters):
+        ev = _live_events(4, stream)
+        flush.fill_(i & 0xFF)
+        P.pcp_set_profile_events(*ev)
+        call()
+        P.pcp_set_profile_events()
+        torch.cuda.synchronize()
+        pre.append(ev[0].elapsed_time(ev[1]))
+        dec.append(ev[2].elapsed_time(ev[3]))
+    step.check_status()
+    return statistics.mean(pre), statistics.mean(dec)
+
+
+def time_e2e(P, spec, bt, bt_dev, kc, vc, q, k, v, steps2, stream, iters: int):
+    """The step end to end from pinned host memory: each step's q, k, v and plan
+    copied in, and its out and lse copied back, inside the timed region. Two
+    buffer sets alternate so that step i + 1's uploads (on a copy-in stream)
+    and step i - 1's downloads (on a copy-out stream) run under step i's
+    kernels; the kernels stay in order on the compute stream (the cache write of
+    step i + 1 after the attention of step i). Returns (ms per step, H2D bytes,
+    D2H bytes per step)."""
+    dev = q.device
+    cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    host = [x.cpu().pin_memory() for x in (q, k, v)]
+    bufs = [(q, k, v), tuple(torch.empty_like(x) for x in (q, k, v))]
+    out_h = [torch.empty(tuple(q.shape), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    lse_h = [torch.empty((spec.num_q_heads, spec.total_q), dtype=torch.float32).pin_memory() for _ in range(2)]
+    ev_in = [_mk(False), _mk(False)]
+    ev_comp = [_mk(False), _mk(False)]
+    ev_out = [_mk(False), _mk(False)]
+
+    def run(n, t0=None, t1=None):
+        torch.cuda.synchronize()
+        if t0 is not None:
+            t0.record(cin)
+        for i in range(n):
+            b = i % 2
+            st = steps2[b]
+            if i >= 2:
+                ev_in[b].synchronize()  # the pinned plan staging of buffer set b is free again
+            st.build_plan(spec.query_len, spec.num_computed, bt)
+            with torch.cuda.stream(cin):
+                if i >= 2:
+                    cin.wait_event(ev_comp[b])  # step i - 2 has consumed buffer set b
+                for d, h in zip(bufs[b], host):
+                    d.copy_(h, non_blocking=True)
+                st.upload_plan(cin)
+                ev_in[b].record(cin)
+            stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_out[b])  # step i - 2's result has left buffer set b
+            st.write_cache(bufs[b][1], bufs[b][2], kc, vc, stream)
+            out, lse = st.attend(bufs[b][0], kc, vc, bt_dev, spec.scale, stream)
+            ev_comp[b].record(stream)
+            with torch.cuda.stream(cout):
+                cout.wait_event(ev_comp[b])
+                out_h[b].copy_(out, non_blocking=True)
+                lse_h[b].copy_(lse, non_blocking=True)
+                ev_out[b].record(cout)
+        if t1 is not None:
+            cout.wait_event(ev_out[(n - 1) % 2])
+            t1.record(cout)
+        torch.cuda.synchronize()
+
+    run(4)
+    t0, t1 = _mk(), _mk()
+    run(iters, t0, t1)
+    plan = steps2[0].plan
+    h2d = sum(x.numel() * x.element_size() for x in host) + plan["rows"].nbytes + plan["slot_mapping"].nbytes
+    d2h = out_h[0].numel() * 2 + lse_h[0].numel() * 4
+    return t0.elapsed_time(t1) / iters, int(h2d), int(d2h)
+
+
+def make_step(P, spec, bt, device, flags, kv_fp8):
+    return P.PcpStep(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                     block_size=spec.block_size, num_shards=spec.num_shards, split_mode=spec.split_mode,
+                     max_tokens=spec.total_q, max_reqs=spec.num_reqs, max_kv_len=bt.shape[1] * spec.block_size,
+                     flags=flags, device=device, kv_cache_dtype="fp8" if kv_fp8 else "bf16",
+                     k_scale=W.FP8_K_SCALE, v_scale=W.FP8_V_SCALE)
+
+
+def workload_line(P, workload: int, device: str, flags: int, kv_fp8: bool, flush, stream, peaks, local: int,
+                  steps: int = 10):
+    """Prefill TFLOP/s (attention kernel over the prefill rows), decode GB/s
+    (over the decode rows, where the workload has some) and the step time of
+    one more workload, with its own clock record."""
+    P, spec, bt, bt_dev, kc, vc, q, k, v, step = setup(workload, device, flags, kv_fp8)
+    plan = step.build_plan(spec.query_len, spec.num_computed, bt)
+    rows = plan["rows"]
+    kvb = 1 if kv_fp8 else 2
+    work = plan_work(rows, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, kvb)
+    for _ in range(3):
+        step.run(q, k, v, kc, vc, bt_dev, spec.scale, stream)
+    torch.cuda.synchronize()
+    st = []
+    with ClockSampler(local) as clocks:
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            e0, e1 = _mk(), _mk()
+            e0.record(stream)
+            step.build_plan(spec.query_len, spec.num_computed, bt)
+            step.run(q, k, v, kc, vc, bt_dev, spec.scale, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            st.append(e0.elapsed_time(e1))
+        dec = rows[:, 7] == 1
+        out = {"name": spec.name + ("-fp8kv" if kv_fp8 else ""), "step_ms": round(statistics.mean(st), 4)}
+        pms, dms = time_rows(P, step, q, kc, vc, bt_dev, rows, spec.scale, stream, flush)
+        if (~dec).any():
+            tf = work["prefill_flop"] / (pms * 1e-3) / 1e12
+            out["prefill"] = {"tflops": round(tf, 2), "ms": round(pms, 4), "frac_bf16_peak": round(tf / peaks["bf16"], 4)}
+        if dec.any():
+            gbs = work["decode_bytes"] / (dms * 1e-3) / 1e9
+            out["decode"] = {"gbs": round(gbs, 1), "ms": round(dms, 4), "frac_hbm_peak": round(gbs / peaks["hbm"], 4)}
+    out["clocks"] = clocks.summary()
+    step.check_status()
+    return out
+
+
 def setup(workload: int, device: str, flags: int, kv_fp8: bool = False):
     import context_prefill_attention_gb300 as P
     P.load()
@@ -229,11 +443,7 @@ def setup(workload: int, device: str, flags: int, kv_fp8: bool = False):
     q = W.packed_new_tokens(spec, W.KIND_Q, device)
     k = W.packed_new_tokens(spec, W.KIND_K, device)
     v = W.packed_new_tokens(spec, W.KIND_V, device)
-    step = P.PcpStep(num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
-                     block_size=spec.block_size, num_shards=spec.num_shards, split_mode=spec.split_mode,
-                     max_tokens=spec.total_q, max_reqs=spec.num_reqs, max_kv_len=bt.shape[1] * spec.block_size,
-                     flags=flags, device=device, kv_cache_dtype="fp8" if kv_fp8 else "bf16",
-                     k_scale=W.FP8_K_SCALE, v_scale=W.FP8_V_SCALE)
+    step = make_step(P, spec, bt, device, flags, kv_fp8)
     return P, spec, bt, bt.to(device), kc, vc, q, k, v, step
 
 
@@ -245,10 +455,12 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     device = f"cuda:{local}"
     kv_fp8 = args.kv_cache == "fp8"
+    kvb = 1 if kv_fp8 else 2
     P, spec, bt, bt_dev, kc, vc, q, k, v, step = setup(args.workload, device, args.flags, kv_fp8)
     workload_name = spec.name + ("-fp8kv" if kv_fp8 else "")
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    peaks = load_peaks()
 
     def one_step(write_events=None):
         # PcpStep.run's three steps, with optional events around the cache write
@@ -262,14 +474,15 @@ def run_gpu(args):
         return step.attend(q, kc, vc, bt_dev, spec.scale, stream)
 
     plan = step.build_plan(spec.query_len, spec.num_computed, bt)
-    work = plan_work(plan["rows"], spec.num_q_heads, spec.num_kv_heads, spec.head_dim, 1 if kv_fp8 else 2)
+    rows = plan["rows"]
+    work = plan_work(rows, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, kvb)
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize()
     step.check_status()
 
-    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    ev = [[mk() for _ in range(8)] for _ in range(args.steps)]
+    # ---- the timed region: exactly K steps, the L2 flushed between them
+    ev = [[_mk() for _ in range(8)] for _ in range(args.steps)]
     for e in ev:
         for x in e:
             x.record(stream)
@@ -278,7 +491,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)  # L2 flush between timed steps, outside the timed window
+            flush.fill_(i & 0xFF)
             P.pcp_set_profile_events(ev[i][2], ev[i][3], ev[i][4], ev[i][5])
             ev[i][0].record(stream)
             one_step(ev[i][6:8])
@@ -288,61 +501,46 @@ def run_gpu(args):
     barrier(ws)
     step.check_status()
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    pre_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    dec_ms = [e[4].elapsed_time(e[5]) for e in ev]
+    pre_ms = [e[2].elapsed_time(e[3]) for e in ev]        # the prefill kernel (prefill rows)
+    dec_ms = [e[4].elapsed_time(e[5]) for e in ev]        # the decode kernels (decode rows)
     write_ms = [e[6].elapsed_time(e[7]) for e in ev]
     total_ms = max_over_ranks(sum(step_ms), ws)
     ms = total_ms / args.steps
     step_flop = work["prefill_flop"] + work["decode_flop"]
     value = ws * step_flop / (ms * 1e-3) / 1e12
+    pre_avg = statistics.mean(pre_ms)
+    achieved = work["prefill_flop"] / (pre_avg * 1e-3) / 1e12
+    write_avg = statistics.mean(write_ms)
+    write_gbs = work["write_bytes"] / (write_avg * 1e-3) / 1e9 if write_avg > 0 else None
+    dec = rows[:, 7] == 1
+    dec_line = None
+    if dec.any():
+        dec_avg = statistics.mean(dec_ms)
+        dec_gbs = work["decode_bytes"] / (dec_avg * 1e-3) / 1e9
+        dec_line = {"gbs": round(dec_gbs, 1), "ms": round(dec_avg, 4), "frac_hbm_peak": round(dec_gbs / peaks["hbm"], 4),
+                    "bytes": work["decode_bytes"]}
 
-    # end to end: host inputs in pinned memory, copies inside the timed region
-    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
-    out_h = torch.empty((spec.total_q, spec.num_q_heads, spec.head_dim), dtype=torch.bfloat16).pin_memory()
-    lse_h = torch.empty((spec.num_q_heads, spec.total_q), dtype=torch.float32).pin_memory()
-    e2e_ms = []
-    for i in range(max(3, args.steps // 2)):
-        flush.fill_(i & 0xFF)
-        s0, s1 = mk(), mk()
-        s0.record(stream)
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        out, lse = one_step()
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
-        s1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms.append(s0.elapsed_time(s1))
-    e2e = max_over_ranks(statistics.mean(e2e_ms), ws)
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv)) + plan["rows"].nbytes + plan["slot_mapping"].nbytes
-    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    # ---- end to end from pinned host buffers, copies overlapped with the kernels
+    step2 = make_step(P, spec, bt, device, args.flags, kv_fp8)
+    if kv_fp8:
+        step2.k_descale.copy_(step.k_descale)
+        step2.v_descale.copy_(step.v_descale)
+    e2e, h2d, d2h = time_e2e(P, spec, bt, bt_dev, kc, vc, q, k, v, [step, step2], stream, max(8, args.steps))
+    e2e = max_over_ranks(e2e, ws)
+    del step2
 
     merge_ms = time_lse_merge(P, spec.total_q, spec.num_q_heads, spec.head_dim, device, stream, flush)
     merge_b = merge_bytes(spec.total_q, spec.num_q_heads, spec.head_dim)
 
-    peaks = load_peaks()
-    pre_avg = statistics.mean(pre_ms)
-    dec_avg = statistics.mean(dec_ms)
-    achieved = work["prefill_flop"] / (pre_avg * 1e-3) / 1e12
-    dec_gbs = work["decode_bytes"] / (dec_avg * 1e-3) / 1e9 if work["decode_bytes"] > 0 and dec_avg > 0 else None
-    write_avg = statistics.mean(write_ms)
-    write_gbs = work["write_bytes"] / (write_avg * 1e-3) / 1e9 if write_avg > 0 else None
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded torch.randn, bf16)",
-        "config": {"workload": workload_name, "rows": int(plan["rows"].shape[0]), "total_q": spec.total_q,
-                   "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
-                   "head_dim": spec.head_dim, "block_size": spec.block_size, "num_shards": spec.num_shards,
-                   "flags": args.flags, "kv_cache": "fp8-e4m3" if kv_fp8 else "bf16",
-                   "l2": "flushed (512 MiB write) between timed steps",
-                   "parallelism": f"replicas x{ws}"},
+        "config": config_of(spec, rows.shape[0], args.flags, kv_fp8),
+        "l2": "flushed (512 MiB write) between timed steps", "parallelism": f"replicas x{ws}",
         "prefill": {"tflops": round(achieved, 2), "ms": round(pre_avg, 4),
                     "frac_bf16_peak": round(achieved / peaks["bf16"], 4), "flop": work["prefill_flop"]},
-        "decode": {"gbs": None if dec_gbs is None else round(dec_gbs, 1), "ms": round(dec_avg, 4),
-                   "frac_hbm_peak": None if dec_gbs is None else round(dec_gbs / peaks["hbm"], 4),
-                   "bytes": work["decode_bytes"]},
+        "decode": dec_line,
         "cache_write": {"gbs": None if write_gbs is None else round(write_gbs, 1), "ms": round(write_avg, 4),
                         "frac_hbm_peak": None if write_gbs is None else round(write_gbs / peaks["hbm"], 4),
                         "bytes": work["write_bytes"]},
@@ -351,13 +549,25 @@ def run_gpu(args):
                       "bytes": merge_b, "timed": "pcp_lse_merge alone on the step's [T, Hq, D] partials"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16"],
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
-                     "traffic": measured_traffic(workload_name),
-                     "kernel": "prefill_kernel", "peak_source": f"{peaks['source']} bf16 burst"},
+                     "traffic": measured_traffic(workload_name), "kernel": "prefill_kernel",
+                     "peak_source": f"{peaks['source']} bf16 burst"},
         "e2e": {"value": round(ws * step_flop / (e2e * 1e-3) / 1e12, 3), "unit": UNIT,
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e, 4)},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e, 4),
+                "host_link_gbs": round((h2d + d2h) / (e2e * 1e-3) / 1e9, 1),
+                "timed": "pinned host buffers, two buffer sets, copies on their own streams"},
         "gpu_launches": args.steps * (5 + (1 if args.flags & 1 else 0)),
         "clocks": clocks.summary(),
     }
+    del q, k, v, kc, vc, step
+    torch.cuda.empty_cache()
+    if not args.headline_only:
+        others = {}
+        for w in (1, 2, 3, 4, 5):
+            if w == args.workload:
+                continue
+            others[str(w)] = workload_line(P, w, device, args.flags, kv_fp8, flush, stream, peaks, local)
+            torch.cuda.empty_cache()
+        line["workloads"] = others
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, bt, target_s=args.cpu_seconds, kv_fp8=kv_fp8)
     if rank == 0:
@@ -431,6 +641,9 @@ def run_reference(args):
     spec = W.workload_spec(args.workload)
     bt, _ = W.block_tables(spec)
     kv_fp8 = args.kv_cache == "fp8"
+    import oracle as O
+    n_rows = O.row_plan(spec.query_len, spec.num_computed, bt.numpy(), spec.block_size, spec.num_shards,
+                        spec.split_mode)["rows"].shape[0]
     per_step = max(1.0, args.ref_seconds / (args.steps + args.warmup))
     for i in range(args.warmup):
         _oracle_sample(spec, bt, per_step, spec.seed + 1000 + i, kv_fp8)
@@ -445,9 +658,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded torch.randn, bf16)",
-            "config": {"workload": spec.name + ("-fp8kv" if kv_fp8 else ""), "total_q": spec.total_q,
-                       "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
-                       "head_dim": spec.head_dim, "kv_cache": "fp8-e4m3" if kv_fp8 else "bf16"},
+            "config": config_of(spec, n_rows, args.flags, kv_fp8),
             "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": f"per step: {desc}"},
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -464,6 +675,7 @@ def main():
     ap.add_argument("--kv-cache", default="bf16", choices=["bf16", "fp8"])
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true", help="skip the other four workloads")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     args = ap.parse_args()
