@@ -17,7 +17,8 @@ write with the layer scales, attention with per-(request, kv head) descales).
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (no data-path collective); rank 0 prints the line, value = all ranks' work /
-the slowest rank's time.
+the slowest rank's time. ``--mode pcp`` instead splits one batch over the N
+ranks, one PCP shard each, with the all-gather of the new tokens' K/V.
 """
 from __future__ import annotations
 
@@ -577,6 +578,110 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_pcp(args):
+    """The multi-GPU PCP step: rank i of N owns shard i of the batch's rows
+    (num_shards = N), writes its own tokens' K/V, all-gathers the new tokens'
+    K/V over the process group and writes the others', then attends its own
+    rows (context_prefill_attention_gb300/ranks.py). The batch is fixed, so
+    the scaling is strong; value = the batch's FLOPs / the slowest rank's step.
+    With N = 1 the same path runs with the gather of a single rank."""
+    import dataclasses
+    from context_prefill_attention_gb300 import ranks as R
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        gather = R.dist_all_gather()
+    else:
+        gather = lambda x: [x]  # noqa: E731
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    P, spec, bt, bt_dev, kc, vc, q, k, v, _ = setup(args.workload, device, args.flags)
+    spec = dataclasses.replace(spec, num_shards=ws)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    peaks = load_peaks()
+    pr = R.PcpRank(rank, ws, num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                   block_size=spec.block_size, split_mode=spec.split_mode, max_tokens=spec.total_q,
+                   max_reqs=spec.num_reqs, max_kv_len=bt.shape[1] * spec.block_size, gather=gather,
+                   flags=args.flags, device=device)
+    plan = pr.build_plan(spec.query_len, spec.num_computed, bt)
+    own = torch.from_numpy(pr.own).to(device)
+    q_own, k_own, v_own = q[own].contiguous(), k[own].contiguous(), v[own].contiguous()
+    del q, k, v
+    work = plan_work(plan["rows"], spec.num_q_heads, spec.num_kv_heads, spec.head_dim)
+    mine = plan_work(pr.rows_host, spec.num_q_heads, spec.num_kv_heads, spec.head_dim)
+
+    def one_step():
+        pr.build_plan(spec.query_len, spec.num_computed, bt)
+        return pr.step(q_own, k_own, v_own, kc, vc, bt_dev, spec.scale, stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    pr.check_status()
+    ev = [_live_events(4, stream) for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            P.pcp_set_profile_events(ev[i][2], ev[i][3])
+            ev[i][0].record(stream)
+            one_step()
+            ev[i][1].record(stream)
+        P.pcp_set_profile_events()
+        torch.cuda.synchronize()
+    barrier(ws)
+    pr.check_status()
+    ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in ev), ws) / args.steps
+    pre_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    step_flop = work["prefill_flop"] + work["decode_flop"]
+    achieved = mine["prefill_flop"] / (pre_ms * 1e-3) / 1e12 if mine["prefill_flop"] > 0 else 0.0
+
+    # end to end: this rank's q, k, v from pinned host memory in, its out and lse back
+    hq_, hk_, hv_ = (x.cpu().pin_memory() for x in (q_own, k_own, v_own))
+    n_own = int(q_own.shape[0])
+    out_h = torch.empty((n_own, spec.num_q_heads, spec.head_dim), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((spec.num_q_heads, n_own), dtype=torch.float32).pin_memory()
+    e2e_ms = []
+    for i in range(max(3, args.steps // 2)):
+        flush.fill_(i & 0xFF)
+        s0, s1 = _mk(), _mk()
+        s0.record(stream)
+        q_own.copy_(hq_, non_blocking=True)
+        k_own.copy_(hk_, non_blocking=True)
+        v_own.copy_(hv_, non_blocking=True)
+        out, lse = one_step()
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(s0.elapsed_time(s1))
+    e2e = max_over_ranks(statistics.mean(e2e_ms), ws)
+    h2d = sum(x.numel() * x.element_size() for x in (hq_, hk_, hv_))
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    line = {
+        "metric": METRIC, "value": round(step_flop / (ms * 1e-3) / 1e12, 3), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded torch.randn, bf16)",
+        "config": config_of(spec, plan["rows"].shape[0], args.flags, False),
+        "l2": "flushed (512 MiB write) between timed steps", "parallelism": f"pcp x{ws} (one shard per rank)",
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16"], 4), "traffic": None, "kernel": "prefill_kernel",
+                     "peak_source": f"{peaks['source']} bf16 burst", "rank": rank},
+        "e2e": {"value": round(step_flop / (e2e * 1e-3) / 1e12, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e, 4)},
+        "gpu_launches": args.steps * 6,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ---------------------------------------------------------------- CPU oracle
 
 def _oracle_sample(spec, bt, target_s: float, seed: int, kv_fp8: bool = False):
@@ -676,6 +781,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true", help="skip the other four workloads")
+    ap.add_argument("--mode", default="replicas", choices=["replicas", "pcp"],
+                    help="N GPUs: independent replicas, or one PCP shard per rank with the K/V all-gather")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     args = ap.parse_args()
@@ -683,6 +790,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.mode == "pcp":
+        run_pcp(args)
     else:
         run_gpu(args)
 
