@@ -34,8 +34,10 @@
 //    in the status word and the CTA winds down, freeing its TMEM;
 //  * FP8 (e4m3) cache: the producer's TMA brings the codes in (for D = 128 into
 //    the upper half of the stage they will be converted into, for D = 64 into
-//    a staging area), warps 10-11 convert them to bf16 in the 128-byte-swizzled
-//    layout the MMA reads (exact: every e4m3 value is a bf16 value), and the
+//    a staging area), warps 10-11 convert them to f16 in the 128-byte-swizzled
+//    layout the MMA reads (one conversion per two codes, exact: every e4m3 value
+//    is an f16 value) and each item's Q tiles from bf16 to f16 in place, so the
+//    MMAs of this variant take f16 operands (P is stored as f16 too); the
 //    per-(request, kv head) descales fold into the softmax scale (K) and the
 //    epilogue's normalisation (V).
 #include <cuda.h>
@@ -111,14 +113,16 @@ struct Cfg {
     __host__ __device__ static constexpr int code_v(int s) {
         return kInPlace ? kV + s * kTileBytes + kHalfBytes : kCV + s * kCodeBytes;
     }
-    static constexpr int kNumBars = 2 + 2 * kNK + 2 * kNV + 8 + kNK + kNV;
+    static constexpr int kNumBars = 2 + 2 * kNK + 2 * kNV + 8 + kNK + kNV + 1;  // + FP8: Q landed
     static constexpr int kMisc = kBar + kNumBars * 8;      // tmem address, abort flag, item ring
     static constexpr int kSmem = kMisc + 16 + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 512;
     __host__ __device__ static constexpr uint32_t tmem_s(int g) { return g ? 128u : 0u; }
     __host__ __device__ static constexpr uint32_t tmem_o(int g) { return g ? 256u + D : 256u; }
-    static constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
-    static constexpr uint32_t kIdescO = idesc_bf16(128, D, false, true);
+    // FP8 cache: the codes are widened to f16 (exact), q converted to f16 and P
+    // stored as f16, so the MMAs take f16 operands; bf16 cache: bf16 operands
+    static constexpr uint32_t kIdescS = F8 ? idesc_f16(128, 128, false, false) : idesc_bf16(128, 128, false, false);
+    static constexpr uint32_t kIdescO = F8 ? idesc_f16(128, D, false, true) : idesc_bf16(128, D, false, true);
 };
 
 struct Item {
@@ -192,8 +196,8 @@ __device__ __forceinline__ void convert_codes(const uint8_t* codes, uint8_t* dst
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
             const int r = r0 + kRpp * b + rsub;
-            const uint2 w0 = e4m3x4_to_bf16x4(c[b].x), w1 = e4m3x4_to_bf16x4(c[b].y);
-            const uint2 w2 = e4m3x4_to_bf16x4(c[b].z), w3 = e4m3x4_to_bf16x4(c[b].w);
+            const uint2 w0 = e4m3x4_to_f16x4(c[b].x), w1 = e4m3x4_to_f16x4(c[b].y);
+            const uint2 w2 = e4m3x4_to_f16x4(c[b].z), w3 = e4m3x4_to_f16x4(c[b].w);
             const uint4 lo = make_uint4(w0.x, w0.y, w1.x, w1.y);  // dims 16t .. 16t+7
             const uint4 hi = make_uint4(w2.x, w2.y, w3.x, w3.y);  // dims 16t+8 .. 16t+15
             uint8_t* row = dst + h * (128 * 128) + r * 128;
@@ -205,27 +209,49 @@ __device__ __forceinline__ void convert_codes(const uint8_t* codes, uint8_t* dst
     }
 }
 
+// The bf16 Q tiles of an item (nslots x kTileBytes bytes from q_base) turned
+// into f16 in place, by the 64 converter threads (ct = 0..63): each 16-byte
+// chunk holds 8 elements whatever the swizzle, so the conversion is
+// elementwise. Values beyond the largest finite f16 saturate to it; the
+// return value says whether any did.
+__device__ __forceinline__ bool convert_q_f16(uint8_t* q_base, int bytes, int ct) {
+    bool over = false;
+#pragma unroll 4
+    for (int off = ct * 16; off < bytes; off += kConvThreads * 16) {
+        uint4 w = *reinterpret_cast<const uint4*>(q_base + off);
+        uint32_t* e = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float lo = __uint_as_float(e[i] << 16), hi = __uint_as_float(e[i] & 0xFFFF0000u);
+            over |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+            e[i] = pack_f16x2_satfinite(lo, hi);
+        }
+        *reinterpret_cast<uint4*>(q_base + off) = w;
+    }
+    return over;
+}
+
 // S = Q_slot K^T over D (K-major A and B, 128-byte swizzle). q_desc / k_desc are
 // the descriptors of the tiles' first k-step; a later k-step only moves the start
 // address (the descriptor's low 14 bits, in 16-byte units), so each MMA costs one
 // add of a constant (the issuing thread's instruction count per MMA is on the
 // critical path of the tensor pipe).
-template <int D>
+template <int D, bool F8>
 __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint64_t q_desc, uint64_t k_desc) {
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
         const uint32_t off = ((ks / 4) * Cfg<D>::kHalfBytes + (ks % 4) * 32) >> 4;
-        mma_ss(tmem_s, q_desc + off, k_desc + off, Cfg<D>::kIdescS, ks > 0 ? 1u : 0u);
+        mma_ss(tmem_s, q_desc + off, k_desc + off, Cfg<D, F8>::kIdescS, ks > 0 ? 1u : 0u);
     }
 }
 
 // O (+)= P V: P from TMEM (bf16 pairs in the S columns), V MN-major in shared
 // memory (v_desc: the descriptor of the tile's first 16 keys).
-template <int D>
+template <int D, bool F8>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc, bool accumulate) {
 #pragma unroll
     for (int ks = 0; ks < kBlockN / 16; ++ks)
-        mma_ts(tmem_o, tmem_p + ks * 8, v_desc + (uint32_t)(ks * 2048 >> 4), Cfg<D>::kIdescO,
+        mma_ts(tmem_o, tmem_p + ks * 8, v_desc + (uint32_t)(ks * 2048 >> 4), Cfg<D, F8>::kIdescO,
                (accumulate || ks > 0) ? 1u : 0u);
 }
 
@@ -253,6 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // FP8: the codes of K / V stage s have landed
     auto kc_full = [&](int s) { return bx + 64 + 8 * s; };
     auto vc_full = [&](int s) { return bx + 64 + 8 * (kNK + s); };
+    // FP8: the bf16 Q tiles have landed (the converters turn them into f16, then arrive on q_full)
+    const uint32_t qc_full = bx + 64 + 8 * (kNK + kNV);
     // bf16: K(j) and V(j) land together on v_full(stage of V(j)), so the MMA
     // issuer reads one barrier per tile for both (every barrier read by the issuer
     // costs tensor-pipe time); FP8: the converters fill k_full and v_full apart
@@ -268,7 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t bs = a.block_size;
 
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
+        mbar_init(q_full, F8 ? kConvThreads / 32 : 1);
+        if (F8) mbar_init(qc_full, 1);
         mbar_init(q_empty, 1);
         // FP8: a stage is full when both converter warps have arrived
         const uint32_t fill_count = F8 ? kConvThreads / 32 : 1;
@@ -333,11 +362,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (it.n_tiles == 0) continue;
             if (c > 0 && !(ok = mbar_wait_warp(q_empty, (c - 1) & 1, abort_flag))) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(q_full, it.nslots * C::kTileBytes);
+                const uint32_t qbar = F8 ? qc_full : q_full;
+                mbar_arrive_expect_tx(qbar, it.nslots * C::kTileBytes);
                 for (int g = 0; g < it.nslots; ++g)
                     for (int h = 0; h < C::kHalves; ++h)
                         tma_load_3d(sbase + C::kQ + g * C::kTileBytes + h * C::kHalfBytes, &tm_q,
-                                    q_full, h * 64, it.h0 + g, it.q_tok0);
+                                    qbar, h * 64, it.h0 + g, it.q_tok0);
             }
             const int32_t* table = a.block_table + (size_t)it.req * a.max_blocks;
             for (int32_t j = 0; j < it.n_tiles && ok; ++j) {
@@ -396,12 +426,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // for the codes, convert them to bf16 in place, make the generic-proxy
         // stores visible to the tensor cores' async proxy, then mark the stage full.
         const int ct = threadIdx.x - kConvWarp0 * 32;
-        uint32_t kt = 0, vt = 0;
+        uint32_t kt = 0, vt = 0, cq = 0;
         bool ok = true;
         for (int32_t round = 0; ok; ++round) {
             const int32_t idx = item_of_round(round);
             if (idx >= total_items) break;
             const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, a.num_rows, bs);
+            if (it.n_tiles == 0) continue;
+            // the item's Q tiles: bf16 -> f16 in place, then ready for the MMAs
+            if (!(ok = mbar_wait_warp(qc_full, cq & 1, abort_flag))) break;
+            ++cq;
+            if (__any_sync(0xffffffffu, convert_q_f16(smem + C::kQ, it.nslots * C::kTileBytes, ct)) && lane == 0)
+                report_status(a.status, PCP_ERR_RANGE);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_full);
             for (int32_t j = 0; j < it.n_tiles && ok; ++j) {
                 const int ks = kt % kNK;
                 if (!(ok = mbar_wait_warp(kc_full(ks), (kt / kNK) & 1, abort_flag))) break;
@@ -452,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             tc_fence_after();
             for (int g = 0; g < it.nslots; ++g) {
-                issue_qk<D>(tmem + C::tmem_s(g), g ? qd1 : qd0, k_desc(ks));
+                issue_qk<D, F8>(tmem + C::tmem_s(g), g ? qd1 : qd0, k_desc(ks));
                 mma_commit(s_full(g));
             }
             ++kt;
@@ -480,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     pph[g] ^= 1;
-                    issue_pv<D>(tmem + C::tmem_o(g), tmem + C::tmem_s(g), v_desc(vs), j > 0);
+                    issue_pv<D, F8>(tmem + C::tmem_o(g), tmem + C::tmem_s(g), v_desc(vs), j > 0);
                     if (j + 1 < n) {
                         if (g == 0) {
                             // K(j + 1) (bf16: with V(j + 1))
@@ -490,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 break;
                             tc_fence_after();
                         }
-                        issue_qk<D>(tmem + C::tmem_s(g), g ? qd1 : qd0, k_desc(ks));
+                        issue_qk<D, F8>(tmem + C::tmem_s(g), g ? qd1 : qd0, k_desc(ks));
                         mma_commit(s_full(g));
                         if (g == it.nslots - 1) ++kt;
                     } else {
@@ -590,11 +629,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c2 = 0; c2 < 64; ++c2) {
                         const float2 e = exp_pair(ffma2(make_float2(sf[2 * c2], sf[2 * c2 + 1]), sl2v, nmu), c2);
                         acc[c2 % 4] = fadd2(acc[c2 % 4], e);
-                        p[c2] = pack_bf16x2(e.x, e.y);
+                        p[c2] = F8 ? pack_f16x2(e.x, e.y) : pack_bf16x2(e.x, e.y);
                     }
                     const float2 a03 = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
                     const float ts = a03.x + a03.y;
-                    if (!__any_sync(0xffffffffu, !(ts < kMaxFreeLimit))) {
+                    // f16 P (FP8 cache) must stay below 65504: a lower limit there
+                    if (!__any_sync(0xffffffffu, !(ts < (F8 ? 32768.0f : kMaxFreeLimit)))) {
                         tmem_st32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
                         tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
                         tmem_wait_st();
@@ -663,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int c2 = half * 32 + c3;
                         const float2 e = exp_pair(ffma2(make_float2(sf[2 * c2], sf[2 * c2 + 1]), sl2v, nmu), c2);
                         acc[c2 % 4] = fadd2(acc[c2 % 4], e);
-                        p[c3] = pack_bf16x2(e.x, e.y);
+                        p[c3] = F8 ? pack_f16x2(e.x, e.y) : pack_bf16x2(e.x, e.y);
                     }
                     tmem_st32(t_s + 32 * half, p);
                     if (half == 1) {

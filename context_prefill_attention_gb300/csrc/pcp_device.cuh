@@ -172,6 +172,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
            | ((uint32_t)(M >> 4) << 24);             // M / 16
 }
 
+// Instruction descriptor of kind::f16 with f16 A and B, fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4)                                 // D format: f32
+           | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17)                // N / 8
+           | ((uint32_t)(M >> 4) << 24);             // M / 16
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (the layout TMA writes with
 // CU_TENSOR_MAP_SWIZZLE_128B): 8-row x 128-byte atoms, atom base 1024-aligned.
 // lbo/sbo in bytes: leading and stride byte offsets of the canonical layout.
@@ -322,12 +330,32 @@ __device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float (&f)[4]) {
         : "r"(w));
 }
 
-// Four e4m3 codes -> four bf16 (two packed pairs, element order kept); exact,
-// since every e4m3 value is a bf16 value.
-__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
-    float f[4];
-    e4m3x4_to_f32(w, f);
-    return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+// Four e4m3 codes (byte i of w = element i) -> four f16 (two packed pairs,
+// element order kept); exact, since every e4m3 value is a normal f16 or zero.
+__device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t w) {
+    uint32_t h0, h1;
+    asm("{\n\t.reg .b16 c0, c1;\n\t"
+        "mov.b32 {c0, c1}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, c0;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, c1;\n\t}"
+        : "=r"(h0), "=r"(h1)
+        : "r"(w));
+    return make_uint2(h0, h1);
+}
+
+// Two floats -> two f16 (lo in the low half), round to nearest even,
+// magnitudes beyond the largest finite f16 (65504) saturated to it.
+__device__ __forceinline__ uint32_t pack_f16x2_satfinite(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Two floats -> two f16 (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
 }
 
 // Two floats -> two e4m3 codes (lo in the low byte), round to nearest even,

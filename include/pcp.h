@@ -274,10 +274,13 @@ int pcp_kv_cache_write_fp8(const void* k, const void* v, const int64_t* slot_map
  * cache with per-(request, kv head) descales ("[MRv2] FlashAttention PCP
  * support ...", the context-pass call: descales of shape (num_seqs,
  * num_kv_heads)). Key k of request r and kv head g is code_K[r][k][g][:] *
- * k_descale[r][g], its value code_V[...] * v_descale[r][g]; q stays bf16 and
- * the result is the same attention as pcp_attn_varlen over those keys and
- * values (the codes are widened to bf16 exactly; the descales multiply the
- * fp32 scores and outputs).
+ * k_descale[r][g], its value code_V[...] * v_descale[r][g]; the result is the
+ * same attention as pcp_attn_varlen over those keys and values. The prefill
+ * rows' products run in f16: the codes are widened to f16 exactly, q is
+ * converted from bf16 to f16 (exact for |q| <= 65504; larger elements saturate
+ * to +-65504 and set *status = PCP_ERR_RANGE), and the softmax weights P are
+ * rounded to f16 (finer than the bf16 weights of pcp_attn_varlen); the
+ * descales multiply the fp32 scores and outputs.
  * key_cache, value_cache: [num_blocks][block_size][Hkv][D] bytes (as written
  * by pcp_kv_cache_write_fp8); k_descale, v_descale: device fp32
  * [num_reqs][Hkv] (inputs: out and lse must not overlap them). Every other

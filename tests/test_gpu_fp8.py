@@ -181,3 +181,22 @@ def test_fp8_workload2_matches_oracle():
     tokens = W.sample_segments(segs, 128, spec.seed + 18).numpy()
     eo, el = case.compare(out, lse, tokens)
     assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+
+
+def test_fp8_q_beyond_f16_range_is_reported():
+    """The FP8 path converts q to f16 for the prefill rows' MMAs: an element
+    beyond +-65504 saturates and the call reports PCP_ERR_RANGE; every other
+    row's output still matches the oracle."""
+    P = _P()
+    spec = W.custom_spec([200, 150], [0, 40], num_q_heads=4, num_kv_heads=2, head_dim=128, seed=6550)
+
+    def hook(case):
+        case.q = case.q.clone()
+        case.q[5, 1, 7] = 1.0e5          # token 5 of the first request, q head 1
+    case = Case(spec, kv_fp8=True, inputs_hook=hook)
+    out, lse = case.step.run(case.q_dev, case.k_dev, case.v_dev, case.kc, case.vc, case.bt_dev, spec.scale)
+    torch.cuda.synchronize()
+    assert int(case.step.status.item()) == P.PCP_ERR_RANGE
+    others = np.array([t for t in range(spec.total_q) if t != 5])
+    eo, el = case.compare(out, lse, others)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
