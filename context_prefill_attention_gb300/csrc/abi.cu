@@ -66,6 +66,8 @@ WorkspaceLayout workspace_layout(int32_t num_rows, int32_t total_q, int32_t num_
     o = align256(o + 64 * sizeof(int32_t));
     w.row_ok = o;
     o = align256(o + (size_t)num_rows * sizeof(int32_t));
+    w.dec_pre = o;
+    o = align256(o + ((size_t)num_rows + 1) * sizeof(int32_t));
     w.units = o;
     o = align256(o + (size_t)w.max_units * sizeof(Unit));
     w.units_sorted = o;
@@ -248,6 +250,7 @@ int pcp::attn_call(const void* q, const void* key_cache, const void* value_cache
     a.row_ok = reinterpret_cast<const int32_t*>(ws + w.row_ok);
     a.units = reinterpret_cast<const Unit*>(ws + w.units_sorted);
     a.num_units = reinterpret_cast<const int32_t*>(ws + w.header);
+    a.dec_pre = reinterpret_cast<const int32_t*>(ws + w.dec_pre);
     a.status = status;
     a.k_descale = k_descale;
     a.v_descale = v_descale;
@@ -255,7 +258,8 @@ int pcp::attn_call(const void* q, const void* key_cache, const void* value_cache
     int rc = launch_schedule(a, flags, reinterpret_cast<Unit*>(ws + w.units),
                              reinterpret_cast<Unit*>(ws + w.units_sorted),
                              reinterpret_cast<int32_t*>(ws + w.header),
-                             reinterpret_cast<int32_t*>(ws + w.row_ok), w.max_units, s);
+                             reinterpret_cast<int32_t*>(ws + w.row_ok),
+                             reinterpret_cast<int32_t*>(ws + w.dec_pre), w.max_units, s);
     if (rc != PCP_OK) return rc;
     if (g_profile[2]) cudaEventRecord(g_profile[2], s);
     rc = launch_decode(a, reinterpret_cast<float*>(ws + w.dec_out), reinterpret_cast<float*>(ws + w.dec_lse),

@@ -449,8 +449,13 @@ int launch_decode_dgf(const PrefillArgs& a, float* dec_out, float* dec_lse, int3
                                                                     box_rows);
     e = cudaGetLastError();
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
-    decode_merge_kernel<D><<<dim3(a.num_rows, a.hq), D, 0, stream>>>(a, dec_out, dec_lse, max_splits);
-    e = cudaGetLastError();
+    return PCP_OK;
+}
+
+int launch_merge(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits, cudaStream_t stream) {
+    if (a.d == 64) decode_merge_kernel<64><<<dim3(a.num_rows, a.hq), 64, 0, stream>>>(a, dec_out, dec_lse, max_splits);
+    else decode_merge_kernel<128><<<dim3(a.num_rows, a.hq), 128, 0, stream>>>(a, dec_out, dec_lse, max_splits);
+    const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
     return PCP_OK;
 }
@@ -475,11 +480,19 @@ int launch_decode_d(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_
 
 }  // namespace
 
+#ifndef PCP_DECODE_TC
+#define PCP_DECODE_TC 1  // 1: the tensor-core decode where it applies (head_dim 128, G <= 8)
+#endif
+
 int launch_decode(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
                   cudaStream_t stream) {
-    if (a.d == 64) return launch_decode_d<64>(a, dec_out, dec_lse, max_splits, stream);
-    if (a.d == 128) return launch_decode_d<128>(a, dec_out, dec_lse, max_splits, stream);
-    return PCP_ERR_UNSUPPORTED;
+    if (a.d != 64 && a.d != 128) return PCP_ERR_UNSUPPORTED;
+    int rc = PCP_DECODE_TC ? launch_decode_tc(a, dec_out, dec_lse, max_splits, stream) : PCP_ERR_UNSUPPORTED;
+    if (rc == PCP_ERR_UNSUPPORTED)
+        rc = a.d == 64 ? launch_decode_d<64>(a, dec_out, dec_lse, max_splits, stream)
+                       : launch_decode_d<128>(a, dec_out, dec_lse, max_splits, stream);
+    if (rc != PCP_OK) return rc;
+    return launch_merge(a, dec_out, dec_lse, max_splits, stream);
 }
 
 int launch_separate_merge(const PrefillArgs& a, cudaStream_t stream) {

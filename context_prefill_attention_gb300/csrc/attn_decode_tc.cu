@@ -1,0 +1,747 @@
+// Decode rows of a mixed PCP batch on the 5th-generation tensor cores: one new
+// token attending all keys [0, C) of its request ("[MRv2] FlashAttention PCP
+// support for GQA on MRv2", overview: mixed-batch decode handled next to the
+// prefill rows; "[MRv2][PCP] Carry the row plan ...", "drop pcp_has_prefill":
+// decode rows carried in the same plan).
+//
+// A decode row has one query token, so the q heads of one kv head (G <= 8)
+// are the only other dimension an MMA can take: the kernel computes the
+// transposed products, keys along M:
+//   S^T [128 keys x 16] = K [128 keys x D] . Q^T      (Q^T: the G q heads, padded to 16 rows)
+//   O^T [D x 16]        = V^T [D x 128 keys] . P^T    (P^T: 16 rows, P in rows 0..7 and the
+//                                                      rounding remainder of P in rows 8..15)
+// The bytes of K and V, read once, set the speed; the tensor cores do the
+// products so that the few instructions per key left are the softmax's.
+//
+// Design (sm_103a, head_dim 128, one CTA per SM, persistent):
+//  * work item = (decode row, kv head, split of kDecodeChunk keys); the
+//    scheduler kernel counts them per row (dec_pre), and CTA b takes items b,
+//    b + grid, ...; partial (out, lse) per split as the CUDA-core decode kernel
+//    writes them, merged by decode_merge_kernel;
+//  * warps 8 (K) and 9 (V) produce: per item the block-table entries of its
+//    keys, then per 128-key tile one TMA box per page (bf16: two 64-dim halves,
+//    128-byte swizzled; FP8: the codes, D bytes per row, into the upper half of
+//    the stage), into a 3-stage ring that runs on across items; warp 8 also
+//    loads each item's Q^T (16 q heads of the token from head hk * G, rows past
+//    Hq zero filled);
+//  * lane 0 of warp 10 issues the MMAs from an event loop: S^T of the next tile
+//    once its K is in, O^T of the oldest tile once its P is written, whichever
+//    comes first; commits free the K stage (after S), the V stage (after PV)
+//    and the S and O buffers;
+//  * warps 0-3 and 4-7 are two softmax warpgroups taking alternate tiles, one
+//    thread per key of the tile (TMEM lane) and per dim of O^T: scores -> tile
+//    max per head (a reduce-scatter over the warp, then the warpgroup's four
+//    warps through a named barrier) -> exact online softmax -> P = hi + lo
+//    rounded to 16 bits into shared memory (P^T rows h and 8 + h; the
+//    remainder keeps P's rounding out of the result); each finished tile's O^T
+//    is added into registers with the running rescale; at the end of an item
+//    warpgroup 0 merges the two warpgroups' (max, l, O) and writes the split's
+//    partial;
+//  * FP8 cache: warps 11-14 widen each tile's codes to f16 in place (exact; rows
+//    past the last key written as zeros), and Q^T from bf16 to f16 (saturating;
+//    PCP_ERR_RANGE if a q head's element exceeds 65504), so the MMAs take f16
+//    operands; the K descale scales the scores, the V descale the partial;
+//  * bf16 cache: V rows past a split's last key (unwritten cache slots, or a
+//    stale stage) are zeroed by the softmax threads before the last PV;
+//  * every wait is bounded (PCP_ERR_TIMEOUT); after a timeout the producer
+//    waits, again bounded, for the copies it issued before the CTA exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "pcp_device.cuh"
+#include "pcp_internal.h"
+
+namespace pcp {
+
+namespace {
+
+constexpr int kD = 128;          // head_dim this kernel takes
+constexpr int kKeys = 128;       // keys per tile: the M of S^T
+constexpr int kN = 16;           // the N of both MMAs
+constexpr int kMaxG = 8;         // q heads per kv head: P's hi and lo rows fit N = 16
+constexpr int kStages = 3;       // K/V tiles in flight per CTA
+constexpr int kProdWarp = 8;     // warp 8: K tiles and Q^T; warp 9: V tiles
+constexpr int kMmaWarp = 10;
+constexpr int kConvWarp0 = 11;
+constexpr int kConvWarps = 4;    // FP8 cache only
+constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kMaxPages = kDecodeChunk / 8;  // block-table entries of one split (block_size >= 8)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <bool F8>
+struct TcCfg {
+    static constexpr int kThreads = 32 * (kConvWarp0 + (F8 ? kConvWarps : 0));
+    static constexpr int kHalfBytes = kKeys * 128;      // 128 keys x 64 dims x 2 bytes
+    static constexpr int kTileBytes = 2 * kHalfBytes;   // one K or V tile (16-bit)
+    static constexpr int kStageBytes = 2 * kTileBytes;  // K tile, then V tile
+    static constexpr int kRowsBytes = kN * 128;         // 16 rows x 128 bytes: one 64-element half
+    static constexpr int kQBytes = 2 * kRowsBytes;      // Q^T: 16 rows x 128 dims
+    static constexpr int kPBytes = 2 * kRowsBytes;      // P^T: 16 rows x 128 keys
+    static constexpr int kQ = kStages * kStageBytes;    // two Q^T buffers
+    static constexpr int kP = kQ + 2 * kQBytes;         // two P^T buffers
+    static constexpr int kPre = kP + 2 * kPBytes;       // int32 [kDecTcMaxRows + 1]
+    static constexpr int kPages = kPre + ((kDecTcMaxRows + 1) * 4 + 15) / 16 * 16;
+    static constexpr int kRed = kPages + 2 * kMaxPages * 4;  // (pages: one list per producer warp)  // float [2 wg][2][4][8] maxima, [2][8][8] sums
+    static constexpr int kXchg = kRed + (2 * 2 * 4 * kMaxG + 2 * 8 * kMaxG) * 4;  // float [2][8 + 8 x 128]
+    static constexpr int kBar = kXchg + 2 * (kMaxG + kMaxG * kKeys) * 4;
+    static constexpr int kNumBars = 6 * kStages + 7 * 2;
+    static constexpr int kMisc = kBar + kNumBars * 8;   // TMEM address, abort flag
+    static constexpr int kSmem = kMisc + 16 + 1024;     // + alignment slack
+    static constexpr uint32_t kTmemCols = 64;           // S^T x 2, O^T x 2, 16 columns each
+    static constexpr uint32_t kIdescS = F8 ? idesc_f16(128, kN, false, false) : idesc_bf16(128, kN, false, false);
+    static constexpr uint32_t kIdescO = F8 ? idesc_f16(128, kN, true, false) : idesc_bf16(128, kN, true, false);
+};
+static_assert(TcCfg<true>::kSmem <= 232448 && TcCfg<false>::kSmem <= 232448, "shared memory");
+static_assert(TcCfg<true>::kQ % 1024 == 0 && TcCfg<true>::kP % 1024 == 0, "1024-byte swizzle atoms");
+
+struct DecItem {
+    int32_t ri, req, q_start, hk, split, lo, hi, nt;
+};
+
+// Item p of the decode work list. The caller's items rise, so the row cursor
+// ri only walks forward over the prefix (rows without items are skipped).
+__device__ __forceinline__ DecItem dec_item(const int32_t* pre, int32_t& ri, int32_t p, const pcp_row_t* rows,
+                                            int32_t hkv) {
+    while (pre[ri + 1] <= p) ++ri;
+    const pcp_row_t row = rows[ri];
+    const int32_t nsplit = (row.kv_end + kDecodeChunk - 1) / kDecodeChunk;
+    const int32_t rem = p - pre[ri];
+    DecItem it;
+    it.ri = ri;
+    it.req = row.req;
+    it.q_start = row.q_start;
+    it.hk = rem / nsplit;
+    it.split = rem % nsplit;
+    it.lo = it.split * kDecodeChunk;
+    it.hi = min(row.kv_end, it.lo + kDecodeChunk);
+    it.nt = (it.hi - it.lo + kKeys - 1) / kKeys;
+    (void)hkv;
+    return it;
+}
+
+// One non-blocking look at an mbarrier phase: true if the phase with the given
+// parity has completed.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Named barrier `id` over `n` threads (whole warps).
+__device__ __forceinline__ void bar_sync_named(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Named barrier 3 over the eight softmax warps that also ORs a predicate: every
+// thread gets the same answer, so the warps leave their loops together.
+__device__ __forceinline__ bool bar_all_or(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 3, 256, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+// Max (kMax) or sum over the warp of GP values per lane, by reduce-scatter: each
+// step with offset o = 16, 8, ... halves the values a lane keeps (the upper half
+// where bit o of the lane is set), the remaining offsets reduce the last one.
+// Lane l ends with head l / (32 / GP) reduced over all 32 lanes.
+template <int GP, bool kMax>
+__device__ __forceinline__ float warp_scatter(const float (&x)[GP], int lane) {
+    float v[GP];
+#pragma unroll
+    for (int h = 0; h < GP; ++h) v[h] = x[h];
+#pragma unroll
+    for (int o = 16, n = GP; n > 1; o >>= 1, n >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < n / 2; ++k) {
+            const float send = upper ? v[k] : v[k + n / 2];
+            const float keep = upper ? v[k + n / 2] : v[k];
+            const float r = __shfl_xor_sync(0xffffffffu, send, o);
+            v[k] = kMax ? fmaxf(keep, r) : keep + r;
+        }
+    }
+#pragma unroll
+    for (int o = 16 / GP; o >= 1; o >>= 1) {
+        const float r = __shfl_xor_sync(0xffffffffu, v[0], o);
+        v[0] = kMax ? fmaxf(v[0], r) : v[0] + r;
+    }
+    return v[0];
+}
+
+// One tile of FP8 codes -> f16 in the 128-byte-swizzled K-major layout of a
+// stage (dims 64h..64h+63 of row r in half h, 16-byte chunk c of that row at
+// chunk c ^ (r & 7)). The codes of row r (128 bytes) sit where half 1 of row r
+// goes; the eight threads of a row are in one warp and all load before any of
+// them stores. Rows at or past nvalid are written as zeros (their codes may be
+// stale or unwritten cache slots). Run by the 128 converter threads.
+__device__ __forceinline__ void widen_tile(uint8_t* tile, int nvalid, int ct) {
+    constexpr int kHalf = kKeys * 128;
+    constexpr int kRpp = kConvThreads / 8;  // rows per pass
+    constexpr int kBatch = 4;
+    const int t = ct % 8, rsub = ct / 8;
+    const int h = t / 4, c0 = 2 * (t % 4);
+    // threads of the second half store their odd chunk first, so the eight
+    // threads of a row hit eight different bank groups in each store
+    const int first = c0 + (t >= 4 ? 1 : 0), second = c0 + (t >= 4 ? 0 : 1);
+    const uint8_t* codes = tile + kHalf;
+#pragma unroll 1
+    for (int r0 = 0; r0 < kKeys; r0 += kRpp * kBatch) {
+        uint4 c[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int r = r0 + kRpp * b + rsub;
+            c[b] = r < nvalid ? *reinterpret_cast<const uint4*>(codes + r * kD + 16 * t) : make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int r = r0 + kRpp * b + rsub;
+            const uint2 w0 = e4m3x4_to_f16x4(c[b].x), w1 = e4m3x4_to_f16x4(c[b].y);
+            const uint2 w2 = e4m3x4_to_f16x4(c[b].z), w3 = e4m3x4_to_f16x4(c[b].w);
+            const uint4 lo = make_uint4(w0.x, w0.y, w1.x, w1.y);  // dims 16t .. 16t+7
+            const uint4 hi = make_uint4(w2.x, w2.y, w3.x, w3.y);  // dims 16t+8 .. 16t+15
+            uint8_t* row = tile + h * kHalf + r * 128;
+            const bool lo_first = first == c0;
+            *reinterpret_cast<uint4*>(row + ((first ^ (r & 7)) << 4)) = lo_first ? lo : hi;
+            *reinterpret_cast<uint4*>(row + ((second ^ (r & 7)) << 4)) = lo_first ? hi : lo;
+        }
+        __syncwarp();
+    }
+}
+
+// Q^T (bf16, 16 rows x 128 dims, swizzled) -> f16 in place, by the 128
+// converter threads; each 16-byte chunk holds 8 elements of one row whatever
+// the swizzle, so the conversion is elementwise. Values beyond the largest
+// finite f16 saturate; the return value says whether an element of one of the
+// group's G rows did (the other rows are other heads' q, or stale).
+__device__ __forceinline__ bool q_to_f16(uint8_t* qbuf, int ct, int G) {
+    bool over = false;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int off = (ct + k * kConvThreads) * 16;
+        const int row = (off % (kN * 128)) / 128;
+        uint4 w = *reinterpret_cast<const uint4*>(qbuf + off);
+        uint32_t* e = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float lo = __uint_as_float(e[i] << 16), hi = __uint_as_float(e[i] & 0xFFFF0000u);
+            over |= row < G && (fabsf(lo) > 65504.f || fabsf(hi) > 65504.f);
+            e[i] = pack_f16x2_satfinite(lo, hi);
+        }
+        *reinterpret_cast<uint4*>(qbuf + off) = w;
+    }
+    return over;
+}
+
+template <bool F8>
+__device__ __forceinline__ uint16_t to16(float x) {
+    if constexpr (F8) return __half_as_ushort(__float2half_rn(x));
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+template <bool F8>
+__device__ __forceinline__ float from16(uint16_t x) {
+    if constexpr (F8) return __half2float(__ushort_as_half(x));
+    return __bfloat162float(__ushort_as_bfloat16(x));
+}
+
+template <bool F8, int GP>
+__global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, PrefillArgs a, float* __restrict__ dec_out,
+                     float* __restrict__ dec_lse, int max_splits, int q_rows) {
+    using C = TcCfg<F8>;
+    const int32_t total = a.num_units[1];
+    if ((int32_t)blockIdx.x >= total) return;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + C::kBar;
+    // stage barriers: 16-bit K / V tile ready, K stage free (its S is done), V
+    // stage free (its PV is done), FP8 codes landed
+    auto k_full = [&](int s) { return bar0 + 8 * s; };
+    auto v_full = [&](int s) { return bar0 + 8 * (kStages + s); };
+    auto k_empty = [&](int s) { return bar0 + 8 * (2 * kStages + s); };
+    auto v_empty = [&](int s) { return bar0 + 8 * (3 * kStages + s); };
+    auto kc_full = [&](int s) { return bar0 + 8 * (4 * kStages + s); };
+    auto vc_full = [&](int s) { return bar0 + 8 * (5 * kStages + s); };
+    // double-buffered: Q^T ready / bf16 Q^T landed (FP8) / free; S^T, P^T, O^T
+    const uint32_t bx = bar0 + 8 * 6 * kStages;
+    auto q_full = [&](int b) { return bx + 8 * b; };
+    auto qc_full = [&](int b) { return bx + 16 + 8 * b; };
+    auto q_empty = [&](int b) { return bx + 32 + 8 * b; };
+    auto s_full = [&](int b) { return bx + 48 + 8 * b; };
+    auto p_full = [&](int b) { return bx + 64 + 8 * b; };
+    auto o_full = [&](int b) { return bx + 80 + 8 * b; };
+    auto o_free = [&](int b) { return bx + 96 + 8 * b; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
+    int32_t* pre = reinterpret_cast<int32_t*>(smem + C::kPre);
+    int32_t* pages = reinterpret_cast<int32_t*>(smem + C::kPages);
+    float* red_m = reinterpret_cast<float*>(smem + C::kRed);  // [warpgroup][tile parity][warp][head]
+    float* red_l = red_m + 2 * 2 * 4 * kMaxG;                 // [item parity][warp][head]
+    float* xchg = reinterpret_cast<float*>(smem + C::kXchg);  // [item parity][head max, head x dim O]
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int G = a.hq / a.hkv;
+    const int32_t bs = a.block_size;
+    const int32_t step = (int32_t)gridDim.x;
+
+    for (int i = threadIdx.x; i <= a.num_rows; i += C::kThreads) pre[i] = a.dec_pre[i];
+    if (threadIdx.x == 0) {
+        const uint32_t filled = F8 ? kConvWarps : 1;  // FP8: each converter warp arrives
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(k_full(s), filled);
+            mbar_init(v_full(s), filled);
+            mbar_init(k_empty(s), 1);
+            mbar_init(v_empty(s), 1);
+            mbar_init(kc_full(s), 1);
+            mbar_init(vc_full(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(q_full(b), filled);
+            mbar_init(qc_full(b), 1);
+            mbar_init(q_empty(b), 1);
+            mbar_init(s_full(b), 1);
+            mbar_init(p_full(b), 4);  // the four warps of the tile's warpgroup
+            mbar_init(o_full(b), 1);
+            mbar_init(o_free(b), 4);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kProdWarp && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProdWarp || warp == kProdWarp + 1) {
+        // ---------------------------------------------------------------- producers
+        // Warp 8 loads the K tiles (and each item's Q^T), warp 9 the V tiles: a K
+        // stage is free again once its S is done, a V stage once its PV is, and
+        // neither side waits for the other.
+        const bool is_k = warp == kProdWarp;
+        const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+        int32_t* my_pages = pages + (is_k ? 0 : kMaxPages);
+        const int32_t oob = (int32_t)(a.num_blocks * bs);  // a row past the cache: zero fill
+        const int ppt = kKeys / bs;                        // pages per tile
+        const uint32_t q_bytes = 2u * (uint32_t)q_rows * 128u;
+        auto full_of = [&](int st) {
+            return F8 ? (is_k ? kc_full(st) : vc_full(st)) : (is_k ? k_full(st) : v_full(st));
+        };
+        uint32_t gt = 0, ic = 0;
+        int32_t ri = 0;
+        bool ok = true;
+        for (int32_t p = blockIdx.x; p < total && ok; p += step) {
+            const DecItem it = dec_item(pre, ri, p, a.rows, a.hkv);
+            // the split's block-table entries as first cache rows; a bad id maps to a
+            // row past the cache (zero filled) and reports PCP_ERR_RANGE
+            const int32_t* table = a.block_table + (size_t)it.req * a.max_blocks;
+            const int32_t pg0 = it.lo / bs;
+            const int npg = (it.hi - it.lo + bs - 1) / bs;
+            __syncwarp();
+            for (int i = lane; i < npg; i += 32) {
+                const int32_t pg = pg0 + i;
+                const int32_t id = pg < a.max_blocks ? __ldg(table + pg) : -1;
+                int32_t y = oob;
+                if (id >= 0 && id < a.num_blocks) y = id * bs;
+                else if (is_k) report_status(a.status, PCP_ERR_RANGE);
+                my_pages[i] = y;
+            }
+            __syncwarp();
+            if (is_k) {
+                const int qb = ic & 1;
+                if (!(ok = mbar_wait_warp(q_empty(qb), ((ic >> 1) & 1) ^ 1, abort_flag))) break;
+                if (lane == 0) {
+                    const uint32_t qbar = F8 ? qc_full(qb) : q_full(qb);
+                    mbar_arrive_expect_tx(qbar, q_bytes);
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_3d(sbase + C::kQ + qb * C::kQBytes + h * C::kRowsBytes, &tm_q, qbar, h * 64,
+                                    it.hk * G, it.q_start);
+                }
+                ++ic;
+            }
+            for (int j = 0; j < it.nt; ++j) {
+                const int st = gt % kStages;
+                const int nvalid = min(kKeys, it.hi - it.lo - j * kKeys);
+                const int np = (nvalid + bs - 1) / bs;
+                if (!(ok = mbar_wait_warp(is_k ? k_empty(st) : v_empty(st), ((gt / kStages) & 1) ^ 1, abort_flag)))
+                    break;
+                const uint32_t fb = full_of(st);
+                if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(np * bs) * (F8 ? kD : 2 * kD));
+                __syncwarp();
+                if (lane < np) {
+                    const int32_t y = my_pages[j * ppt + lane];
+                    const uint32_t dst = sbase + st * C::kStageBytes + (is_k ? 0 : C::kTileBytes);
+                    if constexpr (F8) {
+                        tma_load_3d(dst + C::kHalfBytes + lane * bs * kD, tm, fb, 0, it.hk, y);
+                    } else {
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_3d(dst + h * C::kHalfBytes + lane * bs * 128, tm, fb, h * 64, it.hk, y);
+                    }
+                }
+                ++gt;
+            }
+        }
+        if (!ok && lane == 0) {
+            report_status(a.status, PCP_ERR_TIMEOUT);
+            // wait (bounded, whatever the abort flag says) for the copies already
+            // issued, so that none lands after the CTA has gone
+            int no_abort = 0;
+            for (uint32_t g = gt > kStages ? gt - kStages : 0; g < gt; ++g)
+                mbar_wait(full_of(g % kStages), (g / kStages) & 1, &no_abort, 100000000ull);
+            if (is_k)
+                for (uint32_t i = ic > 2 ? ic - 2 : 0; i < ic; ++i)
+                    mbar_wait(F8 ? qc_full(i & 1) : q_full(i & 1), (i >> 1) & 1, &no_abort, 100000000ull);
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            // descriptors of the first k-step; a later k-step moves the start address
+            auto k_desc = [&](int s) { return sdesc_sw128(sbase + s * C::kStageBytes, 16, 1024); };
+            auto v_desc = [&](int s) {
+                return sdesc_sw128(sbase + s * C::kStageBytes + C::kTileBytes, C::kHalfBytes, 1024);
+            };
+            auto q_desc = [&](int b) { return sdesc_sw128(sbase + C::kQ + b * C::kQBytes, 16, 1024); };
+            auto p_desc = [&](int b) { return sdesc_sw128(sbase + C::kP + b * C::kPBytes, 16, 1024); };
+            // S^T(g) = K(g) Q^T: A = the K tile (K-major, 128 keys), B = Q^T (K-major, 16 rows)
+            auto issue_s = [&](uint32_t g, int qb) {
+                const uint64_t kd = k_desc(g % kStages), qd = q_desc(qb);
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    const uint32_t koff = ((ks / 4) * C::kHalfBytes + (ks % 4) * 32) >> 4;
+                    const uint32_t qoff = ((ks / 4) * C::kRowsBytes + (ks % 4) * 32) >> 4;
+                    mma_ss(tmem + (g & 1) * kN, kd + koff, qd + qoff, C::kIdescS, ks > 0 ? 1u : 0u);
+                }
+                mma_commit(s_full(g & 1));
+                mma_commit(k_empty(g % kStages));
+            };
+            // O^T(g) = V(g)^T P^T: A = the V tile read MN-major (M = D), B = P^T (K-major, 16 rows)
+            auto issue_o = [&](uint32_t g) {
+                const uint64_t vd = v_desc(g % kStages), pd = p_desc(g & 1);
+#pragma unroll
+                for (int ks = 0; ks < kKeys / 16; ++ks) {
+                    const uint32_t poff = ((ks / 4) * C::kRowsBytes + (ks % 4) * 32) >> 4;
+                    mma_ss(tmem + 2 * kN + (g & 1) * kN, vd + (uint32_t)(ks * 2048 >> 4), pd + poff, C::kIdescO,
+                           ks > 0 ? 1u : 0u);
+                }
+                mma_commit(o_full(g & 1));
+                mma_commit(v_empty(g % kStages));
+            };
+            // Event loop: issue S of the next tile (gs) once its K and the item's Q^T
+            // are in and its S buffer is free, and PV of the oldest tile without one
+            // (go) once its P, V and O buffer are; whichever is ready first. Polls do
+            // not block, and a stretch without progress is bounded as a wait is.
+            uint32_t gs = 0, go = 0, ic = 0;
+            int32_t ri = 0, p = blockIdx.x;
+            DecItem it = dec_item(pre, ri, p, a.rows, a.hkv);
+            int js = 0;
+            bool s_done = false, q_ready = false, ok = true;
+            uint64_t t_idle = 0;
+            while (true) {
+                bool progress = false;
+                if (!s_done && gs < go + 2) {  // S buffer gs & 1 is free once PV(gs - 2) is issued
+                    if (!q_ready) q_ready = mbar_test(q_full(ic & 1), (ic >> 1) & 1);
+                    if (q_ready && mbar_test(k_full(gs % kStages), (gs / kStages) & 1)) {
+                        tc_fence_after();
+                        issue_s(gs, ic & 1);
+                        ++gs;
+                        if (++js == it.nt) {
+                            mma_commit(q_empty(ic & 1));
+                            ++ic;
+                            js = 0;
+                            q_ready = false;
+                            p += step;
+                            if (p < total) it = dec_item(pre, ri, p, a.rows, a.hkv);
+                            else s_done = true;
+                        }
+                        progress = true;
+                    }
+                }
+                if (go < gs) {
+                    if (mbar_test(p_full(go & 1), (go >> 1) & 1) && mbar_test(v_full(go % kStages), (go / kStages) & 1) &&
+                        mbar_test(o_free(go & 1), ((go >> 1) & 1) ^ 1)) {
+                        tc_fence_after();
+                        issue_o(go);
+                        ++go;
+                        progress = true;
+                    }
+                } else if (s_done) {
+                    break;  // every tile's S and PV issued
+                }
+                if (progress) {
+                    t_idle = 0;
+                    continue;
+                }
+                if (*abort_flag) {
+                    ok = false;
+                    break;
+                }
+                const uint64_t now = global_timer_ns();
+                if (t_idle == 0) {
+                    t_idle = now;
+                } else if (now - t_idle > kWaitTimeoutNs) {
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok) report_status(a.status, PCP_ERR_TIMEOUT);
+        }
+    } else if (F8 && warp >= kConvWarp0) {
+        // ---------------------------------------------------------------- FP8 converters
+        const int ct = threadIdx.x - kConvWarp0 * 32;
+        uint32_t gt = 0, ic = 0;
+        int32_t ri = 0;
+        bool ok = true;
+        for (int32_t p = blockIdx.x; p < total && ok; p += step) {
+            const DecItem it = dec_item(pre, ri, p, a.rows, a.hkv);
+            const int qb = ic & 1;
+            if (!(ok = mbar_wait_warp(qc_full(qb), (ic >> 1) & 1, abort_flag))) break;
+            if (__any_sync(0xffffffffu, q_to_f16(smem + C::kQ + qb * C::kQBytes, ct, G)) && lane == 0)
+                report_status(a.status, PCP_ERR_RANGE);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_full(qb));
+            ++ic;
+            for (int j = 0; j < it.nt; ++j) {
+                const int st = gt % kStages;
+                const int nvalid = min(kKeys, it.hi - it.lo - j * kKeys);
+                uint8_t* kt = smem + st * C::kStageBytes;
+                if (!(ok = mbar_wait_warp(kc_full(st), (gt / kStages) & 1, abort_flag))) break;
+                widen_tile(kt, nvalid, ct);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(k_full(st));
+                if (!(ok = mbar_wait_warp(vc_full(st), (gt / kStages) & 1, abort_flag))) break;
+                widen_tile(kt + C::kTileBytes, nvalid, ct);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(v_full(st));
+                ++gt;
+            }
+        }
+        if (!ok && lane == 0) report_status(a.status, PCP_ERR_TIMEOUT);
+    } else {
+        // ---------------------------------------------------------------- softmax
+        // Two warpgroups take alternate tiles (tile g: warpgroup g % 2), each with its
+        // own running max, sums and O over its tiles; at the end of an item
+        // warpgroup 0 merges the two and writes the split's partial.
+        const int wg = warp / 4, wq = warp % 4;
+        const int t = threadIdx.x % 128;  // key of the tile (S^T lane), dim (O^T lane)
+        const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+        constexpr int kSpan = 32 / GP;     // lanes that end the reduce-scatter with one head
+        const int hl = lane / kSpan;       // that head
+        uint32_t gt = 0, ic = 0;
+        int32_t ri = 0;
+        bool ok = true;     // every wait of this thread so far completed
+        bool stop = false;  // the eight warps' joint verdict, taken once per item
+        for (int32_t p = blockIdx.x; p < total && !stop; p += step, ++ic) {
+            const DecItem it = dec_item(pre, ri, p, a.rows, a.hkv);
+            const float kd = F8 ? __ldg(a.k_descale + (size_t)it.req * a.hkv + it.hk) : 1.f;
+            const float sl2 = a.scale * kd * kLog2e;
+            float m_run[GP], l_t[GP], acc[GP], a_prev[GP];
+#pragma unroll
+            for (int h = 0; h < GP; ++h) {
+                m_run[h] = -INFINITY;
+                l_t[h] = 0.f;
+                acc[h] = 0.f;
+                a_prev[h] = 0.f;
+            }
+            // O^T of tile g (this thread's dim) into the running sums, rescaled by the
+            // max update of that tile
+            auto accumulate = [&](uint32_t g, const float (&alpha)[GP]) {
+                ok &= mbar_wait_warp(o_full(g & 1), (g >> 1) & 1, abort_flag);
+                tc_fence_after();
+                uint32_t o[16];
+                tmem_ld16(tmem + lane_base + 2 * kN + (g & 1) * kN, o);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_free(g & 1));
+#pragma unroll
+                for (int h = 0; h < GP; ++h)
+                    acc[h] = acc[h] * alpha[h] + (__uint_as_float(o[h]) + __uint_as_float(o[kMaxG + h]));
+            };
+            uint32_t g_prev = 0;
+            bool have_prev = false;
+            for (int j = 0; j < it.nt; ++j) {
+                const uint32_t g = gt + j;
+                if ((int)(g & 1) != wg) continue;
+                const int nvalid = min(kKeys, it.hi - it.lo - j * kKeys);
+                const bool valid = t < nvalid;
+                ok &= mbar_wait_warp(s_full(g & 1), (g >> 1) & 1, abort_flag);
+                tc_fence_after();
+                uint32_t s[16];
+                tmem_ld16(tmem + lane_base + (g & 1) * kN, s);
+                tmem_wait_ld();
+                float x[GP];
+#pragma unroll
+                for (int h = 0; h < GP; ++h) x[h] = valid ? __uint_as_float(s[h]) * sl2 : -INFINITY;
+                // tile max per head: over the warp, then over the warpgroup's four warps
+                float* rm = red_m + (wg * 2 + ((g >> 1) & 1)) * 4 * kMaxG;  // [warp][head]
+                const float wm = warp_scatter<GP, true>(x, lane);
+                if (lane % kSpan == 0) rm[wq * kMaxG + hl] = wm;
+                bar_sync_named(1 + wg, 128);
+                float alpha[GP];
+                uint8_t* pbuf = smem + C::kP + (g & 1) * C::kPBytes;
+                // this key's column of P^T: chunk (t % 64) / 8 of each row, swizzled by the row
+                uint8_t* pcol = pbuf + (t >> 6) * C::kRowsBytes + (t & 7) * 2;
+                const int chunk = (t & 63) >> 3;
+#pragma unroll
+                for (int h = 0; h < GP; ++h) {
+                    const float mt = fmaxf(fmaxf(rm[h], rm[kMaxG + h]), fmaxf(rm[2 * kMaxG + h], rm[3 * kMaxG + h]));
+                    const float m_new = fmaxf(m_run[h], mt);  // finite: the tile has a valid key
+                    alpha[h] = fast_exp2(m_run[h] - m_new);   // 0 on the warpgroup's first tile
+                    m_run[h] = m_new;
+                    const float pe = fast_exp2(x[h] - m_new);
+                    l_t[h] = l_t[h] * alpha[h] + pe;
+                    const uint16_t hi = to16<F8>(pe);
+                    const uint16_t lo = to16<F8>(pe - from16<F8>(hi));
+                    *reinterpret_cast<uint16_t*>(pcol + h * 128 + ((chunk ^ (h & 7)) << 4)) = hi;
+                    *reinterpret_cast<uint16_t*>(pcol + (kMaxG + h) * 128 + ((chunk ^ (h & 7)) << 4)) = lo;
+                }
+                if (!F8 && nvalid < kKeys) {
+                    // keys past the split's end: zero their V rows (unwritten cache slots in
+                    // the last page, stale rows after it) once the tile has landed
+                    const uint32_t g3 = g % kStages;
+                    ok &= mbar_wait_warp(v_full(g3), (g / kStages) & 1, abort_flag);
+                    if (!valid) {
+                        uint8_t* vrow = smem + g3 * C::kStageBytes + C::kTileBytes + t * 128;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                *reinterpret_cast<uint4*>(vrow + h * C::kHalfBytes + c * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full(g & 1));
+                if (have_prev) accumulate(g_prev, a_prev);
+                g_prev = g;
+                have_prev = true;
+#pragma unroll
+                for (int h = 0; h < GP; ++h) a_prev[h] = alpha[h];
+            }
+            if (have_prev) accumulate(g_prev, a_prev);
+            gt += it.nt;
+            // l per head over this warp's keys; warpgroup 1 hands over its max and O
+            const int ip = ic & 1;
+            float* rl = red_l + ip * 8 * kMaxG;                  // [warp 0..7][head]
+            float* xm = xchg + ip * (kMaxG + kMaxG * kKeys);     // [head] max, then [head][dim] O
+            const float wl = warp_scatter<GP, false>(l_t, lane);
+            if (lane % kSpan == 0) rl[warp * kMaxG + hl] = wl;
+            if (wg == 1) {
+#pragma unroll
+                for (int h = 0; h < GP; ++h) {
+                    if (t == 0) xm[h] = m_run[h];
+                    xm[kMaxG + h * kKeys + t] = acc[h];
+                }
+            }
+            if ((stop = bar_all_or(!ok))) break;
+            if (wg == 0) {
+                const float vd = F8 ? __ldg(a.v_descale + (size_t)it.req * a.hkv + it.hk) : 1.f;
+#pragma unroll
+                for (int h = 0; h < GP; ++h) {
+                    if (h >= G) continue;
+                    const float L0 = rl[h] + rl[kMaxG + h] + rl[2 * kMaxG + h] + rl[3 * kMaxG + h];
+                    const float L1 = rl[4 * kMaxG + h] + rl[5 * kMaxG + h] + rl[6 * kMaxG + h] + rl[7 * kMaxG + h];
+                    const float m1 = xm[h];
+                    const float M = fmaxf(m_run[h], m1);  // finite: the item has a tile
+                    const float f0 = fast_exp2(m_run[h] - M), f1 = fast_exp2(m1 - M);
+                    const float L = L0 * f0 + L1 * f1;
+                    const float O = acc[h] * f0 + xm[kMaxG + h * kKeys + t] * f1;
+                    const size_t slot = ((size_t)it.ri * a.hq + it.hk * G + h) * max_splits + it.split;
+                    dec_out[slot * kD + t] = L > 0.f ? O / L * vd : 0.f;
+                    if (t == 0) dec_lse[slot] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+                }
+            }
+        }
+        if (stop && threadIdx.x == 0) report_status(a.status, PCP_ERR_TIMEOUT);
+    }
+
+    __syncwarp();  // lane 0 of the MMA warp and of the producer worked alone: reconverge first
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <bool F8, int GP>
+int launch_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits, cudaStream_t stream) {
+    const int64_t slots = a.num_blocks * a.block_size;
+    const int q_rows = a.hq < kN ? a.hq : kN;
+    CUtensorMap tq, tk, tv;
+    bool maps = make_box_map(&tq, a.q, kD, 2, a.hq, a.total_q, 64, q_rows, 1, true);
+    if (F8)
+        maps = maps && make_box_map(&tk, a.key_cache, kD, 1, a.hkv, slots, kD, 1, a.block_size, false) &&
+               make_box_map(&tv, a.value_cache, kD, 1, a.hkv, slots, kD, 1, a.block_size, false);
+    else
+        maps = maps && make_box_map(&tk, a.key_cache, kD, 2, a.hkv, slots, 64, 1, a.block_size, true) &&
+               make_box_map(&tv, a.value_cache, kD, 2, a.hkv, slots, 64, 1, a.block_size, true);
+    if (!maps) return PCP_ERR_CUDA;
+    const int smem = TcCfg<F8>::kSmem;
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_tc_kernel<F8, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
+    decode_tc_kernel<F8, GP><<<num_sms(), TcCfg<F8>::kThreads, smem, stream>>>(tq, tk, tv, a, dec_out, dec_lse,
+                                                                              max_splits, q_rows);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
+    return PCP_OK;
+}
+
+}  // namespace
+
+int launch_decode_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
+                     cudaStream_t stream) {
+    const int G = a.hkv > 0 ? a.hq / a.hkv : 0;
+    if (a.d != kD || G < 1 || G > kMaxG || a.num_rows > kDecTcMaxRows || a.block_size > kKeys ||
+        kKeys % a.block_size != 0)
+        return PCP_ERR_UNSUPPORTED;
+    // heads per group padded to a power of two (the padded heads' results are not written)
+    const int GP = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
+    if (a.k_descale) {
+        if (GP == 1) return launch_tc<true, 1>(a, dec_out, dec_lse, max_splits, stream);
+        if (GP == 2) return launch_tc<true, 2>(a, dec_out, dec_lse, max_splits, stream);
+        if (GP == 4) return launch_tc<true, 4>(a, dec_out, dec_lse, max_splits, stream);
+        return launch_tc<true, 8>(a, dec_out, dec_lse, max_splits, stream);
+    }
+    if (GP == 1) return launch_tc<false, 1>(a, dec_out, dec_lse, max_splits, stream);
+    if (GP == 2) return launch_tc<false, 2>(a, dec_out, dec_lse, max_splits, stream);
+    if (GP == 4) return launch_tc<false, 4>(a, dec_out, dec_lse, max_splits, stream);
+    return launch_tc<false, 8>(a, dec_out, dec_lse, max_splits, stream);
+}
+
+}  // namespace pcp

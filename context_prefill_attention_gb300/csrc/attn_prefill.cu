@@ -835,10 +835,12 @@ __device__ __forceinline__ int32_t unit_cost(const Unit& u, const pcp_row_t* row
 
 // Check every row, then build the prefill work list: one unit per (valid
 // non-decode row, 128-token tile, pass), ordered by the number of key tiles,
-// longest first.
+// longest first. Also counts the decode work items (kv head x 1024-key split of
+// each valid decode row): dec_pre[i] = items of rows before row i, header[1] =
+// their total.
 __global__ void __launch_bounds__(kSchedThreads, 1)
     schedule_kernel(PrefillArgs a, int32_t flags, Unit* units, Unit* sorted, int32_t* header,
-                    int32_t* row_ok, int64_t max_units) {
+                    int32_t* row_ok, int32_t* dec_pre, int64_t max_units) {
     __shared__ int32_t warp_sums[32];
     // bitonic sort keys, or the counters of the counting sort
     __shared__ __align__(16) unsigned long long keys[kSortCap];
@@ -849,11 +851,11 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     const bool at_row_start = (flags & PCP_ATTN_SPLIT_AT_ROW_START) != 0;
     const int nparts = a.nparts;             // 0: fused; 2: context + new; n: n key shards
     const int passes = nparts > 0 ? nparts : 1;
-    int32_t base = 0;
+    int32_t base = 0, dbase = 0;
     for (int32_t r0 = 0; r0 < num_rows; r0 += kSchedThreads) {
         const int32_t ri = r0 + threadIdx.x;
         pcp_row_t row{};
-        int32_t cnt = 0;
+        int32_t cnt = 0, dcnt = 0;
         if (ri < num_rows) {
             row = rows[ri];
             const bool ok = row.req >= 0 && row.req < a.num_reqs && row.q_len >= 1 && row.q_start >= 0 &&
@@ -863,7 +865,12 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
             row_ok[ri] = ok ? 1 : 0;
             if (!ok) report_status(a.status, PCP_ERR_RANGE);
             if (ok && !row.is_decode) cnt = ((row.q_len + kBlockM - 1) / kBlockM) * passes;
+            if (ok && row.is_decode) dcnt = ((row.kv_end + kDecodeChunk - 1) / kDecodeChunk) * a.hkv;
         }
+        int32_t dtot;
+        const int32_t doff = dbase + block_exclusive_scan(dcnt, warp_sums, &dtot);
+        if (ri < num_rows) dec_pre[ri] = doff;
+        dbase += dtot;
         int32_t tot;
         const int32_t off = base + block_exclusive_scan(cnt, warp_sums, &tot);
         for (int32_t u = 0; u < cnt; ++u) {
@@ -888,7 +895,11 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
         base += tot;
     }
     const int32_t n = (int32_t)min((int64_t)base, max_units);
-    if (threadIdx.x == 0) header[0] = n;
+    if (threadIdx.x == 0) {
+        header[0] = n;
+        header[1] = dbase;
+        dec_pre[num_rows] = dbase;
+    }
     // every thread's units[] writes must be visible before any thread reads them
     __syncthreads();
     if (n > kSortCap) {
@@ -1020,9 +1031,10 @@ int launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
 }  // namespace
 
 int launch_schedule(const PrefillArgs& a, int32_t flags, Unit* units, Unit* units_sorted,
-                    int32_t* header, int32_t* row_ok, int64_t max_units, cudaStream_t stream) {
+                    int32_t* header, int32_t* row_ok, int32_t* dec_pre, int64_t max_units,
+                    cudaStream_t stream) {
     schedule_kernel<<<1, kSchedThreads, 0, stream>>>(a, flags, units, units_sorted, header, row_ok,
-                                                     max_units);
+                                                     dec_pre, max_units);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
     return PCP_OK;
@@ -1037,6 +1049,21 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
 
 bool make_kv_row_map(CUtensorMap* m, const void* base, int D, int esize, int64_t mid, int64_t outer, int rows) {
     return make_row_map(m, base, D, esize, mid, outer, rows);
+}
+
+bool make_box_map(CUtensorMap* m, const void* base, int D, int esize, int64_t mid, int64_t outer, int box_x,
+                  int box_mid, int box_outer, bool swizzle128) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)mid, (cuuint64_t)outer};
+    cuuint64_t strides[2] = {(cuuint64_t)D * esize, (cuuint64_t)(D * esize * mid)};
+    cuuint32_t box[3] = {(cuuint32_t)box_x, (cuuint32_t)box_mid, (cuuint32_t)box_outer};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt = esize == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 }  // namespace pcp

@@ -33,6 +33,7 @@ struct Unit {
 struct WorkspaceLayout {
     size_t header;        // int32[64]: [0] = number of units
     size_t row_ok;        // int32[num_rows]: 1 for a row that passed the checks
+    size_t dec_pre;       // int32[num_rows + 1]: decode work items of the rows before each row
     size_t units;         // Unit[max_units], unsorted
     size_t units_sorted;  // Unit[max_units], longest first
     size_t part_out;      // nparts x fp32 [T][Hq][D] (separate-context / KV-shard modes)
@@ -81,7 +82,10 @@ struct PrefillArgs {
     int32_t nparts;    // 0: one fused pass straight into out / lse
     const int32_t* row_ok;
     const Unit* units;
-    const int32_t* num_units;
+    const int32_t* num_units;   // header: [0] prefill units, [1] decode work items
+    // decode work items (kv head x 1024-key split of a decode row) of the rows
+    // before row i, for i = 0..num_rows (the last entry is the total)
+    const int32_t* dec_pre;
     int32_t* status;
     // FP8 (e4m3) cache: per-(request, kv head) descales [num_reqs][hkv]; both
     // null for a bf16 cache
@@ -92,6 +96,10 @@ struct PrefillArgs {
 // TMA map of a cache viewed as [outer][mid][D] elements of esize bytes (1: FP8
 // codes, 2: bf16) with a box of D x 1 x rows, no swizzle.
 bool make_kv_row_map(CUtensorMap* m, const void* base, int D, int esize, int64_t mid, int64_t outer, int rows);
+// TMA map of [outer][mid][D] elements of esize bytes (1: uint8, 2: bf16) with a
+// box of box_x x box_mid x box_outer elements, 128-byte swizzled or not.
+bool make_box_map(CUtensorMap* m, const void* base, int D, int esize, int64_t mid, int64_t outer, int box_x,
+                  int box_mid, int box_outer, bool swizzle128);
 
 // Supplies the workspace of an attention call that has passed every argument
 // check: at least `need` bytes, 256-byte aligned. Returns PCP_OK after setting
@@ -111,10 +119,16 @@ int attn_call(const void* q, const void* key_cache, const void* value_cache, con
               WorkspaceProvider provide);
 
 int launch_schedule(const PrefillArgs& a, int32_t flags, Unit* units, Unit* units_sorted,
-                    int32_t* header, int32_t* row_ok, int64_t max_units, cudaStream_t stream);
+                    int32_t* header, int32_t* row_ok, int32_t* dec_pre, int64_t max_units,
+                    cudaStream_t stream);
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 int launch_decode(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
                   cudaStream_t stream);
+// The tensor-core decode (head_dim 128, up to 8 q heads per kv head, at most
+// kDecTcMaxRows rows); PCP_ERR_UNSUPPORTED for any other shape.
+constexpr int kDecTcMaxRows = 1024;
+int launch_decode_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
+                     cudaStream_t stream);
 int launch_separate_merge(const PrefillArgs& a, cudaStream_t stream);
 int launch_cache_write(const void* k, const void* v, const int64_t* slot, int32_t num_tokens,
                        int32_t vec_per_tok, void* key_cache, void* value_cache, int64_t num_slots,

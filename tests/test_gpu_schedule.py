@@ -80,20 +80,39 @@ def expected_units(rows: np.ndarray, flags: int, bs: int):
     return out
 
 
+DECODE_CHUNK = 1024
+
+
 def read_schedule(case: Case):
     """Unit count and sorted units from the workspace of the last call. The
     offsets follow pcp_attn_varlen's workspace layout: a 64-entry int32 header
-    (the unit count first), the row flags, the unsorted units, then the sorted
-    units (16 bytes each), every part 256-byte aligned."""
+    (the unit count first), the row flags, the decode-item prefix (num_rows + 1
+    int32), the unsorted units, then the sorted units (16 bytes each), every
+    part 256-byte aligned."""
     spec, flags = case.spec, case.flags
     n_rows = int(case.plan["rows"].shape[0])
     max_units = _passes(flags) * (-(-spec.total_q // BLOCK_M) + n_rows)
-    off_units = 256 + _align256(n_rows * 4)
+    off_units = 256 + _align256(n_rows * 4) + _align256((n_rows + 1) * 4)
     off_sorted = off_units + _align256(max_units * 16)
     ws = case.step.workspace[:off_sorted + max_units * 16].cpu().numpy()
     n = int(ws[:4].view(np.int32)[0])
     units = ws[off_sorted:off_sorted + 16 * n].view(np.int32).reshape(n, 4)
     return n, units
+
+
+def read_decode_prefix(case: Case):
+    """header[1] and the decode-item prefix of the last call."""
+    n_rows = int(case.plan["rows"].shape[0])
+    off = 256 + _align256(n_rows * 4)
+    ws = case.step.workspace[:off + (n_rows + 1) * 4].cpu().numpy()
+    return int(ws[4:8].view(np.int32)[0]), ws[off:off + (n_rows + 1) * 4].view(np.int32).copy()
+
+
+def expected_decode_prefix(rows: np.ndarray, num_kv_heads: int) -> np.ndarray:
+    """Items of the rows before each row: kv heads x 1024-key splits of every
+    decode row, none for prefill rows."""
+    cnt = [num_kv_heads * (-(-int(r[5]) // DECODE_CHUNK)) if int(r[7]) else 0 for r in rows]
+    return np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32)
 
 
 def check_schedule(case: Case):
@@ -120,11 +139,16 @@ def _run(spec, flags, tokens=None):
 
 
 def test_bitonic_path_order_and_parity():
-    """A list under the limit: exact longest-first order."""
+    """A list under the limit: exact longest-first order. The decode rows'
+    work-item prefix is checked too."""
     spec = W.custom_spec([3, 64, 129, 1, 17, 256, 2, 90, 1, 500], [0, 5, 0, 44, 130, 0, 1, 7, 300, 0],
                          num_q_heads=8, num_kv_heads=4, head_dim=128, seed=31)
     case = _run(spec, 0)
     assert 0 < check_schedule(case) <= SORT_CAP
+    total, pre = read_decode_prefix(case)
+    want = expected_decode_prefix(case.plan["rows"], spec.num_kv_heads)
+    assert total == int(want[-1]) > 0
+    np.testing.assert_array_equal(pre, want)
 
 
 def test_kv_shards_64_over_limit():
