@@ -24,10 +24,10 @@
 //    the stage), into a 3-stage ring that runs on across items; warp 8 also
 //    loads each item's Q^T (16 q heads of the token from head hk * G, rows past
 //    Hq zero filled);
-//  * lane 0 of warp 10 issues the MMAs from an event loop: S^T of the next tile
-//    once its K is in, O^T of the oldest tile once its P is written, whichever
-//    comes first; commits free the K stage (after S), the V stage (after PV)
-//    and the S and O buffers;
+//  * lane 0 of warp 10 issues every S^T (once K(g) is in and P(g - 2) has left
+//    its S buffer), lane 0 of warp 11 every O^T (once P(g) is written); one
+//    thread cannot issue the 16 small MMAs of a tile fast enough. Commits free
+//    the K stage (after S), the V stage (after PV) and the S and O buffers;
 //  * warps 0-3 and 4-7 are two softmax warpgroups taking alternate tiles, one
 //    thread per key of the tile (TMEM lane) and per dim of O^T: scores -> tile
 //    max per head (a reduce-scatter over the warp, then the warpgroup's four
@@ -37,7 +37,7 @@
 //    is added into registers with the running rescale; at the end of an item
 //    warpgroup 0 merges the two warpgroups' (max, l, O) and writes the split's
 //    partial;
-//  * FP8 cache: warps 11-14 widen each tile's codes to f16 in place (exact; rows
+//  * FP8 cache: warps 12-15 widen each tile's codes to f16 in place (exact; rows
 //    past the last key written as zeros), and Q^T from bf16 to f16 (saturating;
 //    PCP_ERR_RANGE if a q head's element exceeds 65504), so the MMAs take f16
 //    operands; the K descale scales the scores, the V descale the partial;
@@ -65,8 +65,9 @@ constexpr int kN = 16;           // the N of both MMAs
 constexpr int kMaxG = 8;         // q heads per kv head: P's hi and lo rows fit N = 16
 constexpr int kStages = 3;       // K/V tiles in flight per CTA
 constexpr int kProdWarp = 8;     // warp 8: K tiles and Q^T; warp 9: V tiles
-constexpr int kMmaWarp = 10;
-constexpr int kConvWarp0 = 11;
+constexpr int kMmaWarp = 10;     // lane 0 issues the S MMAs (the warp owns the TMEM allocation)
+constexpr int kPvWarp = 11;      // lane 0 issues the PV MMAs
+constexpr int kConvWarp0 = 12;
 constexpr int kConvWarps = 4;    // FP8 cache only
 constexpr int kConvThreads = 32 * kConvWarps;
 constexpr int kMaxPages = kDecodeChunk / 8;  // block-table entries of one split (block_size >= 8)
@@ -122,20 +123,6 @@ __device__ __forceinline__ DecItem dec_item(const int32_t* pre, int32_t& ri, int
     it.nt = (it.hi - it.lo + kKeys - 1) / kKeys;
     (void)hkv;
     return it;
-}
-
-// One non-blocking look at an mbarrier phase: true if the phase with the given
-// parity has completed.
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
 }
 
 // Named barrier `id` over `n` threads (whole warps).
@@ -421,8 +408,12 @@ __global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
                 for (uint32_t i = ic > 2 ? ic - 2 : 0; i < ic; ++i)
                     mbar_wait(F8 ? qc_full(i & 1) : q_full(i & 1), (i >> 1) & 1, &no_abort, 100000000ull);
         }
-    } else if (warp == kMmaWarp) {
-        // ---------------------------------------------------------------- MMA issuer
+    } else if (warp == kMmaWarp || warp == kPvWarp) {
+        // ---------------------------------------------------------------- MMA issuers
+        // Two threads in different warps: one issues every S, the other every PV.
+        // They share no operand (S reads a K stage and Q^T, PV a V stage and P^T;
+        // their TMEM columns differ), and each commit covers the MMAs of the thread
+        // that makes it, so the two streams need no ordering between them.
         if (lane == 0) {
             // descriptors of the first k-step; a later k-step moves the start address
             auto k_desc = [&](int s) { return sdesc_sw128(sbase + s * C::kStageBytes, 16, 1024); };
@@ -431,87 +422,52 @@ __global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
             };
             auto q_desc = [&](int b) { return sdesc_sw128(sbase + C::kQ + b * C::kQBytes, 16, 1024); };
             auto p_desc = [&](int b) { return sdesc_sw128(sbase + C::kP + b * C::kPBytes, 16, 1024); };
-            // S^T(g) = K(g) Q^T: A = the K tile (K-major, 128 keys), B = Q^T (K-major, 16 rows)
-            auto issue_s = [&](uint32_t g, int qb) {
-                const uint64_t kd = k_desc(g % kStages), qd = q_desc(qb);
-#pragma unroll
-                for (int ks = 0; ks < kD / 16; ++ks) {
-                    const uint32_t koff = ((ks / 4) * C::kHalfBytes + (ks % 4) * 32) >> 4;
-                    const uint32_t qoff = ((ks / 4) * C::kRowsBytes + (ks % 4) * 32) >> 4;
-                    mma_ss(tmem + (g & 1) * kN, kd + koff, qd + qoff, C::kIdescS, ks > 0 ? 1u : 0u);
-                }
-                mma_commit(s_full(g & 1));
-                mma_commit(k_empty(g % kStages));
-            };
-            // O^T(g) = V(g)^T P^T: A = the V tile read MN-major (M = D), B = P^T (K-major, 16 rows)
-            auto issue_o = [&](uint32_t g) {
-                const uint64_t vd = v_desc(g % kStages), pd = p_desc(g & 1);
-#pragma unroll
-                for (int ks = 0; ks < kKeys / 16; ++ks) {
-                    const uint32_t poff = ((ks / 4) * C::kRowsBytes + (ks % 4) * 32) >> 4;
-                    mma_ss(tmem + 2 * kN + (g & 1) * kN, vd + (uint32_t)(ks * 2048 >> 4), pd + poff, C::kIdescO,
-                           ks > 0 ? 1u : 0u);
-                }
-                mma_commit(o_full(g & 1));
-                mma_commit(v_empty(g % kStages));
-            };
-            // Event loop: issue S of the next tile (gs) once its K and the item's Q^T
-            // are in and its S buffer is free, and PV of the oldest tile without one
-            // (go) once its P, V and O buffer are; whichever is ready first. Polls do
-            // not block, and a stretch without progress is bounded as a wait is.
-            uint32_t gs = 0, go = 0, ic = 0;
-            int32_t ri = 0, p = blockIdx.x;
-            DecItem it = dec_item(pre, ri, p, a.rows, a.hkv);
-            int js = 0;
-            bool s_done = false, q_ready = false, ok = true;
-            uint64_t t_idle = 0;
-            while (true) {
-                bool progress = false;
-                if (!s_done && gs < go + 2) {  // S buffer gs & 1 is free once PV(gs - 2) is issued
-                    if (!q_ready) q_ready = mbar_test(q_full(ic & 1), (ic >> 1) & 1);
-                    if (q_ready && mbar_test(k_full(gs % kStages), (gs / kStages) & 1)) {
+            uint32_t g = 0, ic = 0;
+            int32_t ri = 0;
+            bool ok = true;
+            const bool s_role = warp == kMmaWarp;
+            for (int32_t p = blockIdx.x; p < total && ok; p += step) {
+                const DecItem it = dec_item(pre, ri, p, a.rows, a.hkv);
+                const int qb = ic & 1;
+                if (s_role && !(ok = mbar_wait(q_full(qb), (ic >> 1) & 1, abort_flag))) break;
+                for (int j = 0; j < it.nt; ++j, ++g) {
+                    if (s_role) {
+                        // S^T(g) = K(g) Q^T: A = the K tile (K-major, 128 keys), B = Q^T
+                        // (K-major, 16 rows); S buffer g & 1 is free once P(g - 2) is written
+                        if (g >= 2 && !(ok = mbar_wait(p_full(g & 1), ((g - 2) >> 1) & 1, abort_flag))) break;
+                        if (!(ok = mbar_wait(k_full(g % kStages), (g / kStages) & 1, abort_flag))) break;
                         tc_fence_after();
-                        issue_s(gs, ic & 1);
-                        ++gs;
-                        if (++js == it.nt) {
-                            mma_commit(q_empty(ic & 1));
-                            ++ic;
-                            js = 0;
-                            q_ready = false;
-                            p += step;
-                            if (p < total) it = dec_item(pre, ri, p, a.rows, a.hkv);
-                            else s_done = true;
+                        const uint64_t kd = k_desc(g % kStages), qd = q_desc(qb);
+#pragma unroll
+                        for (int ks = 0; ks < kD / 16; ++ks) {
+                            const uint32_t koff = ((ks / 4) * C::kHalfBytes + (ks % 4) * 32) >> 4;
+                            const uint32_t qoff = ((ks / 4) * C::kRowsBytes + (ks % 4) * 32) >> 4;
+                            mma_ss(tmem + (g & 1) * kN, kd + koff, qd + qoff, C::kIdescS, ks > 0 ? 1u : 0u);
                         }
-                        progress = true;
-                    }
-                }
-                if (go < gs) {
-                    if (mbar_test(p_full(go & 1), (go >> 1) & 1) && mbar_test(v_full(go % kStages), (go / kStages) & 1) &&
-                        mbar_test(o_free(go & 1), ((go >> 1) & 1) ^ 1)) {
+                        mma_commit(s_full(g & 1));
+                        mma_commit(k_empty(g % kStages));
+                    } else {
+                        // O^T(g) = V(g)^T P^T: A = the V tile read MN-major (M = D), B = P^T
+                        // (K-major, 16 rows), once P(g) is written, V(g) is in and the softmax
+                        // has taken O(g - 2) out of the O buffer
+                        if (!(ok = mbar_wait(p_full(g & 1), (g >> 1) & 1, abort_flag))) break;
+                        if (!(ok = mbar_wait(v_full(g % kStages), (g / kStages) & 1, abort_flag))) break;
+                        if (!(ok = mbar_wait(o_free(g & 1), ((g >> 1) & 1) ^ 1, abort_flag))) break;
                         tc_fence_after();
-                        issue_o(go);
-                        ++go;
-                        progress = true;
+                        const uint64_t vd = v_desc(g % kStages), pd = p_desc(g & 1);
+#pragma unroll
+                        for (int ks = 0; ks < kKeys / 16; ++ks) {
+                            const uint32_t poff = ((ks / 4) * C::kRowsBytes + (ks % 4) * 32) >> 4;
+                            mma_ss(tmem + 2 * kN + (g & 1) * kN, vd + (uint32_t)(ks * 2048 >> 4), pd + poff,
+                                   C::kIdescO, ks > 0 ? 1u : 0u);
+                        }
+                        mma_commit(o_full(g & 1));
+                        mma_commit(v_empty(g % kStages));
                     }
-                } else if (s_done) {
-                    break;  // every tile's S and PV issued
                 }
-                if (progress) {
-                    t_idle = 0;
-                    continue;
-                }
-                if (*abort_flag) {
-                    ok = false;
-                    break;
-                }
-                const uint64_t now = global_timer_ns();
-                if (t_idle == 0) {
-                    t_idle = now;
-                } else if (now - t_idle > kWaitTimeoutNs) {
-                    *abort_flag = 1;
-                    ok = false;
-                    break;
-                }
+                if (!ok) break;
+                if (s_role) mma_commit(q_empty(qb));
+                ++ic;
             }
             if (!ok) report_status(a.status, PCP_ERR_TIMEOUT);
         }
@@ -610,6 +566,8 @@ __global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
                 const float wm = warp_scatter<GP, true>(x, lane);
                 if (lane % kSpan == 0) rm[wq * kMaxG + hl] = wm;
                 bar_sync_named(1 + wg, 128);
+                // O(g - 2) out of TMEM first: PV(g - 2) complete frees P buffer g & 1
+                if (have_prev) accumulate(g_prev, a_prev);
                 float alpha[GP];
                 uint8_t* pbuf = smem + C::kP + (g & 1) * C::kPBytes;
                 // this key's column of P^T: chunk (t % 64) / 8 of each row, swizzled by the row
@@ -646,7 +604,6 @@ __global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_full(g & 1));
-                if (have_prev) accumulate(g_prev, a_prev);
                 g_prev = g;
                 have_prev = true;
 #pragma unroll
