@@ -21,7 +21,7 @@
 //  * warps 8 (K) and 9 (V) produce: per item the block-table entries of its
 //    keys, then per 128-key tile one TMA box per page (bf16: two 64-dim halves,
 //    128-byte swizzled; FP8: the codes, D bytes per row, into the upper half of
-//    the stage), into a 3-stage ring that runs on across items; warp 8 also
+//    the tile), into rings of 3 K and 3 V tiles that run on across items; warp 8 also
 //    loads each item's Q^T (16 q heads of the token from head hk * G, rows past
 //    Hq zero filled);
 //  * lane 0 of warp 10 issues every S^T (once K(g) is in and P(g - 2) has left
@@ -37,7 +37,8 @@
 //    is added into registers with the running rescale; at the end of an item
 //    warpgroup 0 merges the two warpgroups' (max, l, O) and writes the split's
 //    partial;
-//  * FP8 cache: warps 12-15 widen each tile's codes to f16 in place (exact; rows
+//  * FP8 cache: converter warps (12-15 for K and 16-19 for V where G <= 4,
+//    else 12-15 for both) widen each tile's codes to f16 in place (exact; rows
 //    past the last key written as zeros), and Q^T from bf16 to f16 (saturating;
 //    PCP_ERR_RANGE if a q head's element exceeds 65504), so the MMAs take f16
 //    operands; the K descale scales the scores, the V descale the partial;
@@ -63,34 +64,44 @@ constexpr int kD = 128;          // head_dim this kernel takes
 constexpr int kKeys = 128;       // keys per tile: the M of S^T
 constexpr int kN = 16;           // the N of both MMAs
 constexpr int kMaxG = 8;         // q heads per kv head: P's hi and lo rows fit N = 16
-constexpr int kStages = 3;       // K/V tiles in flight per CTA
+#ifndef PCP_DECTC_K_STAGES
+#define PCP_DECTC_K_STAGES 3
+#endif
+#ifndef PCP_DECTC_V_STAGES
+#define PCP_DECTC_V_STAGES 3
+#endif
+constexpr int kKS = PCP_DECTC_K_STAGES;  // K tiles in flight per CTA (a K stage is free after its S)
+constexpr int kVS = PCP_DECTC_V_STAGES;  // V tiles in flight (a V stage is free after its PV)
 constexpr int kProdWarp = 8;     // warp 8: K tiles and Q^T; warp 9: V tiles
 constexpr int kMmaWarp = 10;     // lane 0 issues the S MMAs (the warp owns the TMEM allocation)
 constexpr int kPvWarp = 11;      // lane 0 issues the PV MMAs
 constexpr int kConvWarp0 = 12;
-constexpr int kConvWarps = 4;    // FP8 cache only
-constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kConvThreads = 128;  // FP8: threads widening one tile (one or two such sets)
+// FP8 converter warps: two sets of four (one widens K, the other V) where the
+// softmax fits the registers that 20 warps leave (G <= 4), else one set for both
+__host__ __device__ constexpr int conv_warps(bool f8, int gp) { return f8 ? (gp <= 4 ? 8 : 4) : 0; }
+__host__ __device__ constexpr int tc_threads(bool f8, int gp) { return 32 * (12 + conv_warps(f8, gp)); }
 constexpr int kMaxPages = kDecodeChunk / 8;  // block-table entries of one split (block_size >= 8)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <bool F8>
 struct TcCfg {
-    static constexpr int kThreads = 32 * (kConvWarp0 + (F8 ? kConvWarps : 0));
     static constexpr int kHalfBytes = kKeys * 128;      // 128 keys x 64 dims x 2 bytes
     static constexpr int kTileBytes = 2 * kHalfBytes;   // one K or V tile (16-bit)
-    static constexpr int kStageBytes = 2 * kTileBytes;  // K tile, then V tile
+    static constexpr int kK = 0;                        // K stages
+    static constexpr int kV = kKS * kTileBytes;         // V stages
     static constexpr int kRowsBytes = kN * 128;         // 16 rows x 128 bytes: one 64-element half
     static constexpr int kQBytes = 2 * kRowsBytes;      // Q^T: 16 rows x 128 dims
     static constexpr int kPBytes = 2 * kRowsBytes;      // P^T: 16 rows x 128 keys
-    static constexpr int kQ = kStages * kStageBytes;    // two Q^T buffers
+    static constexpr int kQ = (kKS + kVS) * kTileBytes;  // two Q^T buffers
     static constexpr int kP = kQ + 2 * kQBytes;         // two P^T buffers
     static constexpr int kPre = kP + 2 * kPBytes;       // int32 [kDecTcMaxRows + 1]
     static constexpr int kPages = kPre + ((kDecTcMaxRows + 1) * 4 + 15) / 16 * 16;
     static constexpr int kRed = kPages + 2 * kMaxPages * 4;  // (pages: one list per producer warp)  // float [2 wg][2][4][8] maxima, [2][8][8] sums
     static constexpr int kXchg = kRed + (2 * 2 * 4 * kMaxG + 2 * 8 * kMaxG) * 4;  // float [2][8 + 8 x 128]
     static constexpr int kBar = kXchg + 2 * (kMaxG + kMaxG * kKeys) * 4;
-    static constexpr int kNumBars = 6 * kStages + 7 * 2;
+    static constexpr int kNumBars = 3 * (kKS + kVS) + 7 * 2;
     static constexpr int kMisc = kBar + kNumBars * 8;   // TMEM address, abort flag
     static constexpr int kSmem = kMisc + 16 + 1024;     // + alignment slack
     static constexpr uint32_t kTmemCols = 64;           // S^T x 2, O^T x 2, 16 columns each
@@ -250,7 +261,7 @@ __device__ __forceinline__ float from16(uint16_t x) {
 }
 
 template <bool F8, int GP>
-__global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
+__global__ void __launch_bounds__(tc_threads(F8, GP), 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, PrefillArgs a, float* __restrict__ dec_out,
                      float* __restrict__ dec_lse, int max_splits, int q_rows) {
@@ -265,13 +276,14 @@ __global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
     // stage barriers: 16-bit K / V tile ready, K stage free (its S is done), V
     // stage free (its PV is done), FP8 codes landed
     auto k_full = [&](int s) { return bar0 + 8 * s; };
-    auto v_full = [&](int s) { return bar0 + 8 * (kStages + s); };
-    auto k_empty = [&](int s) { return bar0 + 8 * (2 * kStages + s); };
-    auto v_empty = [&](int s) { return bar0 + 8 * (3 * kStages + s); };
-    auto kc_full = [&](int s) { return bar0 + 8 * (4 * kStages + s); };
-    auto vc_full = [&](int s) { return bar0 + 8 * (5 * kStages + s); };
+    auto k_empty = [&](int s) { return bar0 + 8 * (kKS + s); };
+    auto kc_full = [&](int s) { return bar0 + 8 * (2 * kKS + s); };
+    const uint32_t bv = bar0 + 8 * 3 * kKS;
+    auto v_full = [&](int s) { return bv + 8 * s; };
+    auto v_empty = [&](int s) { return bv + 8 * (kVS + s); };
+    auto vc_full = [&](int s) { return bv + 8 * (2 * kVS + s); };
     // double-buffered: Q^T ready / bf16 Q^T landed (FP8) / free; S^T, P^T, O^T
-    const uint32_t bx = bar0 + 8 * 6 * kStages;
+    const uint32_t bx = bv + 8 * 3 * kVS;
     auto q_full = [&](int b) { return bx + 8 * b; };
     auto qc_full = [&](int b) { return bx + 16 + 8 * b; };
     auto q_empty = [&](int b) { return bx + 32 + 8 * b; };
@@ -292,15 +304,17 @@ __global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
     const int32_t bs = a.block_size;
     const int32_t step = (int32_t)gridDim.x;
 
-    for (int i = threadIdx.x; i <= a.num_rows; i += C::kThreads) pre[i] = a.dec_pre[i];
+    for (int i = threadIdx.x; i <= a.num_rows; i += tc_threads(F8, GP)) pre[i] = a.dec_pre[i];
     if (threadIdx.x == 0) {
-        const uint32_t filled = F8 ? kConvWarps : 1;  // FP8: each converter warp arrives
-        for (int s = 0; s < kStages; ++s) {
+        const uint32_t filled = F8 ? 4 : 1;  // FP8: each warp of the converter set arrives
+        for (int s = 0; s < kKS; ++s) {
             mbar_init(k_full(s), filled);
-            mbar_init(v_full(s), filled);
             mbar_init(k_empty(s), 1);
-            mbar_init(v_empty(s), 1);
             mbar_init(kc_full(s), 1);
+        }
+        for (int s = 0; s < kVS; ++s) {
+            mbar_init(v_full(s), filled);
+            mbar_init(v_empty(s), 1);
             mbar_init(vc_full(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -337,6 +351,7 @@ __global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
         const bool is_k = warp == kProdWarp;
         const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
         int32_t* my_pages = pages + (is_k ? 0 : kMaxPages);
+        const int nst = is_k ? kKS : kVS;
         const int32_t oob = (int32_t)(a.num_blocks * bs);  // a row past the cache: zero fill
         const int ppt = kKeys / bs;                        // pages per tile
         const uint32_t q_bytes = 2u * (uint32_t)q_rows * 128u;
@@ -376,17 +391,17 @@ __global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
                 ++ic;
             }
             for (int j = 0; j < it.nt; ++j) {
-                const int st = gt % kStages;
+                const int st = gt % nst;
                 const int nvalid = min(kKeys, it.hi - it.lo - j * kKeys);
                 const int np = (nvalid + bs - 1) / bs;
-                if (!(ok = mbar_wait_warp(is_k ? k_empty(st) : v_empty(st), ((gt / kStages) & 1) ^ 1, abort_flag)))
+                if (!(ok = mbar_wait_warp(is_k ? k_empty(st) : v_empty(st), ((gt / nst) & 1) ^ 1, abort_flag)))
                     break;
                 const uint32_t fb = full_of(st);
                 if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(np * bs) * (F8 ? kD : 2 * kD));
                 __syncwarp();
                 if (lane < np) {
                     const int32_t y = my_pages[j * ppt + lane];
-                    const uint32_t dst = sbase + st * C::kStageBytes + (is_k ? 0 : C::kTileBytes);
+                    const uint32_t dst = sbase + (is_k ? C::kK : C::kV) + st * C::kTileBytes;
                     if constexpr (F8) {
                         tma_load_3d(dst + C::kHalfBytes + lane * bs * kD, tm, fb, 0, it.hk, y);
                     } else {
@@ -402,8 +417,8 @@ __global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
             // wait (bounded, whatever the abort flag says) for the copies already
             // issued, so that none lands after the CTA has gone
             int no_abort = 0;
-            for (uint32_t g = gt > kStages ? gt - kStages : 0; g < gt; ++g)
-                mbar_wait(full_of(g % kStages), (g / kStages) & 1, &no_abort, 100000000ull);
+            for (uint32_t g = gt > (uint32_t)nst ? gt - nst : 0; g < gt; ++g)
+                mbar_wait(full_of(g % nst), (g / nst) & 1, &no_abort, 100000000ull);
             if (is_k)
                 for (uint32_t i = ic > 2 ? ic - 2 : 0; i < ic; ++i)
                     mbar_wait(F8 ? qc_full(i & 1) : q_full(i & 1), (i >> 1) & 1, &no_abort, 100000000ull);
@@ -416,9 +431,9 @@ __global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
         // that makes it, so the two streams need no ordering between them.
         if (lane == 0) {
             // descriptors of the first k-step; a later k-step moves the start address
-            auto k_desc = [&](int s) { return sdesc_sw128(sbase + s * C::kStageBytes, 16, 1024); };
+            auto k_desc = [&](int s) { return sdesc_sw128(sbase + C::kK + s * C::kTileBytes, 16, 1024); };
             auto v_desc = [&](int s) {
-                return sdesc_sw128(sbase + s * C::kStageBytes + C::kTileBytes, C::kHalfBytes, 1024);
+                return sdesc_sw128(sbase + C::kV + s * C::kTileBytes, C::kHalfBytes, 1024);
             };
             auto q_desc = [&](int b) { return sdesc_sw128(sbase + C::kQ + b * C::kQBytes, 16, 1024); };
             auto p_desc = [&](int b) { return sdesc_sw128(sbase + C::kP + b * C::kPBytes, 16, 1024); };
@@ -435,9 +450,9 @@ __global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
                         // S^T(g) = K(g) Q^T: A = the K tile (K-major, 128 keys), B = Q^T
                         // (K-major, 16 rows); S buffer g & 1 is free once P(g - 2) is written
                         if (g >= 2 && !(ok = mbar_wait(p_full(g & 1), ((g - 2) >> 1) & 1, abort_flag))) break;
-                        if (!(ok = mbar_wait(k_full(g % kStages), (g / kStages) & 1, abort_flag))) break;
+                        if (!(ok = mbar_wait(k_full(g % kKS), (g / kKS) & 1, abort_flag))) break;
                         tc_fence_after();
-                        const uint64_t kd = k_desc(g % kStages), qd = q_desc(qb);
+                        const uint64_t kd = k_desc(g % kKS), qd = q_desc(qb);
 #pragma unroll
                         for (int ks = 0; ks < kD / 16; ++ks) {
                             const uint32_t koff = ((ks / 4) * C::kHalfBytes + (ks % 4) * 32) >> 4;
@@ -445,16 +460,16 @@ __global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
                             mma_ss(tmem + (g & 1) * kN, kd + koff, qd + qoff, C::kIdescS, ks > 0 ? 1u : 0u);
                         }
                         mma_commit(s_full(g & 1));
-                        mma_commit(k_empty(g % kStages));
+                        mma_commit(k_empty(g % kKS));
                     } else {
                         // O^T(g) = V(g)^T P^T: A = the V tile read MN-major (M = D), B = P^T
                         // (K-major, 16 rows), once P(g) is written, V(g) is in and the softmax
                         // has taken O(g - 2) out of the O buffer
                         if (!(ok = mbar_wait(p_full(g & 1), (g >> 1) & 1, abort_flag))) break;
-                        if (!(ok = mbar_wait(v_full(g % kStages), (g / kStages) & 1, abort_flag))) break;
+                        if (!(ok = mbar_wait(v_full(g % kVS), (g / kVS) & 1, abort_flag))) break;
                         if (!(ok = mbar_wait(o_free(g & 1), ((g >> 1) & 1) ^ 1, abort_flag))) break;
                         tc_fence_after();
-                        const uint64_t vd = v_desc(g % kStages), pd = p_desc(g & 1);
+                        const uint64_t vd = v_desc(g % kVS), pd = p_desc(g & 1);
 #pragma unroll
                         for (int ks = 0; ks < kKeys / 16; ++ks) {
                             const uint32_t poff = ((ks / 4) * C::kRowsBytes + (ks % 4) * 32) >> 4;
@@ -462,7 +477,7 @@ __global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
                                    C::kIdescO, ks > 0 ? 1u : 0u);
                         }
                         mma_commit(o_full(g & 1));
-                        mma_commit(v_empty(g % kStages));
+                        mma_commit(v_empty(g % kVS));
                     }
                 }
                 if (!ok) break;
@@ -473,34 +488,44 @@ __global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
         }
     } else if (F8 && warp >= kConvWarp0) {
         // ---------------------------------------------------------------- FP8 converters
-        const int ct = threadIdx.x - kConvWarp0 * 32;
+        // With two sets, warps 12-15 widen the K tiles (and Q^T), warps 16-19 the V
+        // tiles, at the same time; with one set, warps 12-15 do both in turn.
+        constexpr bool kTwoSets = conv_warps(F8, GP) == 8;
+        const int cset = (warp - kConvWarp0) / 4;
+        const bool do_k = !kTwoSets || cset == 0, do_v = !kTwoSets || cset == 1;
+        const int ct = (threadIdx.x - kConvWarp0 * 32) % kConvThreads;
         uint32_t gt = 0, ic = 0;
         int32_t ri = 0;
         bool ok = true;
         for (int32_t p = blockIdx.x; p < total && ok; p += step) {
             const DecItem it = dec_item(pre, ri, p, a.rows, a.hkv);
             const int qb = ic & 1;
-            if (!(ok = mbar_wait_warp(qc_full(qb), (ic >> 1) & 1, abort_flag))) break;
-            if (__any_sync(0xffffffffu, q_to_f16(smem + C::kQ + qb * C::kQBytes, ct, G)) && lane == 0)
-                report_status(a.status, PCP_ERR_RANGE);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(q_full(qb));
+            if (do_k) {
+                if (!(ok = mbar_wait_warp(qc_full(qb), (ic >> 1) & 1, abort_flag))) break;
+                if (__any_sync(0xffffffffu, q_to_f16(smem + C::kQ + qb * C::kQBytes, ct, G)) && lane == 0)
+                    report_status(a.status, PCP_ERR_RANGE);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(q_full(qb));
+            }
             ++ic;
             for (int j = 0; j < it.nt; ++j) {
-                const int st = gt % kStages;
+                const int ks = gt % kKS, vs = gt % kVS;
                 const int nvalid = min(kKeys, it.hi - it.lo - j * kKeys);
-                uint8_t* kt = smem + st * C::kStageBytes;
-                if (!(ok = mbar_wait_warp(kc_full(st), (gt / kStages) & 1, abort_flag))) break;
-                widen_tile(kt, nvalid, ct);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(k_full(st));
-                if (!(ok = mbar_wait_warp(vc_full(st), (gt / kStages) & 1, abort_flag))) break;
-                widen_tile(kt + C::kTileBytes, nvalid, ct);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(v_full(st));
+                if (do_k) {
+                    if (!(ok = mbar_wait_warp(kc_full(ks), (gt / kKS) & 1, abort_flag))) break;
+                    widen_tile(smem + C::kK + ks * C::kTileBytes, nvalid, ct);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(k_full(ks));
+                }
+                if (do_v) {
+                    if (!(ok = mbar_wait_warp(vc_full(vs), (gt / kVS) & 1, abort_flag))) break;
+                    widen_tile(smem + C::kV + vs * C::kTileBytes, nvalid, ct);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(v_full(vs));
+                }
                 ++gt;
             }
         }
@@ -589,10 +614,10 @@ __global__ void __launch_bounds__(TcCfg<F8>::kThreads, 1)
                 if (!F8 && nvalid < kKeys) {
                     // keys past the split's end: zero their V rows (unwritten cache slots in
                     // the last page, stale rows after it) once the tile has landed
-                    const uint32_t g3 = g % kStages;
-                    ok &= mbar_wait_warp(v_full(g3), (g / kStages) & 1, abort_flag);
+                    const uint32_t vs = g % kVS;
+                    ok &= mbar_wait_warp(v_full(vs), (g / kVS) & 1, abort_flag);
                     if (!valid) {
-                        uint8_t* vrow = smem + g3 * C::kStageBytes + C::kTileBytes + t * 128;
+                        uint8_t* vrow = smem + C::kV + vs * C::kTileBytes + t * 128;
 #pragma unroll
                         for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -672,7 +697,7 @@ int launch_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_
     cudaError_t e =
         cudaFuncSetAttribute(decode_tc_kernel<F8, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
-    decode_tc_kernel<F8, GP><<<num_sms(), TcCfg<F8>::kThreads, smem, stream>>>(tq, tk, tv, a, dec_out, dec_lse,
+    decode_tc_kernel<F8, GP><<<num_sms(), tc_threads(F8, GP), smem, stream>>>(tq, tk, tv, a, dec_out, dec_lse,
                                                                               max_splits, q_rows);
     e = cudaGetLastError();
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
