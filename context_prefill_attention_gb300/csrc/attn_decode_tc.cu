@@ -10,6 +10,10 @@
 //   S^T [128 keys x 16] = K [128 keys x D] . Q^T      (Q^T: the G q heads, padded to 16 rows)
 //   O^T [D x 16]        = V^T [D x 128 keys] . P^T    (P^T: 16 rows, P in rows 0..7 and the
 //                                                      rounding remainder of P in rows 8..15)
+// Over an FP8 cache S^T takes the e4m3 codes of K as they are (kind::f8f6f4,
+// 32 dims per MMA) against q written as three e4m3 terms per element after a
+// power-of-two scaling per head, whose sum is the bf16 q (16 or 32 columns:
+// term t of head h in column t * GP + h).
 // The bytes of K and V, read once, set the speed; the tensor cores do the
 // products so that the few instructions per key left are the softmax's.
 //
@@ -37,11 +41,12 @@
 //    is added into registers with the running rescale; at the end of an item
 //    warpgroup 0 merges the two warpgroups' (max, l, O) and writes the split's
 //    partial;
-//  * FP8 cache: converter warps (12-15 for K and 16-19 for V where G <= 4,
-//    else 12-15 for both) widen each tile's codes to f16 in place (exact; rows
-//    past the last key written as zeros), and Q^T from bf16 to f16 (saturating;
-//    PCP_ERR_RANGE if a q head's element exceeds 65504), so the MMAs take f16
-//    operands; the K descale scales the scores, the V descale the partial;
+//  * FP8 cache: the K codes land 128-byte swizzled and are the S operand; the
+//    converter warps (two sets taking alternate tiles where G <= 4, else one)
+//    widen each V tile's codes to f16 in place (exact; rows past the last key
+//    written as zeros) for the f16 PV, and set 0 turns each item's q into its
+//    e4m3 terms and per-head scales; the K descale and the q scale multiply
+//    the scores, the V descale the partial;
 //  * bf16 cache: V rows past a split's last key (unwritten cache slots, or a
 //    stale stage) are zeroed by the softmax threads before the last PV;
 //  * every wait is bounded (PCP_ERR_TIMEOUT); after a timeout the producer
@@ -64,52 +69,78 @@ constexpr int kD = 128;          // head_dim this kernel takes
 constexpr int kKeys = 128;       // keys per tile: the M of S^T
 constexpr int kN = 16;           // the N of both MMAs
 constexpr int kMaxG = 8;         // q heads per kv head: P's hi and lo rows fit N = 16
-#ifndef PCP_DECTC_K_STAGES
-#define PCP_DECTC_K_STAGES 3
-#endif
-#ifndef PCP_DECTC_V_STAGES
-#define PCP_DECTC_V_STAGES 3
-#endif
-constexpr int kKS = PCP_DECTC_K_STAGES;  // K tiles in flight per CTA (a K stage is free after its S)
-constexpr int kVS = PCP_DECTC_V_STAGES;  // V tiles in flight (a V stage is free after its PV)
+constexpr int kTerms = 3;        // FP8: e4m3 terms per q element (their sum is the bf16 q exactly)
 constexpr int kProdWarp = 8;     // warp 8: K tiles and Q^T; warp 9: V tiles
 constexpr int kMmaWarp = 10;     // lane 0 issues the S MMAs (the warp owns the TMEM allocation)
 constexpr int kPvWarp = 11;      // lane 0 issues the PV MMAs
 constexpr int kConvWarp0 = 12;
-constexpr int kConvThreads = 128;  // FP8: threads widening one tile (one or two such sets)
-// FP8 converter warps: two sets of four (one widens K, the other V) where the
-// softmax fits the registers that 20 warps leave (G <= 4), else one set for both
+constexpr int kConvThreads = 128;  // FP8: threads widening one V tile (one or two such sets)
+// FP8 converter warps: two sets of four taking alternate V tiles where the
+// softmax fits the registers that 20 warps leave (G <= 4), else one set
 __host__ __device__ constexpr int conv_warps(bool f8, int gp) { return f8 ? (gp <= 4 ? 8 : 4) : 0; }
 __host__ __device__ constexpr int tc_threads(bool f8, int gp) { return 32 * (12 + conv_warps(f8, gp)); }
 constexpr int kMaxPages = kDecodeChunk / 8;  // block-table entries of one split (block_size >= 8)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <bool F8>
+// Instruction descriptor of kind::f8f6f4 with e4m3 A and B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+    return (1u << 4)                     // D format: f32; A and B format 0: e4m3
+           | ((uint32_t)(N >> 3) << 17)  // N / 8
+           | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+
+template <bool F8, int GP>
 struct TcCfg {
+    // S^T columns: the G q heads (bf16), or their kTerms e4m3 terms (FP8)
+    static constexpr int kNS = F8 ? (kTerms * GP <= 16 ? 16 : 32) : 16;
+    static constexpr int kKS = F8 ? 4 : 3;                 // K tiles in flight (free after their S)
+    static constexpr int kVS = (F8 && GP <= 4) ? 4 : 3;    // V tiles in flight (free after their PV)
     static constexpr int kHalfBytes = kKeys * 128;      // 128 keys x 64 dims x 2 bytes
-    static constexpr int kTileBytes = 2 * kHalfBytes;   // one K or V tile (16-bit)
-    static constexpr int kK = 0;                        // K stages
-    static constexpr int kV = kKS * kTileBytes;         // V stages
+    static constexpr int kTileBytes = 2 * kHalfBytes;   // one 16-bit K or V tile
+    // FP8: a K tile is its codes, 128 keys x 128 bytes (the MMA reads them as e4m3)
+    static constexpr int kKTileBytes = F8 ? kHalfBytes : kTileBytes;
     static constexpr int kRowsBytes = kN * 128;         // 16 rows x 128 bytes: one 64-element half
-    static constexpr int kQBytes = 2 * kRowsBytes;      // Q^T: 16 rows x 128 dims
+    static constexpr int kQBytes = 2 * kRowsBytes;      // bf16 Q^T: 16 rows x 128 dims
+    static constexpr int kQCBytes = F8 ? kNS * 128 : 0;  // FP8: the e4m3 terms of Q^T, kNS rows
     static constexpr int kPBytes = 2 * kRowsBytes;      // P^T: 16 rows x 128 keys
-    static constexpr int kQ = (kKS + kVS) * kTileBytes;  // two Q^T buffers
-    static constexpr int kP = kQ + 2 * kQBytes;         // two P^T buffers
+    static constexpr int kK = 0;                        // K stages
+    static constexpr int kV = kKS * kKTileBytes;        // V stages
+    static constexpr int kQ = kV + kVS * kTileBytes;    // two Q^T buffers (bf16)
+    static constexpr int kQC = kQ + 2 * kQBytes;        // two Q^T term buffers (FP8)
+    static constexpr int kP = kQC + 2 * kQCBytes;       // two P^T buffers
     static constexpr int kPre = kP + 2 * kPBytes;       // int32 [kDecTcMaxRows + 1]
-    static constexpr int kPages = kPre + ((kDecTcMaxRows + 1) * 4 + 15) / 16 * 16;
-    static constexpr int kRed = kPages + 2 * kMaxPages * 4;  // (pages: one list per producer warp)  // float [2 wg][2][4][8] maxima, [2][8][8] sums
-    static constexpr int kXchg = kRed + (2 * 2 * 4 * kMaxG + 2 * 8 * kMaxG) * 4;  // float [2][8 + 8 x 128]
-    static constexpr int kBar = kXchg + 2 * (kMaxG + kMaxG * kKeys) * 4;
-    static constexpr int kNumBars = 3 * (kKS + kVS) + 7 * 2;
+    static constexpr int kPages = kPre + ((kDecTcMaxRows + 1) * 4 + 15) / 16 * 16;  // one list per producer
+    static constexpr int kRed = kPages + 2 * kMaxPages * 4;  // float [2 wg][2][4][8] maxima, [2][8][8] sums
+    static constexpr int kXchg = kRed + (2 * 2 * 4 * kMaxG + 2 * 8 * kMaxG) * 4;  // float [8 + 8 x 128]
+    // FP8: float [4][8] q scales, a ring of four items: the converters run at most
+    // three items ahead of the softmax (they prepare item i + 3 only once S of item
+    // i + 1 is done, which needs the softmax in item i at least)
+    static constexpr int kQs = kXchg + (kMaxG + kMaxG * kKeys) * 4;
+    static constexpr int kBar = kQs + 4 * kMaxG * 4;
+    static constexpr int kNumBars = 2 * kKS + 3 * kVS + 7 * 2 + 4;
     static constexpr int kMisc = kBar + kNumBars * 8;   // TMEM address, abort flag
     static constexpr int kSmem = kMisc + 16 + 1024;     // + alignment slack
-    static constexpr uint32_t kTmemCols = 64;           // S^T x 2, O^T x 2, 16 columns each
-    static constexpr uint32_t kIdescS = F8 ? idesc_f16(128, kN, false, false) : idesc_bf16(128, kN, false, false);
+    static constexpr uint32_t kTmemS = 0, kTmemO = 2 * kNS;  // S^T x 2 (kNS columns), O^T x 2 (16)
+    static constexpr uint32_t kTmemCols = 2 * kNS + 2 * kN <= 64 ? 64 : 128;
+    static constexpr uint32_t kIdescS = F8 ? idesc_e4m3(128, kNS) : idesc_bf16(128, kN, false, false);
     static constexpr uint32_t kIdescO = F8 ? idesc_f16(128, kN, true, false) : idesc_bf16(128, kN, true, false);
 };
-static_assert(TcCfg<true>::kSmem <= 232448 && TcCfg<false>::kSmem <= 232448, "shared memory");
-static_assert(TcCfg<true>::kQ % 1024 == 0 && TcCfg<true>::kP % 1024 == 0, "1024-byte swizzle atoms");
+static_assert(TcCfg<true, 4>::kSmem <= 232448 && TcCfg<true, 8>::kSmem <= 232448 &&
+                  TcCfg<false, 8>::kSmem <= 232448, "shared memory");
+static_assert(TcCfg<true, 4>::kQC % 1024 == 0 && TcCfg<true, 8>::kP % 1024 == 0 &&
+                  TcCfg<false, 8>::kP % 1024 == 0, "1024-byte swizzle atoms");
+
+// D[tmem] (+)= A[smem] * B[smem]^T with e4m3 A and B (kind::f8f6f4, K = 32 per MMA).
+__device__ __forceinline__ void mma_ss_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 
 struct DecItem {
     int32_t ri, req, q_start, hk, split, lo, hi, nt;
@@ -225,28 +256,49 @@ __device__ __forceinline__ void widen_tile(uint8_t* tile, int nvalid, int ct) {
     }
 }
 
-// Q^T (bf16, 16 rows x 128 dims, swizzled) -> f16 in place, by the 128
-// converter threads; each 16-byte chunk holds 8 elements of one row whatever
-// the swizzle, so the conversion is elementwise. Values beyond the largest
-// finite f16 saturate; the return value says whether an element of one of the
-// group's G rows did (the other rows are other heads' q, or stale).
-__device__ __forceinline__ bool q_to_f16(uint8_t* qbuf, int ct, int G) {
-    bool over = false;
+// FP8: the group's q heads as kTerms e4m3 terms each. Input: the bf16 Q^T
+// tile as TMA wrote it (two 64-dim halves of 16 rows, 128-byte swizzled).
+// Output: the swizzled K-major layout of an e4m3 MMA operand, row t * GP + h
+// holding term t of head h (128 codes, 16-byte chunk c of row r at chunk
+// c ^ (r & 7)). Head h is first scaled by 2^(8 - ex), ex the binary exponent
+// of its largest magnitude (frexp), so that every element lies below 256; each
+// term is the e4m3 rounding of what the earlier terms left. Three 4-bit
+// significands hold a bf16 value's 8 bits, so the terms sum to the scaled q
+// exactly, except for elements below 2^-17 of the head's largest, which lose
+// what falls under e4m3's smallest subnormal (2^-9 of the scaled unit).
+// qscale[h] = 2^(ex - 8) undoes the scaling. Warp w of the converter set does
+// heads w and w + 4, lane l dims 4l .. 4l + 3.
+template <int GP>
+__device__ __forceinline__ void q_to_e4m3_terms(const uint8_t* qbf, uint8_t* qc, float* qscale, int w, int lane) {
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int off = (ct + k * kConvThreads) * 16;
-        const int row = (off % (kN * 128)) / 128;
-        uint4 w = *reinterpret_cast<const uint4*>(qbuf + off);
-        uint32_t* e = reinterpret_cast<uint32_t*>(&w);
+    for (int h = w; h < GP; h += 4) {
+        const int d = 4 * lane, half = d >> 6, col = d & 63;
+        const uint2 raw =
+            *reinterpret_cast<const uint2*>(qbf + half * (kN * 128) + h * 128 + (((col >> 3) ^ (h & 7)) << 4) + (col & 7) * 2);
+        float x[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                      __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
+        float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float lo = __uint_as_float(e[i] << 16), hi = __uint_as_float(e[i] & 0xFFFF0000u);
-            over |= row < G && (fabsf(lo) > 65504.f || fabsf(hi) > 65504.f);
-            e[i] = pack_f16x2_satfinite(lo, hi);
+        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        int ex = 0;
+        frexpf(m, &ex);
+        const float f = ldexpf(1.f, 8 - ex);
+        if (lane == 0) qscale[h] = ldexpf(1.f, ex - 8);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] *= f;
+#pragma unroll
+        for (int t = 0; t < kTerms; ++t) {
+            const uint32_t codes = f32x2_to_e4m3x2(x[0], x[1]) | (f32x2_to_e4m3x2(x[2], x[3]) << 16);
+            const int row = t * GP + h;
+            *reinterpret_cast<uint32_t*>(qc + row * 128 + (((d >> 4) ^ (row & 7)) << 4) + (d & 15)) = codes;
+            if (t + 1 < kTerms) {
+                float back[4];
+                e4m3x4_to_f32(codes, back);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) x[e] -= back[e];  // exact: both hold few significant bits
+            }
         }
-        *reinterpret_cast<uint4*>(qbuf + off) = w;
     }
-    return over;
 }
 
 template <bool F8>
@@ -265,7 +317,8 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, PrefillArgs a, float* __restrict__ dec_out,
                      float* __restrict__ dec_lse, int max_splits, int q_rows) {
-    using C = TcCfg<F8>;
+    using C = TcCfg<F8, GP>;
+    constexpr int kKS = C::kKS, kVS = C::kVS, kNS = C::kNS;
     const int32_t total = a.num_units[1];
     if ((int32_t)blockIdx.x >= total) return;
     extern __shared__ uint8_t smem_raw[];
@@ -273,12 +326,11 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
                                                ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + C::kBar;
-    // stage barriers: 16-bit K / V tile ready, K stage free (its S is done), V
-    // stage free (its PV is done), FP8 codes landed
+    // stage barriers: K tile landed, K stage free (its S is done); V tile ready
+    // (FP8: widened), V stage free (its PV is done), FP8 V codes landed
     auto k_full = [&](int s) { return bar0 + 8 * s; };
     auto k_empty = [&](int s) { return bar0 + 8 * (kKS + s); };
-    auto kc_full = [&](int s) { return bar0 + 8 * (2 * kKS + s); };
-    const uint32_t bv = bar0 + 8 * 3 * kKS;
+    const uint32_t bv = bar0 + 8 * 2 * kKS;
     auto v_full = [&](int s) { return bv + 8 * s; };
     auto v_empty = [&](int s) { return bv + 8 * (kVS + s); };
     auto vc_full = [&](int s) { return bv + 8 * (2 * kVS + s); };
@@ -291,13 +343,15 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
     auto p_full = [&](int b) { return bx + 64 + 8 * b; };
     auto o_full = [&](int b) { return bx + 80 + 8 * b; };
     auto o_free = [&](int b) { return bx + 96 + 8 * b; };
+    // FP8: the q scales of item i are in slot i % 4 (for the softmax)
+    auto q_ready = [&](int b) { return bx + 112 + 8 * b; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
     int32_t* pre = reinterpret_cast<int32_t*>(smem + C::kPre);
     int32_t* pages = reinterpret_cast<int32_t*>(smem + C::kPages);
     float* red_m = reinterpret_cast<float*>(smem + C::kRed);  // [warpgroup][tile parity][warp][head]
     float* red_l = red_m + 2 * 2 * 4 * kMaxG;                 // [item parity][warp][head]
-    float* xchg = reinterpret_cast<float*>(smem + C::kXchg);  // [item parity][head max, head x dim O]
+    float* xchg = reinterpret_cast<float*>(smem + C::kXchg);  // [head max, head x dim O]
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int G = a.hq / a.hkv;
@@ -308,9 +362,8 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
     if (threadIdx.x == 0) {
         const uint32_t filled = F8 ? 4 : 1;  // FP8: each warp of the converter set arrives
         for (int s = 0; s < kKS; ++s) {
-            mbar_init(k_full(s), filled);
+            mbar_init(k_full(s), 1);  // the producer's expect_tx (FP8 too: the codes are the operand)
             mbar_init(k_empty(s), 1);
-            mbar_init(kc_full(s), 1);
         }
         for (int s = 0; s < kVS; ++s) {
             mbar_init(v_full(s), filled);
@@ -326,6 +379,7 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
             mbar_init(o_full(b), 1);
             mbar_init(o_free(b), 4);
         }
+        for (int b = 0; b < 4; ++b) mbar_init(q_ready(b), 4);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -355,9 +409,9 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
         const int32_t oob = (int32_t)(a.num_blocks * bs);  // a row past the cache: zero fill
         const int ppt = kKeys / bs;                        // pages per tile
         const uint32_t q_bytes = 2u * (uint32_t)q_rows * 128u;
-        auto full_of = [&](int st) {
-            return F8 ? (is_k ? kc_full(st) : vc_full(st)) : (is_k ? k_full(st) : v_full(st));
-        };
+        // FP8: the K codes are the MMA's operand (full on landing), the V codes go
+        // to the converters first
+        auto full_of = [&](int st) { return is_k ? k_full(st) : (F8 ? vc_full(st) : v_full(st)); };
         uint32_t gt = 0, ic = 0;
         int32_t ri = 0;
         bool ok = true;
@@ -401,9 +455,11 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
                 __syncwarp();
                 if (lane < np) {
                     const int32_t y = my_pages[j * ppt + lane];
-                    const uint32_t dst = sbase + (is_k ? C::kK : C::kV) + st * C::kTileBytes;
+                    const uint32_t dst = sbase + (is_k ? C::kK + st * C::kKTileBytes : C::kV + st * C::kTileBytes);
                     if constexpr (F8) {
-                        tma_load_3d(dst + C::kHalfBytes + lane * bs * kD, tm, fb, 0, it.hk, y);
+                        // K: the codes, 128-byte swizzled, as the e4m3 operand; V: the codes
+                        // where half 1 of the f16 tile goes, unswizzled, for the converters
+                        tma_load_3d(dst + (is_k ? 0 : C::kHalfBytes) + lane * bs * kD, tm, fb, 0, it.hk, y);
                     } else {
                         for (int h = 0; h < 2; ++h)
                             tma_load_3d(dst + h * C::kHalfBytes + lane * bs * 128, tm, fb, h * 64, it.hk, y);
@@ -431,11 +487,13 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
         // that makes it, so the two streams need no ordering between them.
         if (lane == 0) {
             // descriptors of the first k-step; a later k-step moves the start address
-            auto k_desc = [&](int s) { return sdesc_sw128(sbase + C::kK + s * C::kTileBytes, 16, 1024); };
+            auto k_desc = [&](int s) { return sdesc_sw128(sbase + C::kK + s * C::kKTileBytes, 16, 1024); };
             auto v_desc = [&](int s) {
                 return sdesc_sw128(sbase + C::kV + s * C::kTileBytes, C::kHalfBytes, 1024);
             };
-            auto q_desc = [&](int b) { return sdesc_sw128(sbase + C::kQ + b * C::kQBytes, 16, 1024); };
+            auto q_desc = [&](int b) {
+                return sdesc_sw128(sbase + (F8 ? C::kQC + b * C::kQCBytes : C::kQ + b * C::kQBytes), 16, 1024);
+            };
             auto p_desc = [&](int b) { return sdesc_sw128(sbase + C::kP + b * C::kPBytes, 16, 1024); };
             uint32_t g = 0, ic = 0;
             int32_t ri = 0;
@@ -453,11 +511,20 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
                         if (!(ok = mbar_wait(k_full(g % kKS), (g / kKS) & 1, abort_flag))) break;
                         tc_fence_after();
                         const uint64_t kd = k_desc(g % kKS), qd = q_desc(qb);
+                        const uint32_t ts = tmem + C::kTmemS + (g & 1) * kNS;
+                        if constexpr (F8) {
+                            // e4m3 x e4m3, 32 dims (32 bytes of each 128-byte row) per MMA
 #pragma unroll
-                        for (int ks = 0; ks < kD / 16; ++ks) {
-                            const uint32_t koff = ((ks / 4) * C::kHalfBytes + (ks % 4) * 32) >> 4;
-                            const uint32_t qoff = ((ks / 4) * C::kRowsBytes + (ks % 4) * 32) >> 4;
-                            mma_ss(tmem + (g & 1) * kN, kd + koff, qd + qoff, C::kIdescS, ks > 0 ? 1u : 0u);
+                            for (int ks = 0; ks < kD / 32; ++ks)
+                                mma_ss_e4m3(ts, kd + (uint32_t)(ks * 2), qd + (uint32_t)(ks * 2), C::kIdescS,
+                                            ks > 0 ? 1u : 0u);
+                        } else {
+#pragma unroll
+                            for (int ks = 0; ks < kD / 16; ++ks) {
+                                const uint32_t koff = ((ks / 4) * C::kHalfBytes + (ks % 4) * 32) >> 4;
+                                const uint32_t qoff = ((ks / 4) * C::kRowsBytes + (ks % 4) * 32) >> 4;
+                                mma_ss(ts, kd + koff, qd + qoff, C::kIdescS, ks > 0 ? 1u : 0u);
+                            }
                         }
                         mma_commit(s_full(g & 1));
                         mma_commit(k_empty(g % kKS));
@@ -473,7 +540,7 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
 #pragma unroll
                         for (int ks = 0; ks < kKeys / 16; ++ks) {
                             const uint32_t poff = ((ks / 4) * C::kRowsBytes + (ks % 4) * 32) >> 4;
-                            mma_ss(tmem + 2 * kN + (g & 1) * kN, vd + (uint32_t)(ks * 2048 >> 4), pd + poff,
+                            mma_ss(tmem + C::kTmemO + (g & 1) * kN, vd + (uint32_t)(ks * 2048 >> 4), pd + poff,
                                    C::kIdescO, ks > 0 ? 1u : 0u);
                         }
                         mma_commit(o_full(g & 1));
@@ -488,11 +555,10 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
         }
     } else if (F8 && warp >= kConvWarp0) {
         // ---------------------------------------------------------------- FP8 converters
-        // With two sets, warps 12-15 widen the K tiles (and Q^T), warps 16-19 the V
-        // tiles, at the same time; with one set, warps 12-15 do both in turn.
-        constexpr bool kTwoSets = conv_warps(F8, GP) == 8;
-        const int cset = (warp - kConvWarp0) / 4;
-        const bool do_k = !kTwoSets || cset == 0, do_v = !kTwoSets || cset == 1;
+        // Set 0 (warps 12-15) also turns each item's q into its e4m3 terms; the V
+        // tiles are widened by set g % (number of sets).
+        constexpr int kSets = F8 ? conv_warps(F8, GP) / 4 : 1;
+        const int cset = (warp - kConvWarp0) / 4, cw = (warp - kConvWarp0) % 4;
         const int ct = (threadIdx.x - kConvWarp0 * 32) % kConvThreads;
         uint32_t gt = 0, ic = 0;
         int32_t ri = 0;
@@ -500,34 +566,30 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
         for (int32_t p = blockIdx.x; p < total && ok; p += step) {
             const DecItem it = dec_item(pre, ri, p, a.rows, a.hkv);
             const int qb = ic & 1;
-            if (do_k) {
+            if (cset == 0) {
                 if (!(ok = mbar_wait_warp(qc_full(qb), (ic >> 1) & 1, abort_flag))) break;
-                if (__any_sync(0xffffffffu, q_to_f16(smem + C::kQ + qb * C::kQBytes, ct, G)) && lane == 0)
-                    report_status(a.status, PCP_ERR_RANGE);
+                q_to_e4m3_terms<GP>(smem + C::kQ + qb * C::kQBytes, smem + C::kQC + qb * C::kQCBytes,
+                                    reinterpret_cast<float*>(smem + C::kQs) + (ic & 3) * kMaxG, cw, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(q_full(qb));
+                if (lane == 0) {
+                    mbar_arrive(q_full(qb));
+                    mbar_arrive(q_ready(ic & 3));
+                }
             }
             ++ic;
             for (int j = 0; j < it.nt; ++j) {
-                const int ks = gt % kKS, vs = gt % kVS;
+                const uint32_t g = gt + j;
+                if ((int)(g % kSets) != cset) continue;
+                const int vs = g % kVS;
                 const int nvalid = min(kKeys, it.hi - it.lo - j * kKeys);
-                if (do_k) {
-                    if (!(ok = mbar_wait_warp(kc_full(ks), (gt / kKS) & 1, abort_flag))) break;
-                    widen_tile(smem + C::kK + ks * C::kTileBytes, nvalid, ct);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(k_full(ks));
-                }
-                if (do_v) {
-                    if (!(ok = mbar_wait_warp(vc_full(vs), (gt / kVS) & 1, abort_flag))) break;
-                    widen_tile(smem + C::kV + vs * C::kTileBytes, nvalid, ct);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(v_full(vs));
-                }
-                ++gt;
+                if (!(ok = mbar_wait_warp(vc_full(vs), (g / kVS) & 1, abort_flag))) break;
+                widen_tile(smem + C::kV + vs * C::kTileBytes, nvalid, ct);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(v_full(vs));
             }
+            gt += it.nt;
         }
         if (!ok && lane == 0) report_status(a.status, PCP_ERR_TIMEOUT);
     } else {
@@ -548,6 +610,16 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
             const DecItem it = dec_item(pre, ri, p, a.rows, a.hkv);
             const float kd = F8 ? __ldg(a.k_descale + (size_t)it.req * a.hkv + it.hk) : 1.f;
             const float sl2 = a.scale * kd * kLog2e;
+            // FP8: the power of two that undoes each head's q scaling (see q_to_e4m3_terms)
+            float qs[GP];
+#pragma unroll
+            for (int h = 0; h < GP; ++h) qs[h] = 1.f;
+            if constexpr (F8) {
+                ok &= mbar_wait_warp(q_ready(ic & 3), (ic >> 2) & 1, abort_flag);
+#pragma unroll
+                for (int h = 0; h < GP; ++h)
+                    qs[h] = reinterpret_cast<const float*>(smem + C::kQs)[(ic & 3) * kMaxG + h];
+            }
             float m_run[GP], l_t[GP], acc[GP], a_prev[GP];
 #pragma unroll
             for (int h = 0; h < GP; ++h) {
@@ -562,7 +634,7 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
                 ok &= mbar_wait_warp(o_full(g & 1), (g >> 1) & 1, abort_flag);
                 tc_fence_after();
                 uint32_t o[16];
-                tmem_ld16(tmem + lane_base + 2 * kN + (g & 1) * kN, o);
+                tmem_ld16(tmem + lane_base + C::kTmemO + (g & 1) * kN, o);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
@@ -580,12 +652,23 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
                 const bool valid = t < nvalid;
                 ok &= mbar_wait_warp(s_full(g & 1), (g >> 1) & 1, abort_flag);
                 tc_fence_after();
-                uint32_t s[16];
-                tmem_ld16(tmem + lane_base + (g & 1) * kN, s);
+                uint32_t s[kNS];
+                const uint32_t t_s = tmem + lane_base + C::kTmemS + (g & 1) * kNS;
+                if constexpr (kNS == 32) {
+                    tmem_ld32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+                } else {
+                    tmem_ld16(t_s, *reinterpret_cast<uint32_t(*)[16]>(&s[0]));
+                }
                 tmem_wait_ld();
                 float x[GP];
 #pragma unroll
-                for (int h = 0; h < GP; ++h) x[h] = valid ? __uint_as_float(s[h]) * sl2 : -INFINITY;
+                for (int h = 0; h < GP; ++h) {
+                    float sh = __uint_as_float(s[h]);
+                    if constexpr (F8) {  // the q terms' scores, then the head's q scale
+                        sh = (sh + __uint_as_float(s[GP + h]) + __uint_as_float(s[2 * GP + h])) * qs[h];
+                    }
+                    x[h] = valid ? sh * sl2 : -INFINITY;
+                }
                 // tile max per head: over the warp, then over the warpgroup's four warps
                 float* rm = red_m + (wg * 2 + ((g >> 1) & 1)) * 4 * kMaxG;  // [warp][head]
                 const float wm = warp_scatter<GP, true>(x, lane);
@@ -639,7 +722,7 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
             // l per head over this warp's keys; warpgroup 1 hands over its max and O
             const int ip = ic & 1;
             float* rl = red_l + ip * 8 * kMaxG;                  // [warp 0..7][head]
-            float* xm = xchg + ip * (kMaxG + kMaxG * kKeys);     // [head] max, then [head][dim] O
+            float* xm = xchg;                                    // [head] max, then [head][dim] O
             const float wl = warp_scatter<GP, false>(l_t, lane);
             if (lane % kSpan == 0) rl[warp * kMaxG + hl] = wl;
             if (wg == 1) {
@@ -667,6 +750,8 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
                     if (t == 0) dec_lse[slot] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
                 }
             }
+            // warpgroup 1 writes the exchange area of the next item only after this
+            bar_sync_named(4, 256);
         }
         if (stop && threadIdx.x == 0) report_status(a.status, PCP_ERR_TIMEOUT);
     }
@@ -686,14 +771,14 @@ int launch_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_
     const int q_rows = a.hq < kN ? a.hq : kN;
     CUtensorMap tq, tk, tv;
     bool maps = make_box_map(&tq, a.q, kD, 2, a.hq, a.total_q, 64, q_rows, 1, true);
-    if (F8)
-        maps = maps && make_box_map(&tk, a.key_cache, kD, 1, a.hkv, slots, kD, 1, a.block_size, false) &&
+    if (F8)  // K codes 128-byte swizzled (the MMA operand), V codes plain (for the converters)
+        maps = maps && make_box_map(&tk, a.key_cache, kD, 1, a.hkv, slots, kD, 1, a.block_size, true) &&
                make_box_map(&tv, a.value_cache, kD, 1, a.hkv, slots, kD, 1, a.block_size, false);
     else
         maps = maps && make_box_map(&tk, a.key_cache, kD, 2, a.hkv, slots, 64, 1, a.block_size, true) &&
                make_box_map(&tv, a.value_cache, kD, 2, a.hkv, slots, 64, 1, a.block_size, true);
     if (!maps) return PCP_ERR_CUDA;
-    const int smem = TcCfg<F8>::kSmem;
+    const int smem = TcCfg<F8, GP>::kSmem;
     cudaError_t e =
         cudaFuncSetAttribute(decode_tc_kernel<F8, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
