@@ -78,7 +78,8 @@ WorkspaceLayout workspace_layout(int32_t num_rows, int32_t total_q, int32_t num_
     o = align256(o + (size_t)w.nparts * part);
     w.part_lse = o;
     o = align256(o + (size_t)w.nparts * plse);
-    const size_t dec = (size_t)num_rows * num_q_heads * w.max_splits;
+    // two partials per decode split: the tensor-core decode writes one per softmax warpgroup
+    const size_t dec = (size_t)num_rows * num_q_heads * 2 * w.max_splits;
     w.dec_out = o;
     o = align256(o + dec * head_dim * sizeof(float));
     w.dec_lse = o;

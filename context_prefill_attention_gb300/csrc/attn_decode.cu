@@ -353,27 +353,33 @@ __global__ void __launch_bounds__(kDecThreads)
             }
         }
         const int h = hk * G + g;
-        const size_t slot = ((size_t)ri * a.hq + h) * max_splits + split;
+        const size_t slot = ((size_t)ri * a.hq + h) * (2 * max_splits) + split;  // one partial per split
         dec_out[slot * D + d] = L > 0.f ? O / L * vd : 0.f;
         if (d == 0) dec_lse[slot] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
     }
 }
 
-// Merge the per-split partials of every decode row into out (bf16) and lse.
+// Merge the partials of every decode row into out (bf16) and lse: parts_per_split
+// partials for each of the row's splits (the first ones of its 2 x max_splits
+// slots).
 template <int D>
 __global__ void __launch_bounds__(D)
     decode_merge_kernel(PrefillArgs a, const float* __restrict__ dec_out, const float* __restrict__ dec_lse,
-                        int max_splits) {
+                        int max_splits, int parts_per_split) {
     const int ri = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
     if (!a.row_ok[ri]) return;
     const pcp_row_t row = a.rows[ri];
     if (!row.is_decode) return;
-    const int n = min(max_splits, (row.kv_end + kDecodeChunk - 1) / kDecodeChunk);
-    const size_t base = ((size_t)ri * a.hq + h) * max_splits;
+    const int n = parts_per_split * min(max_splits, (row.kv_end + kDecodeChunk - 1) / kDecodeChunk);
+    const size_t base = ((size_t)ri * a.hq + h) * (2 * max_splits);
+    // the loads of several partials in flight at once (each loop is a chain of
+    // loads otherwise)
     float M = -INFINITY;
+#pragma unroll 8
     for (int s = 0; s < n; ++s) M = fmaxf(M, dec_lse[base + s]);
     float W = 0.f, O = 0.f;
     if (M != -INFINITY) {
+#pragma unroll 8
         for (int s = 0; s < n; ++s) {
             const float w = __expf(dec_lse[base + s] - M);
             W += w;
@@ -452,9 +458,12 @@ int launch_decode_dgf(const PrefillArgs& a, float* dec_out, float* dec_lse, int3
     return PCP_OK;
 }
 
-int launch_merge(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits, cudaStream_t stream) {
-    if (a.d == 64) decode_merge_kernel<64><<<dim3(a.num_rows, a.hq), 64, 0, stream>>>(a, dec_out, dec_lse, max_splits);
-    else decode_merge_kernel<128><<<dim3(a.num_rows, a.hq), 128, 0, stream>>>(a, dec_out, dec_lse, max_splits);
+int launch_merge(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits, int pps,
+                 cudaStream_t stream) {
+    if (a.d == 64)
+        decode_merge_kernel<64><<<dim3(a.num_rows, a.hq), 64, 0, stream>>>(a, dec_out, dec_lse, max_splits, pps);
+    else
+        decode_merge_kernel<128><<<dim3(a.num_rows, a.hq), 128, 0, stream>>>(a, dec_out, dec_lse, max_splits, pps);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
     return PCP_OK;
@@ -488,11 +497,16 @@ int launch_decode(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t 
                   cudaStream_t stream) {
     if (a.d != 64 && a.d != 128) return PCP_ERR_UNSUPPORTED;
     int rc = PCP_DECODE_TC ? launch_decode_tc(a, dec_out, dec_lse, max_splits, stream) : PCP_ERR_UNSUPPORTED;
-    if (rc == PCP_ERR_UNSUPPORTED)
+    // partials per split: the tensor-core kernel over an FP8 cache writes one per
+    // softmax warpgroup
+    int pps = a.k_descale ? 2 : 1;
+    if (rc == PCP_ERR_UNSUPPORTED) {
         rc = a.d == 64 ? launch_decode_d<64>(a, dec_out, dec_lse, max_splits, stream)
                        : launch_decode_d<128>(a, dec_out, dec_lse, max_splits, stream);
+        pps = 1;
+    }
     if (rc != PCP_OK) return rc;
-    return launch_merge(a, dec_out, dec_lse, max_splits, stream);
+    return launch_merge(a, dec_out, dec_lse, max_splits, pps, stream);
 }
 
 int launch_separate_merge(const PrefillArgs& a, cudaStream_t stream) {

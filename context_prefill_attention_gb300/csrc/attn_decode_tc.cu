@@ -39,8 +39,9 @@
 //    rounded to 16 bits into shared memory (P^T rows h and 8 + h; the
 //    remainder keeps P's rounding out of the result); each finished tile's O^T
 //    is added into registers with the running rescale; at the end of an item
-//    warpgroup 0 merges the two warpgroups' (max, l, O) and writes the split's
-//    partial;
+//    the split's partial is written: bf16, warpgroup 0 merges the two
+//    warpgroups' (max, l, O); FP8, each warpgroup writes its own partial (two
+//    per split, merged by decode_merge_kernel) and never waits for the other;
 //  * FP8 cache: the K codes land 128-byte swizzled and are the S operand; the
 //    converter warps (two sets taking alternate tiles where G <= 4, else one)
 //    widen each V tile's codes to f16 in place (exact; rows past the last key
@@ -111,12 +112,13 @@ struct TcCfg {
     static constexpr int kP = kQC + 2 * kQCBytes;       // two P^T buffers
     static constexpr int kPre = kP + 2 * kPBytes;       // int32 [kDecTcMaxRows + 1]
     static constexpr int kPages = kPre + ((kDecTcMaxRows + 1) * 4 + 15) / 16 * 16;  // one list per producer
-    static constexpr int kRed = kPages + 2 * kMaxPages * 4;  // float [2 wg][2][4][8] maxima, [2][8][8] sums
-    static constexpr int kXchg = kRed + (2 * 2 * 4 * kMaxG + 2 * 8 * kMaxG) * 4;  // float [8 + 8 x 128]
+    static constexpr int kRed = kPages + 2 * kMaxPages * 4;  // float [2 wg][2][4][8] maxima and sums
+    // bf16: warpgroup 1's max and O of an item, handed to warpgroup 0 (float [8 + 8 x 128])
+    static constexpr int kXchg = kRed + (2 * 2 * 4 * kMaxG) * 2 * 4;
     // FP8: float [4][8] q scales, a ring of four items: the converters run at most
     // three items ahead of the softmax (they prepare item i + 3 only once S of item
     // i + 1 is done, which needs the softmax in item i at least)
-    static constexpr int kQs = kXchg + (kMaxG + kMaxG * kKeys) * 4;
+    static constexpr int kQs = kXchg + (F8 ? 0 : (kMaxG + kMaxG * kKeys) * 4);
     static constexpr int kBar = kQs + 4 * kMaxG * 4;
     static constexpr int kNumBars = 2 * kKS + 3 * kVS + 7 * 2 + 4;
     static constexpr int kMisc = kBar + kNumBars * 8;   // TMEM address, abort flag
@@ -167,13 +169,7 @@ __device__ __forceinline__ DecItem dec_item(const int32_t* pre, int32_t& ri, int
     return it;
 }
 
-// Named barrier `id` over `n` threads (whole warps).
-__device__ __forceinline__ void bar_sync_named(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// Named barrier 3 over the eight softmax warps that also ORs a predicate: every
-// thread gets the same answer, so the warps leave their loops together.
+// Named barrier 3 over the eight softmax warps that also ORs a predicate.
 __device__ __forceinline__ bool bar_all_or(bool pred) {
     uint32_t r;
     asm volatile(
@@ -183,6 +179,27 @@ __device__ __forceinline__ bool bar_all_or(bool pred) {
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
         : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+// Named barrier `id` over `n` threads (whole warps).
+__device__ __forceinline__ void bar_sync_named(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Named barrier `id` over one softmax warpgroup (128 threads) that also ORs a
+// predicate: every thread gets the same answer, so the warps leave their loops
+// together.
+__device__ __forceinline__ bool bar_wg_or(int id, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id)
         : "memory");
     return r != 0;
 }
@@ -350,8 +367,8 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
     int32_t* pre = reinterpret_cast<int32_t*>(smem + C::kPre);
     int32_t* pages = reinterpret_cast<int32_t*>(smem + C::kPages);
     float* red_m = reinterpret_cast<float*>(smem + C::kRed);  // [warpgroup][tile parity][warp][head]
-    float* red_l = red_m + 2 * 2 * 4 * kMaxG;                 // [item parity][warp][head]
-    float* xchg = reinterpret_cast<float*>(smem + C::kXchg);  // [head max, head x dim O]
+    float* red_l = red_m + 2 * 2 * 4 * kMaxG;                 // [item parity][8 warps][head]
+    float* xchg = reinterpret_cast<float*>(smem + C::kXchg);  // bf16: [head max, head x dim O]
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int G = a.hq / a.hkv;
@@ -605,7 +622,7 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
         uint32_t gt = 0, ic = 0;
         int32_t ri = 0;
         bool ok = true;     // every wait of this thread so far completed
-        bool stop = false;  // the eight warps' joint verdict, taken once per item
+        bool stop = false;  // the joint verdict (FP8: of the warpgroup; bf16: of both), once per item
         for (int32_t p = blockIdx.x; p < total && !stop; p += step, ++ic) {
             const DecItem it = dec_item(pre, ri, p, a.rows, a.hkv);
             const float kd = F8 ? __ldg(a.k_descale + (size_t)it.req * a.hkv + it.hk) : 1.f;
@@ -719,41 +736,60 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
             }
             if (have_prev) accumulate(g_prev, a_prev);
             gt += it.nt;
-            // l per head over this warp's keys; warpgroup 1 hands over its max and O
-            const int ip = ic & 1;
-            float* rl = red_l + ip * 8 * kMaxG;                  // [warp 0..7][head]
-            float* xm = xchg;                                    // [head] max, then [head][dim] O
+            float* rl = red_l + (ic & 1) * 8 * kMaxG;  // [warp 0..7][head]
             const float wl = warp_scatter<GP, false>(l_t, lane);
             if (lane % kSpan == 0) rl[warp * kMaxG + hl] = wl;
-            if (wg == 1) {
-#pragma unroll
-                for (int h = 0; h < GP; ++h) {
-                    if (t == 0) xm[h] = m_run[h];
-                    xm[kMaxG + h * kKeys + t] = acc[h];
-                }
-            }
-            if ((stop = bar_all_or(!ok))) break;
-            if (wg == 0) {
-                const float vd = F8 ? __ldg(a.v_descale + (size_t)it.req * a.hkv + it.hk) : 1.f;
+            const float vd = F8 ? __ldg(a.v_descale + (size_t)it.req * a.hkv + it.hk) : 1.f;
+            if constexpr (F8) {
+                // FP8: each warpgroup writes its own partial of the split (a warpgroup
+                // without a tile of the item writes (0, -inf)); decode_merge_kernel
+                // combines the two, so the warpgroups never wait for each other
+                if ((stop = bar_wg_or(1 + wg, !ok))) break;
+                const float* rw = rl + wg * 4 * kMaxG;
 #pragma unroll
                 for (int h = 0; h < GP; ++h) {
                     if (h >= G) continue;
-                    const float L0 = rl[h] + rl[kMaxG + h] + rl[2 * kMaxG + h] + rl[3 * kMaxG + h];
-                    const float L1 = rl[4 * kMaxG + h] + rl[5 * kMaxG + h] + rl[6 * kMaxG + h] + rl[7 * kMaxG + h];
-                    const float m1 = xm[h];
-                    const float M = fmaxf(m_run[h], m1);  // finite: the item has a tile
-                    const float f0 = fast_exp2(m_run[h] - M), f1 = fast_exp2(m1 - M);
-                    const float L = L0 * f0 + L1 * f1;
-                    const float O = acc[h] * f0 + xm[kMaxG + h * kKeys + t] * f1;
-                    const size_t slot = ((size_t)it.ri * a.hq + it.hk * G + h) * max_splits + it.split;
-                    dec_out[slot * kD + t] = L > 0.f ? O / L * vd : 0.f;
-                    if (t == 0) dec_lse[slot] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+                    const float L = rw[h] + rw[kMaxG + h] + rw[2 * kMaxG + h] + rw[3 * kMaxG + h];
+                    const size_t slot =
+                        ((size_t)it.ri * a.hq + it.hk * G + h) * (2 * max_splits) + 2 * it.split + wg;
+                    dec_out[slot * kD + t] = L > 0.f ? acc[h] / L * vd : 0.f;
+                    if (t == 0) dec_lse[slot] = L > 0.f ? (m_run[h] + __log2f(L)) * kLn2 : -INFINITY;
                 }
+            } else {
+                // bf16: warpgroup 1 hands its max and O over, warpgroup 0 merges and
+                // writes the split's one partial (measured faster here than two
+                // partials: this decode streams near the HBM bound, where the extra
+                // partials' bytes show)
+                if (wg == 1) {
+#pragma unroll
+                    for (int h = 0; h < GP; ++h) {
+                        if (t == 0) xchg[h] = m_run[h];
+                        xchg[kMaxG + h * kKeys + t] = acc[h];
+                    }
+                }
+                if ((stop = bar_all_or(!ok))) break;
+                if (wg == 0) {
+#pragma unroll
+                    for (int h = 0; h < GP; ++h) {
+                        if (h >= G) continue;
+                        const float L0 = rl[h] + rl[kMaxG + h] + rl[2 * kMaxG + h] + rl[3 * kMaxG + h];
+                        const float L1 =
+                            rl[4 * kMaxG + h] + rl[5 * kMaxG + h] + rl[6 * kMaxG + h] + rl[7 * kMaxG + h];
+                        const float m1 = xchg[h];
+                        const float M = fmaxf(m_run[h], m1);  // finite: the item has a tile
+                        const float f0 = fast_exp2(m_run[h] - M), f1 = fast_exp2(m1 - M);
+                        const float L = L0 * f0 + L1 * f1;
+                        const float O = acc[h] * f0 + xchg[kMaxG + h * kKeys + t] * f1;
+                        const size_t slot = ((size_t)it.ri * a.hq + it.hk * G + h) * (2 * max_splits) + it.split;
+                        dec_out[slot * kD + t] = L > 0.f ? O / L : 0.f;
+                        if (t == 0) dec_lse[slot] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+                    }
+                }
+                // warpgroup 1 writes the exchange area of the next item only after this
+                bar_sync_named(4, 256);
             }
-            // warpgroup 1 writes the exchange area of the next item only after this
-            bar_sync_named(4, 256);
         }
-        if (stop && threadIdx.x == 0) report_status(a.status, PCP_ERR_TIMEOUT);
+        if (stop && t == 0) report_status(a.status, PCP_ERR_TIMEOUT);
     }
 
     __syncwarp();  // lane 0 of the MMA warp and of the producer worked alone: reconverge first

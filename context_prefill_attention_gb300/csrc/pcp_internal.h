@@ -39,8 +39,8 @@ struct WorkspaceLayout {
     size_t part_out;      // nparts x fp32 [T][Hq][D] (separate-context / KV-shard modes)
     size_t part_lse;      // nparts x fp32 [Hq][T]
     int32_t nparts;
-    size_t dec_out;       // fp32 [num_rows][Hq][max_splits][D]
-    size_t dec_lse;       // fp32 [num_rows][Hq][max_splits]
+    size_t dec_out;       // fp32 [num_rows][Hq][2 x max_splits][D]: decode partials
+    size_t dec_lse;       // fp32 [num_rows][Hq][2 x max_splits]
     size_t total;
     int64_t max_units;
     int32_t max_splits;
@@ -125,7 +125,9 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 int launch_decode(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
                   cudaStream_t stream);
 // The tensor-core decode (head_dim 128, up to 8 q heads per kv head, at most
-// kDecTcMaxRows rows); PCP_ERR_UNSUPPORTED for any other shape.
+// kDecTcMaxRows rows); PCP_ERR_UNSUPPORTED for any other shape. Over an FP8
+// cache it writes two partials per split (slots 2 split and 2 split + 1 of the
+// row's 2 x max_splits), else one (slot split).
 constexpr int kDecTcMaxRows = 1024;
 int launch_decode_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
                      cudaStream_t stream);
