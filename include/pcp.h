@@ -172,7 +172,9 @@ size_t pcp_attn_workspace_size(int32_t num_rows, int32_t total_q, int32_t num_q_
  * pcp_attn_varlen — device. Attention of every planned row in one call:
  * prefill rows (end-aligned causal over the new tokens, plus the non-causal
  * context over the cached prefix) on the tensor cores, decode rows on a
- * split-KV bandwidth path. ("Feat/pcp qwen36 hybrid", "Changes"; "[MRv2]
+ * split-KV bandwidth path (tensor cores for head_dim 128 with up to 8 q heads
+ * per kv head and at most 1024 rows, P carried as bf16 hi + lo; CUDA cores in
+ * fp32 otherwise). ("Feat/pcp qwen36 hybrid", "Changes"; "[MRv2]
  * FlashAttention PCP support ...", overview and the context-pass call returning
  * (ctx_out, ctx_lse); "Carry the row plan ...", "What made it removable".)
  *
@@ -279,8 +281,12 @@ int pcp_kv_cache_write_fp8(const void* k, const void* v, const int64_t* slot_map
  * rows' products run in f16: the codes are widened to f16 exactly, q is
  * converted from bf16 to f16 (exact for |q| <= 65504; larger elements saturate
  * to +-65504 and set *status = PCP_ERR_RANGE), and the softmax weights P are
- * rounded to f16 (finer than the bf16 weights of pcp_attn_varlen); the
- * descales multiply the fp32 scores and outputs.
+ * rounded to f16 (finer than the bf16 weights of pcp_attn_varlen). Decode rows
+ * (head_dim 128, up to 8 q heads per kv head): the scores take the K codes as
+ * e4m3 operands against q written as three e4m3 terms per element after a
+ * power-of-two scale per head (their sum is the bf16 q), V is widened to f16
+ * and P carried as two f16 parts; other decode rows run in fp32. The descales
+ * multiply the fp32 scores and outputs.
  * key_cache, value_cache: [num_blocks][block_size][Hkv][D] bytes (as written
  * by pcp_kv_cache_write_fp8); k_descale, v_descale: device fp32
  * [num_reqs][Hkv] (inputs: out and lse must not overlap them). Every other
