@@ -11,9 +11,9 @@
 //   O^T [D x 16]        = V^T [D x 128 keys] . P^T    (P^T: 16 rows, P in rows 0..7 and the
 //                                                      rounding remainder of P in rows 8..15)
 // Over an FP8 cache S^T takes the e4m3 codes of K as they are (kind::f8f6f4,
-// 32 dims per MMA) against q written as three e4m3 terms per element after a
-// power-of-two scaling per head, whose sum is the bf16 q (16 or 32 columns:
-// term t of head h in column t * GP + h).
+// 32 dims per MMA) against q written as two e4m3 terms per element after a
+// power-of-two scaling per head, whose sum is the bf16 q (term t of head h in
+// column t * GP + h).
 // The bytes of K and V, read once, set the speed; the tensor cores do the
 // products so that the few instructions per key left are the softmax's.
 //
@@ -70,7 +70,7 @@ constexpr int kD = 128;          // head_dim this kernel takes
 constexpr int kKeys = 128;       // keys per tile: the M of S^T
 constexpr int kN = 16;           // the N of both MMAs
 constexpr int kMaxG = 8;         // q heads per kv head: P's hi and lo rows fit N = 16
-constexpr int kTerms = 3;        // FP8: e4m3 terms per q element (their sum is the bf16 q exactly)
+constexpr int kTerms = 2;        // FP8: e4m3 terms per q element (their sum is the bf16 q exactly)
 constexpr int kProdWarp = 8;     // warp 8: K tiles and Q^T; warp 9: V tiles
 constexpr int kMmaWarp = 10;     // lane 0 issues the S MMAs (the warp owns the TMEM allocation)
 constexpr int kPvWarp = 11;      // lane 0 issues the PV MMAs
@@ -83,13 +83,6 @@ __host__ __device__ constexpr int tc_threads(bool f8, int gp) { return 32 * (12 
 constexpr int kMaxPages = kDecodeChunk / 8;  // block-table entries of one split (block_size >= 8)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-
-// Instruction descriptor of kind::f8f6f4 with e4m3 A and B, fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
-    return (1u << 4)                     // D format: f32; A and B format 0: e4m3
-           | ((uint32_t)(N >> 3) << 17)  // N / 8
-           | ((uint32_t)(M >> 4) << 24);  // M / 16
-}
 
 template <bool F8, int GP>
 struct TcCfg {
@@ -133,16 +126,6 @@ static_assert(TcCfg<true, 4>::kSmem <= 232448 && TcCfg<true, 8>::kSmem <= 232448
 static_assert(TcCfg<true, 4>::kQC % 1024 == 0 && TcCfg<true, 8>::kP % 1024 == 0 &&
                   TcCfg<false, 8>::kP % 1024 == 0, "1024-byte swizzle atoms");
 
-// D[tmem] (+)= A[smem] * B[smem]^T with e4m3 A and B (kind::f8f6f4, K = 32 per MMA).
-__device__ __forceinline__ void mma_ss_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 
 struct DecItem {
     int32_t ri, req, q_start, hk, split, lo, hi, nt;
@@ -278,15 +261,20 @@ __device__ __forceinline__ void widen_tile(uint8_t* tile, int nvalid, int ct) {
 // Output: the swizzled K-major layout of an e4m3 MMA operand, row t * GP + h
 // holding term t of head h (128 codes, 16-byte chunk c of row r at chunk
 // c ^ (r & 7)). Head h is first scaled by 2^(8 - ex), ex the binary exponent
-// of its largest magnitude (frexp), so that every element lies below 256; each
-// term is the e4m3 rounding of what the earlier terms left. Three 4-bit
-// significands hold a bf16 value's 8 bits, so the terms sum to the scaled q
-// exactly, except for elements below 2^-17 of the head's largest, which lose
-// what falls under e4m3's smallest subnormal (2^-9 of the scaled unit).
-// qscale[h] = 2^(ex - 8) undoes the scaling. Warp w of the converter set does
-// heads w and w + 4, lane l dims 4l .. 4l + 3.
+// of its largest magnitude (frexp), so that every element lies below 256. The
+// first term is the e4m3 rounding of the scaled element x (4 significant bits);
+// the remainder x - term is a multiple of x's last bit no larger than 8 of
+// them (x has 8 significant bits), so it is an e4m3 value too and the two
+// terms sum to x exactly, unless the remainder falls under e4m3's smallest
+// subnormal (2^-9 of the scaled unit: elements below 2^-10 of the head's
+// largest can lose bits, at most 2^-18 of it). qscale[h] = 2^(ex - 8) undoes
+// the scaling. Warp w of the converter set does heads w and w + 4, lane l dims
+// 4l .. 4l + 3. Returns whether an element of one of the G real heads lies
+// beyond +-65504 (reported as PCP_ERR_RANGE, as the prefill rows' q is).
 template <int GP>
-__device__ __forceinline__ void q_to_e4m3_terms(const uint8_t* qbf, uint8_t* qc, float* qscale, int w, int lane) {
+__device__ __forceinline__ bool q_to_e4m3_terms(const uint8_t* qbf, uint8_t* qc, float* qscale, int w, int lane,
+                                                int G) {
+    bool over = false;
 #pragma unroll
     for (int h = w; h < GP; h += 4) {
         const int d = 4 * lane, half = d >> 6, col = d & 63;
@@ -297,6 +285,7 @@ __device__ __forceinline__ void q_to_e4m3_terms(const uint8_t* qbf, uint8_t* qc,
         float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        over |= h < G && m > 65504.f;
         int ex = 0;
         frexpf(m, &ex);
         const float f = ldexpf(1.f, 8 - ex);
@@ -316,6 +305,7 @@ __device__ __forceinline__ void q_to_e4m3_terms(const uint8_t* qbf, uint8_t* qc,
             }
         }
     }
+    return over;
 }
 
 template <bool F8>
@@ -585,8 +575,10 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
             const int qb = ic & 1;
             if (cset == 0) {
                 if (!(ok = mbar_wait_warp(qc_full(qb), (ic >> 1) & 1, abort_flag))) break;
-                q_to_e4m3_terms<GP>(smem + C::kQ + qb * C::kQBytes, smem + C::kQC + qb * C::kQCBytes,
-                                    reinterpret_cast<float*>(smem + C::kQs) + (ic & 3) * kMaxG, cw, lane);
+                if (q_to_e4m3_terms<GP>(smem + C::kQ + qb * C::kQBytes, smem + C::kQC + qb * C::kQCBytes,
+                                        reinterpret_cast<float*>(smem + C::kQs) + (ic & 3) * kMaxG, cw, lane, G) &&
+                    lane == 0)
+                    report_status(a.status, PCP_ERR_RANGE);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -682,7 +674,7 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
                 for (int h = 0; h < GP; ++h) {
                     float sh = __uint_as_float(s[h]);
                     if constexpr (F8) {  // the q terms' scores, then the head's q scale
-                        sh = (sh + __uint_as_float(s[GP + h]) + __uint_as_float(s[2 * GP + h])) * qs[h];
+                        sh = (sh + __uint_as_float(s[GP + h])) * qs[h];
                     }
                     x[h] = valid ? sh * sl2 : -INFINITY;
                 }

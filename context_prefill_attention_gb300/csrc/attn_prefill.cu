@@ -32,14 +32,17 @@
 //    warpgroup's softmax overlaps the other head's MMAs;
 //  * every mbarrier wait is bounded: a wait that runs out sets PCP_ERR_TIMEOUT
 //    in the status word and the CTA winds down, freeing its TMEM;
-//  * FP8 (e4m3) cache: the producer's TMA brings the codes in (for D = 128 into
-//    the upper half of the stage they will be converted into, for D = 64 into
-//    a staging area), warps 10-11 convert them to f16 in the 128-byte-swizzled
-//    layout the MMA reads (one conversion per two codes, exact: every e4m3 value
-//    is an f16 value) and each item's Q tiles from bf16 to f16 in place, so the
-//    MMAs of this variant take f16 operands (P is stored as f16 too); the
-//    per-(request, kv head) descales fold into the softmax scale (K) and the
-//    epilogue's normalisation (V).
+//  * FP8 (e4m3) cache: the producer's TMA brings the codes in. D = 128: the K
+//    codes land 128-byte swizzled and S takes them as e4m3 operands (kind::
+//    f8f6f4) against each item's q, which the softmax threads rewrite (a row
+//    each) as two e4m3 terms per element after a power-of-two scale per row
+//    (their sum is the bf16 q);
+//    the V codes land in the upper half of their stage and warps 10-11 widen
+//    them to f16 (one conversion per two codes, exact). D = 64: K and V codes
+//    are widened to f16 from a staging area and q converted to f16. P is
+//    stored as f16 and PV takes f16 operands; the per-(request, kv head)
+//    descales fold into the softmax scale (K) and the epilogue's normalisation
+//    (V).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -104,24 +107,29 @@ struct Cfg {
     // staging area after the V stages.
     static constexpr int kCodeBytes = kBlockN * D;
     static constexpr bool kInPlace = D == 128;
+    // FP8, D = 128: S takes the K codes as e4m3 operands (128 bytes per key, one
+    // 128-byte swizzle atom wide, at the start of the K stage) against q written
+    // as two e4m3 terms per element; only V is widened to f16
+    static constexpr bool kE4 = F8 && D == 128;
     static constexpr int kCK = kV + kNV * kTileBytes;
     static constexpr int kCV = kCK + (F8 && !kInPlace ? kNK * kCodeBytes : 0);
     static constexpr int kBar = kCV + (F8 && !kInPlace ? kNV * kCodeBytes : 0);
     __host__ __device__ static constexpr int code_k(int s) {
-        return kInPlace ? kK + s * kTileBytes + kHalfBytes : kCK + s * kCodeBytes;
+        return kE4 ? kK + s * kTileBytes : kInPlace ? kK + s * kTileBytes + kHalfBytes : kCK + s * kCodeBytes;
     }
     __host__ __device__ static constexpr int code_v(int s) {
         return kInPlace ? kV + s * kTileBytes + kHalfBytes : kCV + s * kCodeBytes;
     }
     static constexpr int kNumBars = 2 + 2 * kNK + 2 * kNV + 8 + kNK + kNV + 1;  // + FP8: Q landed
-    static constexpr int kMisc = kBar + kNumBars * 8;      // tmem address, abort flag, item ring
+    static constexpr int kMisc = kBar + kNumBars * 8;      // tmem address, abort flag
     static constexpr int kSmem = kMisc + 16 + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 512;
     __host__ __device__ static constexpr uint32_t tmem_s(int g) { return g ? 128u : 0u; }
     __host__ __device__ static constexpr uint32_t tmem_o(int g) { return g ? 256u + D : 256u; }
     // FP8 cache: the codes are widened to f16 (exact), q converted to f16 and P
     // stored as f16, so the MMAs take f16 operands; bf16 cache: bf16 operands
-    static constexpr uint32_t kIdescS = F8 ? idesc_f16(128, 128, false, false) : idesc_bf16(128, 128, false, false);
+    static constexpr uint32_t kIdescS =
+        kE4 ? idesc_e4m3(128, 128) : F8 ? idesc_f16(128, 128, false, false) : idesc_bf16(128, 128, false, false);
     static constexpr uint32_t kIdescO = F8 ? idesc_f16(128, D, false, true) : idesc_bf16(128, D, false, true);
 };
 
@@ -231,6 +239,60 @@ __device__ __forceinline__ bool convert_q_f16(uint8_t* q_base, int bytes, int ct
     return over;
 }
 
+// FP8, D = 128: row r of a head's Q tile (bf16, two 64-dim halves of 128 rows,
+// 128-byte swizzled) rewritten in place as two e4m3 terms: term t at
+// t * kHalfBytes + r * 128, 16-byte chunk c at c ^ (r & 7), the K-major layout
+// of an e4m3 MMA operand. The row is first scaled by 2^(8 - ex), ex the binary
+// exponent of its largest magnitude (frexp), so that its elements lie below
+// 256; the first term is the e4m3 rounding of a scaled element x (4 significant
+// bits), and the remainder, a multiple of x's last bit no larger than 8 of them
+// (x has bf16's 8 significant bits), is an e4m3 value too: the terms sum to x
+// exactly unless the remainder falls under e4m3's smallest subnormal (2^-9 of
+// the scaled unit; an element below 2^-10 of its row's largest can lose bits,
+// at most 2^-18 of that largest). Run by the row's own softmax thread, which
+// reads the whole row before writing it. Returns 2^(ex - 8), the factor that
+// undoes the scaling; *over is set if an element lies beyond +-65504.
+__device__ __forceinline__ float q_row_to_e4m3(uint8_t* tile, int r, bool* over) {
+    constexpr int kHalf = 128 * 128;
+    uint4 raw[16];  // bf16 chunk c of half h (dims 64h + 8c ..) in raw[8h + c]
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            raw[8 * h + c] = *reinterpret_cast<const uint4*>(tile + h * kHalf + r * 128 + ((c ^ (r & 7)) << 4));
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            m = fmax3(m, fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xFFFF0000u)));
+    }
+    *over = m > 65504.f;
+    int ex = 0;
+    frexpf(m, &ex);
+    const float f = ldexpf(1.f, 8 - ex);
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {  // codes 16 cc .. 16 cc + 15 = bf16 chunks 2 cc, 2 cc + 1
+        uint32_t c1[4], c2[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint4 u = raw[2 * cc + k / 2];
+            const uint32_t w0 = (k & 1) ? u.z : u.x, w1 = (k & 1) ? u.w : u.y;
+            const float v0 = __uint_as_float(w0 << 16) * f, v1 = __uint_as_float(w0 & 0xFFFF0000u) * f;
+            const float v2 = __uint_as_float(w1 << 16) * f, v3 = __uint_as_float(w1 & 0xFFFF0000u) * f;
+            c1[k] = f32x2_to_e4m3x2(v0, v1) | (f32x2_to_e4m3x2(v2, v3) << 16);
+            float back[4];
+            e4m3x4_to_f32(c1[k], back);
+            c2[k] = f32x2_to_e4m3x2(v0 - back[0], v1 - back[1]) | (f32x2_to_e4m3x2(v2 - back[2], v3 - back[3]) << 16);
+        }
+        const int chunk = (cc ^ (r & 7)) << 4;
+        *reinterpret_cast<uint4*>(tile + r * 128 + chunk) = make_uint4(c1[0], c1[1], c1[2], c1[3]);
+        *reinterpret_cast<uint4*>(tile + kHalf + r * 128 + chunk) = make_uint4(c2[0], c2[1], c2[2], c2[3]);
+    }
+    return ldexpf(1.f, ex - 8);
+}
+
 // S = Q_slot K^T over D (K-major A and B, 128-byte swizzle). q_desc / k_desc are
 // the descriptors of the tiles' first k-step; a later k-step only moves the start
 // address (the descriptor's low 14 bits, in 16-byte units), so each MMA costs one
@@ -238,10 +300,21 @@ __device__ __forceinline__ bool convert_q_f16(uint8_t* q_base, int bytes, int ct
 // critical path of the tensor pipe).
 template <int D, bool F8>
 __device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint64_t q_desc, uint64_t k_desc) {
+    if constexpr (Cfg<D, F8>::kE4) {
+        // e4m3: q's two term tiles (term t at + t * kHalfBytes) against the K codes,
+        // 32 dims (32 bytes of each 128-byte row) per MMA: the same 8 MMAs
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t off = ((ks / 4) * Cfg<D>::kHalfBytes + (ks % 4) * 32) >> 4;
-        mma_ss(tmem_s, q_desc + off, k_desc + off, Cfg<D, F8>::kIdescS, ks > 0 ? 1u : 0u);
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int ks = 0; ks < D / 32; ++ks)
+                mma_ss_e4m3(tmem_s, q_desc + (uint32_t)((t * Cfg<D>::kHalfBytes + ks * 32) >> 4),
+                            k_desc + (uint32_t)(ks * 2), Cfg<D, F8>::kIdescS, (t | ks) ? 1u : 0u);
+    } else {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = ((ks / 4) * Cfg<D>::kHalfBytes + (ks % 4) * 32) >> 4;
+            mma_ss(tmem_s, q_desc + off, k_desc + off, Cfg<D, F8>::kIdescS, ks > 0 ? 1u : 0u);
+        }
     }
 }
 
@@ -296,12 +369,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t bs = a.block_size;
 
     if (threadIdx.x == 0) {
-        mbar_init(q_full, F8 ? kConvThreads / 32 : 1);
+        // q_full: the TMA (bf16), the converter warps (FP8, D = 64) or the softmax
+        // warps of the item's head slots (FP8, D = 128)
+        mbar_init(q_full, C::kE4 ? (dual ? 8 : 4) : F8 ? kConvThreads / 32 : 1);
         if (F8) mbar_init(qc_full, 1);
-        mbar_init(q_empty, 1);
+        // both head slots' warpgroups free Q when an item has two (each reads its
+        // rows' q scales at the item's start, before its last tile)
+        mbar_init(q_empty, dual ? 2 : 1);
         // FP8: a stage is full when both converter warps have arrived
         const uint32_t fill_count = F8 ? kConvThreads / 32 : 1;
-        for (int s = 0; s < kNK; ++s) { mbar_init(k_full(s), fill_count); mbar_init(k_empty(s), 1); }
+        // (FP8, D = 128: the K codes are the MMA operand, full once TMA has landed them)
+        for (int s = 0; s < kNK; ++s) { mbar_init(k_full(s), C::kE4 ? 1 : fill_count); mbar_init(k_empty(s), 1); }
         for (int s = 0; s < kNV; ++s) { mbar_init(v_full(s), fill_count); mbar_init(v_empty(s), 1); }
         if (F8) {
             for (int s = 0; s < kNK; ++s) mbar_init(kc_full(s), 1);
@@ -384,11 +462,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ks = kt % kNK;
                 if (!(ok = mbar_wait_warp(k_empty(ks), ((kt / kNK) & 1) ^ 1, abort_flag))) break;
                 if constexpr (F8) {
-                    // codes: one box of bs rows x D bytes per page
-                    if (lane == 0) mbar_arrive_expect_tx(kc_full(ks), C::kCodeBytes);
+                    // codes: one box of bs rows x D bytes per page (D = 128: 128-byte
+                    // swizzled, the e4m3 operand itself; else for the converters)
+                    const uint32_t kb = C::kE4 ? k_full(ks) : kc_full(ks);
+                    if (lane == 0) mbar_arrive_expect_tx(kb, C::kCodeBytes);
                     __syncwarp();
                     if (lane < pages)
-                        tma_load_3d(sbase + C::code_k(ks) + lane * bs * D, &tm_k, kc_full(ks), 0, it.hk, y);
+                        tma_load_3d(sbase + C::code_k(ks) + lane * bs * D, &tm_k, kb, 0, it.hk, y);
                 } else {
                     // K(j) and V(j) on one barrier: wait for both stages first
                     const int vs = vt % kNV;
@@ -434,21 +514,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, a.num_rows, bs);
             if (it.n_tiles == 0) continue;
             // the item's Q tiles: bf16 -> f16 in place, then ready for the MMAs
-            if (!(ok = mbar_wait_warp(qc_full, cq & 1, abort_flag))) break;
-            ++cq;
-            if (__any_sync(0xffffffffu, convert_q_f16(smem + C::kQ, it.nslots * C::kTileBytes, ct)) && lane == 0)
-                report_status(a.status, PCP_ERR_RANGE);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(q_full);
-            for (int32_t j = 0; j < it.n_tiles && ok; ++j) {
-                const int ks = kt % kNK;
-                if (!(ok = mbar_wait_warp(kc_full(ks), (kt / kNK) & 1, abort_flag))) break;
-                convert_codes<D>(smem + C::code_k(ks), smem + C::kK + ks * C::kTileBytes, ct);
+            // (D = 128: the softmax threads write each row's e4m3 terms instead)
+            if constexpr (!C::kE4) {
+                if (!(ok = mbar_wait_warp(qc_full, cq & 1, abort_flag))) break;
+                ++cq;
+                if (__any_sync(0xffffffffu, convert_q_f16(smem + C::kQ, it.nslots * C::kTileBytes, ct)) && lane == 0)
+                    report_status(a.status, PCP_ERR_RANGE);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(k_full(ks));
-                ++kt;
+                if (lane == 0) mbar_arrive(q_full);
+            }
+            for (int32_t j = 0; j < it.n_tiles && ok; ++j) {
+                if constexpr (!C::kE4) {
+                    const int ks = kt % kNK;
+                    if (!(ok = mbar_wait_warp(kc_full(ks), (kt / kNK) & 1, abort_flag))) break;
+                    convert_codes<D>(smem + C::code_k(ks), smem + C::kK + ks * C::kTileBytes, ct);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(k_full(ks));
+                    ++kt;
+                }
                 const int vs = vt % kNV;
                 if (!(ok = mbar_wait_warp(vc_full(vs), (vt / kNV) & 1, abort_flag))) break;
                 convert_codes<D>(smem + C::code_v(vs), smem + C::kV + vs * C::kTileBytes, ct);
@@ -557,12 +642,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // on the last tile, Q are free); O done frees the item's last V. Its thread 0
         // arrives, so that the MMA issuer spends no commits on them.
         const bool releaser = g == slots_per_item - 1;
-        uint32_t rel_k = 0, rel_v = 0;
+        uint32_t rel_k = 0, rel_v = 0, cq = 0;
         bool ok = true;
         for (int32_t round = 0; ok; ++round) {
             const int32_t idx = item_of_round(round);
             if (idx >= total_items) break;
             const Item it = decode_item(a.units, idx, slots_per_unit, dual, G, a.rows, a.num_rows, bs);
+            const uint32_t my_q = cq;  // Q loads so far (items with key tiles)
+            if (it.n_tiles > 0) ++cq;
             if (g >= it.nslots) continue;
             const int h = it.h0 + g;
             // FP8: the K descale scales every score (the V descale the output, below);
@@ -574,22 +661,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t tok = it.q_tok0 + r;
             float m = -INFINITY, l = 0.f;
             const int n = it.n_tiles;
+            // FP8, D = 128: once the item's bf16 Q has landed, this thread rewrites its
+            // own row as e4m3 terms (the softmax warps are idle until the item's first S)
+            // and keeps the row's q scale
+            float qs_row = 1.f;
+            if constexpr (C::kE4) {
+                if (n > 0) {
+                    if (!(ok = mbar_wait_warp(qc_full, my_q & 1, abort_flag))) break;
+                    bool over = false;
+                    qs_row = q_row_to_e4m3(smem + C::kQ + g * C::kTileBytes, r, &over);
+                    if (over) report_status(a.status, PCP_ERR_RANGE);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if ((threadIdx.x & 31) == 0) mbar_arrive(q_full);
+                }
+            }
             for (int j = 0; j < n && ok; ++j) {
                 if (!(ok = mbar_wait_warp(s_full(g), sph, abort_flag))) break;
                 sph ^= 1;
                 if (releaser) {
                     if (r == 0) {
                         mbar_arrive(k_empty(rel_k % kNK));
-                        if (j == n - 1) mbar_arrive(q_empty);
                         if (j > 0) mbar_arrive(v_empty(rel_v % kNV));
                     }
                     ++rel_k;
                     if (j > 0) ++rel_v;
                 }
+                if (j == n - 1 && (releaser || dual) && r == 0) mbar_arrive(q_empty);
                 tc_fence_after();
                 uint32_t s[128];
                 float* sf = reinterpret_cast<float*>(s);
-                const float sl2 = F8 ? a.scale * __ldg(kd_ptr) * kLog2e : a.scale * kLog2e;
+                const float sl2 = F8 ? a.scale * __ldg(kd_ptr) * kLog2e * qs_row : a.scale * kLog2e;
                 const int32_t key0 = it.kb + j * kBlockN;
                 const bool full = key0 >= it.k_lo && key0 + kBlockN <= it.k_hi &&
                                   key0 + kBlockN - 1 <= it.pos0;
@@ -1013,7 +1115,9 @@ template <int D, bool F8>
 int launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
     CUtensorMap tq, tk, tv;
     const int64_t slots = a.num_blocks * a.block_size;
-    const bool maps = F8 ? make_row_map(&tk, a.key_cache, D, 1, a.hkv, slots, a.block_size) &&
+    // FP8: K codes 128-byte swizzled where they are the MMA operand (D = 128)
+    const bool maps = F8 ? (Cfg<D, F8>::kE4 ? make_box_map(&tk, a.key_cache, D, 1, a.hkv, slots, D, 1, a.block_size, true)
+                                            : make_row_map(&tk, a.key_cache, D, 1, a.hkv, slots, a.block_size)) &&
                                make_row_map(&tv, a.value_cache, D, 1, a.hkv, slots, a.block_size)
                          : make_map(&tk, a.key_cache, D, a.hkv, slots, a.block_size) &&
                                make_map(&tv, a.value_cache, D, a.hkv, slots, a.block_size);

@@ -180,6 +180,24 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b
            | ((uint32_t)(M >> 4) << 24);             // M / 16
 }
 
+// Instruction descriptor of kind::f8f6f4 with e4m3 A and B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+    return (1u << 4)                     // D format: f32; A and B format 0: e4m3
+           | ((uint32_t)(N >> 3) << 17)  // N / 8
+           | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T with e4m3 A and B (kind::f8f6f4, K = 32 per MMA).
+__device__ __forceinline__ void mma_ss_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (the layout TMA writes with
 // CU_TENSOR_MAP_SWIZZLE_128B): 8-row x 128-byte atoms, atom base 1024-aligned.
 // lbo/sbo in bytes: leading and stride byte offsets of the canonical layout.
