@@ -277,16 +277,17 @@ int pcp_kv_cache_write_fp8(const void* k, const void* v, const int64_t* slot_map
  * support ...", the context-pass call: descales of shape (num_seqs,
  * num_kv_heads)). Key k of request r and kv head g is code_K[r][k][g][:] *
  * k_descale[r][g], its value code_V[...] * v_descale[r][g]; the result is the
- * same attention as pcp_attn_varlen over those keys and values. The prefill
- * rows' products run in f16: the codes are widened to f16 exactly, q is
- * converted from bf16 to f16 (exact for |q| <= 65504; larger elements saturate
- * to +-65504 and set *status = PCP_ERR_RANGE), and the softmax weights P are
- * rounded to f16 (finer than the bf16 weights of pcp_attn_varlen). Decode rows
- * (head_dim 128, up to 8 q heads per kv head): the scores take the K codes as
- * e4m3 operands against q written as three e4m3 terms per element after a
- * power-of-two scale per head (their sum is the bf16 q), V is widened to f16
- * and P carried as two f16 parts; other decode rows run in fp32. The descales
- * multiply the fp32 scores and outputs.
+ * same attention as pcp_attn_varlen over those keys and values. head_dim 128:
+ * the scores take the K codes as e4m3 MMA operands against q written as two
+ * e4m3 terms per element after a power-of-two scale per query row (prefill)
+ * or per q head (decode rows); the terms sum to the bf16 q exactly except for
+ * elements below 2^-10 of the row's largest, whose error is at most 2^-18 of
+ * it. V is widened to f16 (exact) and the softmax weights P are f16 (decode
+ * rows: two f16 parts). head_dim 64: the prefill rows' products run in f16
+ * (codes widened, q converted to f16, P f16) and decode rows in fp32. An
+ * element of q beyond +-65504 sets *status = PCP_ERR_RANGE (with head_dim 64
+ * it is saturated to +-65504). The descales multiply the fp32 scores and
+ * outputs.
  * key_cache, value_cache: [num_blocks][block_size][Hkv][D] bytes (as written
  * by pcp_kv_cache_write_fp8); k_descale, v_descale: device fp32
  * [num_reqs][Hkv] (inputs: out and lse must not overlap them). Every other

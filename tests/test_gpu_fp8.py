@@ -184,8 +184,9 @@ def test_fp8_workload2_matches_oracle():
 
 
 def test_fp8_q_beyond_f16_range_is_reported():
-    """The FP8 path converts q to f16 for the prefill rows' MMAs: an element
-    beyond +-65504 saturates and the call reports PCP_ERR_RANGE; every other
+    """An element of q beyond +-65504 on the FP8 path is reported as
+    PCP_ERR_RANGE (head_dim 128 writes q as two e4m3 terms after a per-row
+    scale, head_dim 64 converts it to f16 and saturates there); every other
     row's output still matches the oracle."""
     P = _P()
     spec = W.custom_spec([200, 150], [0, 40], num_q_heads=4, num_kv_heads=2, head_dim=128, seed=6550)
