@@ -49,7 +49,7 @@ def test_decode_group_sizes(G):
     _check(spec)
 
 
-@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 8])
 def test_decode_fp8_group_sizes(G):
     """FP8 cache with a different descale per (request, kv head): G <= 4 uses two
     converter sets, G = 8 one."""

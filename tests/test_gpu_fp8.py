@@ -117,6 +117,12 @@ FP8_CASES = {
     "tile_exact": dict(q=[256, 128], p=[128, 0], hq=4, hkv=2, d=128),
     "bs64": dict(q=[200, 1], p=[77, 300], hq=8, hkv=2, d=128, bs=64),
     "gqa16_d64": dict(q=[140, 1, 1], p=[9, 300, 1200], hq=32, hkv=2, d=64),
+    # head_dim 128 with an odd group (one head slot per item: one warpgroup splits q
+    # into its e4m3 terms and frees Q alone) and a decode row of that group
+    "gqa3_odd_d128": dict(q=[140, 1], p=[10, 700], hq=6, hkv=2, d=128),
+    "gqa5_d128": dict(q=[200, 1, 1], p=[30, 1025, 9], hq=10, hkv=2, d=128),
+    "request_without_new_tokens": dict(q=[0, 150, 0, 1], p=[64, 10, 30, 99], hq=4, hkv=2, d=128),
+    "all_decode": dict(q=[1, 1, 1, 1, 1], p=[5, 900, 33, 1, 2048], hq=8, hkv=2, d=128),
 }
 
 
