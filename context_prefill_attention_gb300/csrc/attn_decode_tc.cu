@@ -87,7 +87,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 template <bool F8, int GP>
 struct TcCfg {
     // S^T columns: the G q heads (bf16), or their kTerms e4m3 terms (FP8)
-    static constexpr int kNS = F8 ? (kTerms * GP <= 16 ? 16 : 32) : 16;
+    static constexpr int kNS = 16;
+    static_assert(!F8 || kTerms * GP <= kNS, "the q terms of a group fill N = 16");
     static constexpr int kKS = F8 ? 4 : 3;                 // K tiles in flight (free after their S)
     static constexpr int kVS = (F8 && GP <= 4) ? 4 : 3;    // V tiles in flight (free after their PV)
     static constexpr int kHalfBytes = kKeys * 128;      // 128 keys x 64 dims x 2 bytes
@@ -117,7 +118,7 @@ struct TcCfg {
     static constexpr int kMisc = kBar + kNumBars * 8;   // TMEM address, abort flag
     static constexpr int kSmem = kMisc + 16 + 1024;     // + alignment slack
     static constexpr uint32_t kTmemS = 0, kTmemO = 2 * kNS;  // S^T x 2 (kNS columns), O^T x 2 (16)
-    static constexpr uint32_t kTmemCols = 2 * kNS + 2 * kN <= 64 ? 64 : 128;
+    static constexpr uint32_t kTmemCols = 64;
     static constexpr uint32_t kIdescS = F8 ? idesc_e4m3(128, kNS) : idesc_bf16(128, kN, false, false);
     static constexpr uint32_t kIdescO = F8 ? idesc_f16(128, kN, true, false) : idesc_bf16(128, kN, true, false);
 };
@@ -133,8 +134,7 @@ struct DecItem {
 
 // Item p of the decode work list. The caller's items rise, so the row cursor
 // ri only walks forward over the prefix (rows without items are skipped).
-__device__ __forceinline__ DecItem dec_item(const int32_t* pre, int32_t& ri, int32_t p, const pcp_row_t* rows,
-                                            int32_t hkv) {
+__device__ __forceinline__ DecItem dec_item(const int32_t* pre, int32_t& ri, int32_t p, const pcp_row_t* rows) {
     while (pre[ri + 1] <= p) ++ri;
     const pcp_row_t row = rows[ri];
     const int32_t nsplit = (row.kv_end + kDecodeChunk - 1) / kDecodeChunk;
@@ -148,7 +148,6 @@ __device__ __forceinline__ DecItem dec_item(const int32_t* pre, int32_t& ri, int
     it.lo = it.split * kDecodeChunk;
     it.hi = min(row.kv_end, it.lo + kDecodeChunk);
     it.nt = (it.hi - it.lo + kKeys - 1) / kKeys;
-    (void)hkv;
     return it;
 }
 
@@ -423,7 +422,7 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
         int32_t ri = 0;
         bool ok = true;
         for (int32_t p = blockIdx.x; p < total && ok; p += step) {
-            const DecItem it = dec_item(pre, ri, p, a.rows, a.hkv);
+            const DecItem it = dec_item(pre, ri, p, a.rows);
             // the split's block-table entries as first cache rows; a bad id maps to a
             // row past the cache (zero filled) and reports PCP_ERR_RANGE
             const int32_t* table = a.block_table + (size_t)it.req * a.max_blocks;
@@ -507,7 +506,7 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
             bool ok = true;
             const bool s_role = warp == kMmaWarp;
             for (int32_t p = blockIdx.x; p < total && ok; p += step) {
-                const DecItem it = dec_item(pre, ri, p, a.rows, a.hkv);
+                const DecItem it = dec_item(pre, ri, p, a.rows);
                 const int qb = ic & 1;
                 if (s_role && !(ok = mbar_wait(q_full(qb), (ic >> 1) & 1, abort_flag))) break;
                 for (int j = 0; j < it.nt; ++j, ++g) {
@@ -571,7 +570,7 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
         int32_t ri = 0;
         bool ok = true;
         for (int32_t p = blockIdx.x; p < total && ok; p += step) {
-            const DecItem it = dec_item(pre, ri, p, a.rows, a.hkv);
+            const DecItem it = dec_item(pre, ri, p, a.rows);
             const int qb = ic & 1;
             if (cset == 0) {
                 if (!(ok = mbar_wait_warp(qc_full(qb), (ic >> 1) & 1, abort_flag))) break;
@@ -616,7 +615,7 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
         bool ok = true;     // every wait of this thread so far completed
         bool stop = false;  // the joint verdict (FP8: of the warpgroup; bf16: of both), once per item
         for (int32_t p = blockIdx.x; p < total && !stop; p += step, ++ic) {
-            const DecItem it = dec_item(pre, ri, p, a.rows, a.hkv);
+            const DecItem it = dec_item(pre, ri, p, a.rows);
             const float kd = F8 ? __ldg(a.k_descale + (size_t)it.req * a.hkv + it.hk) : 1.f;
             const float sl2 = a.scale * kd * kLog2e;
             // FP8: the power of two that undoes each head's q scaling (see q_to_e4m3_terms)
@@ -662,12 +661,7 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
                 ok &= mbar_wait_warp(s_full(g & 1), (g >> 1) & 1, abort_flag);
                 tc_fence_after();
                 uint32_t s[kNS];
-                const uint32_t t_s = tmem + lane_base + C::kTmemS + (g & 1) * kNS;
-                if constexpr (kNS == 32) {
-                    tmem_ld32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-                } else {
-                    tmem_ld16(t_s, *reinterpret_cast<uint32_t(*)[16]>(&s[0]));
-                }
+                tmem_ld16(tmem + lane_base + C::kTmemS + (g & 1) * kNS, s);
                 tmem_wait_ld();
                 float x[GP];
 #pragma unroll
