@@ -613,7 +613,7 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
         uint32_t gt = 0, ic = 0;
         int32_t ri = 0;
         bool ok = true;     // every wait of this thread so far completed
-        bool stop = false;  // the joint verdict (FP8: of the warpgroup; bf16: of both), once per item
+        bool stop = false;  // the joint decision to stop (FP8: the warpgroup's; bf16: both's), once per item
         for (int32_t p = blockIdx.x; p < total && !stop; p += step, ++ic) {
             const DecItem it = dec_item(pre, ri, p, a.rows);
             const float kd = F8 ? __ldg(a.k_descale + (size_t)it.req * a.hkv + it.hk) : 1.f;
