@@ -497,9 +497,9 @@ int launch_decode(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t 
                   cudaStream_t stream) {
     if (a.d != 64 && a.d != 128) return PCP_ERR_UNSUPPORTED;
     int rc = PCP_DECODE_TC ? launch_decode_tc(a, dec_out, dec_lse, max_splits, stream) : PCP_ERR_UNSUPPORTED;
-    // partials per split: the tensor-core kernel over an FP8 cache writes one per
-    // softmax warpgroup
-    int pps = a.k_descale ? 2 : 1;
+    // partials per split: the tensor-core kernel writes one per softmax warpgroup
+    // over an FP8 cache and with more than 8 q heads per kv head
+    int pps = (a.k_descale || a.hq / a.hkv > 8) ? 2 : 1;
     if (rc == PCP_ERR_UNSUPPORTED) {
         rc = a.d == 64 ? launch_decode_d<64>(a, dec_out, dec_lse, max_splits, stream)
                        : launch_decode_d<128>(a, dec_out, dec_lse, max_splits, stream);

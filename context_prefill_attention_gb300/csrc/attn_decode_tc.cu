@@ -4,12 +4,13 @@
 // prefill rows; "[MRv2][PCP] Carry the row plan ...", "drop pcp_has_prefill":
 // decode rows carried in the same plan).
 //
-// A decode row has one query token, so the q heads of one kv head (G <= 8)
-// are the only other dimension an MMA can take: the kernel computes the
-// transposed products, keys along M:
+// A decode row has one query token, so the q heads of one kv head (G <= 16;
+// FP8: G <= 8) are the only other dimension an MMA can take: the kernel
+// computes the transposed products, keys along M:
 //   S^T [128 keys x 16] = K [128 keys x D] . Q^T      (Q^T: the G q heads, padded to 16 rows)
 //   O^T [D x 16]        = V^T [D x 128 keys] . P^T    (P^T: 16 rows, P in rows 0..7 and the
-//                                                      rounding remainder of P in rows 8..15)
+//                                                      rounding remainder of P in rows 8..15;
+//                                                      G > 8: 32 rows, 0..15 and 16..31)
 // Over an FP8 cache S^T takes the e4m3 codes of K as they are (kind::f8f6f4,
 // 32 dims per MMA) against q written as two e4m3 terms per element after a
 // power-of-two scaling per head, whose sum is the bf16 q (term t of head h in
@@ -39,9 +40,10 @@
 //    rounded to 16 bits into shared memory (P^T rows h and 8 + h; the
 //    remainder keeps P's rounding out of the result); each finished tile's O^T
 //    is added into registers with the running rescale; at the end of an item
-//    the split's partial is written: bf16, warpgroup 0 merges the two
-//    warpgroups' (max, l, O); FP8, each warpgroup writes its own partial (two
-//    per split, merged by decode_merge_kernel) and never waits for the other;
+//    the split's partial is written: bf16 up to 8 heads, warpgroup 0 merges the
+//    two warpgroups' (max, l, O); FP8 and 16 heads, each warpgroup writes its
+//    own partial (two per split, merged by decode_merge_kernel) and never waits
+//    for the other;
 //  * FP8 cache: the K codes land 128-byte swizzled and are the S operand; the
 //    converter warps (two sets taking alternate tiles where G <= 4, else one)
 //    widen each V tile's codes to f16 in place (exact; rows past the last key
@@ -68,8 +70,8 @@ namespace {
 
 constexpr int kD = 128;          // head_dim this kernel takes
 constexpr int kKeys = 128;       // keys per tile: the M of S^T
-constexpr int kN = 16;           // the N of both MMAs
-constexpr int kMaxG = 8;         // q heads per kv head: P's hi and lo rows fit N = 16
+constexpr int kN = 16;           // the N of S^T (and of O^T up to 8 q heads per kv head)
+constexpr int kMaxG = 16;        // q heads per kv head (FP8: 8)
 constexpr int kTerms = 2;        // FP8: e4m3 terms per q element (their sum is the bf16 q exactly)
 constexpr int kProdWarp = 8;     // warp 8: K tiles and Q^T; warp 9: V tiles
 constexpr int kMmaWarp = 10;     // lane 0 issues the S MMAs (the warp owns the TMEM allocation)
@@ -89,6 +91,13 @@ struct TcCfg {
     // S^T columns: the G q heads (bf16), or their kTerms e4m3 terms (FP8)
     static constexpr int kNS = 16;
     static_assert(!F8 || kTerms * GP <= kNS, "the q terms of a group fill N = 16");
+    // head stride of the per-head arrays; O^T columns = P^T rows: P's hi parts in
+    // rows 0 .. kGS - 1, the remainders from row kGS (N = 16, or 32 for 16 heads)
+    static constexpr int kGS = GP <= 8 ? 8 : 16;
+    static constexpr int kNO = 2 * kGS;
+    // a partial per softmax warpgroup and split (no hand-over area): FP8, and 16
+    // heads (whose hand-over area would not fit)
+    static constexpr bool kSplitParts = F8 || GP > 8;
     static constexpr int kKS = F8 ? 4 : 3;                 // K tiles in flight (free after their S)
     static constexpr int kVS = (F8 && GP <= 4) ? 4 : 3;    // V tiles in flight (free after their PV)
     static constexpr int kHalfBytes = kKeys * 128;      // 128 keys x 64 dims x 2 bytes
@@ -98,7 +107,7 @@ struct TcCfg {
     static constexpr int kRowsBytes = kN * 128;         // 16 rows x 128 bytes: one 64-element half
     static constexpr int kQBytes = 2 * kRowsBytes;      // bf16 Q^T: 16 rows x 128 dims
     static constexpr int kQCBytes = F8 ? kNS * 128 : 0;  // FP8: the e4m3 terms of Q^T, kNS rows
-    static constexpr int kPBytes = 2 * kRowsBytes;      // P^T: 16 rows x 128 keys
+    static constexpr int kPBytes = 2 * kNO * 128;       // P^T: kNO rows x 128 keys
     static constexpr int kK = 0;                        // K stages
     static constexpr int kV = kKS * kKTileBytes;        // V stages
     static constexpr int kQ = kV + kVS * kTileBytes;    // two Q^T buffers (bf16)
@@ -108,22 +117,22 @@ struct TcCfg {
     static constexpr int kPages = kPre + ((kDecTcMaxRows + 1) * 4 + 15) / 16 * 16;  // one list per producer
     static constexpr int kRed = kPages + 2 * kMaxPages * 4;  // float [2 wg][2][4][8] maxima and sums
     // bf16: warpgroup 1's max and O of an item, handed to warpgroup 0 (float [8 + 8 x 128])
-    static constexpr int kXchg = kRed + (2 * 2 * 4 * kMaxG) * 2 * 4;
+    static constexpr int kXchg = kRed + (2 * 2 * 4 * kGS) * 2 * 4;
     // FP8: float [4][8] q scales, a ring of four items: the converters run at most
     // three items ahead of the softmax (they prepare item i + 3 only once S of item
     // i + 1 is done, which needs the softmax in item i at least)
-    static constexpr int kQs = kXchg + (F8 ? 0 : (kMaxG + kMaxG * kKeys) * 4);
-    static constexpr int kBar = kQs + 4 * kMaxG * 4;
+    static constexpr int kQs = kXchg + (kSplitParts ? 0 : (kGS + kGS * kKeys) * 4);
+    static constexpr int kBar = kQs + 4 * kGS * 4;
     static constexpr int kNumBars = 2 * kKS + 3 * kVS + 7 * 2 + 4;
     static constexpr int kMisc = kBar + kNumBars * 8;   // TMEM address, abort flag
     static constexpr int kSmem = kMisc + 16 + 1024;     // + alignment slack
-    static constexpr uint32_t kTmemS = 0, kTmemO = 2 * kNS;  // S^T x 2 (kNS columns), O^T x 2 (16)
-    static constexpr uint32_t kTmemCols = 64;
+    static constexpr uint32_t kTmemS = 0, kTmemO = 2 * kNS;  // S^T x 2 (kNS columns), O^T x 2 (kNO)
+    static constexpr uint32_t kTmemCols = 2 * kNS + 2 * kNO <= 64 ? 64 : 128;
     static constexpr uint32_t kIdescS = F8 ? idesc_e4m3(128, kNS) : idesc_bf16(128, kN, false, false);
-    static constexpr uint32_t kIdescO = F8 ? idesc_f16(128, kN, true, false) : idesc_bf16(128, kN, true, false);
+    static constexpr uint32_t kIdescO = F8 ? idesc_f16(128, kNO, true, false) : idesc_bf16(128, kNO, true, false);
 };
 static_assert(TcCfg<true, 4>::kSmem <= 232448 && TcCfg<true, 8>::kSmem <= 232448 &&
-                  TcCfg<false, 8>::kSmem <= 232448, "shared memory");
+                  TcCfg<false, 8>::kSmem <= 232448 && TcCfg<false, 16>::kSmem <= 232448, "shared memory");
 static_assert(TcCfg<true, 4>::kQC % 1024 == 0 && TcCfg<true, 8>::kP % 1024 == 0 &&
                   TcCfg<false, 8>::kP % 1024 == 0, "1024-byte swizzle atoms");
 
@@ -356,7 +365,8 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
     int32_t* pre = reinterpret_cast<int32_t*>(smem + C::kPre);
     int32_t* pages = reinterpret_cast<int32_t*>(smem + C::kPages);
     float* red_m = reinterpret_cast<float*>(smem + C::kRed);  // [warpgroup][tile parity][warp][head]
-    float* red_l = red_m + 2 * 2 * 4 * kMaxG;                 // [item parity][8 warps][head]
+    constexpr int kGS = C::kGS, kNO = C::kNO;
+    float* red_l = red_m + 2 * 2 * 4 * kGS;                   // [item parity][8 warps][head]
     float* xchg = reinterpret_cast<float*>(smem + C::kXchg);  // bf16: [head max, head x dim O]
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -545,8 +555,8 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
                         const uint64_t vd = v_desc(g % kVS), pd = p_desc(g & 1);
 #pragma unroll
                         for (int ks = 0; ks < kKeys / 16; ++ks) {
-                            const uint32_t poff = ((ks / 4) * C::kRowsBytes + (ks % 4) * 32) >> 4;
-                            mma_ss(tmem + C::kTmemO + (g & 1) * kN, vd + (uint32_t)(ks * 2048 >> 4), pd + poff,
+                            const uint32_t poff = ((ks / 4) * (kNO * 128) + (ks % 4) * 32) >> 4;
+                            mma_ss(tmem + C::kTmemO + (g & 1) * kNO, vd + (uint32_t)(ks * 2048 >> 4), pd + poff,
                                    C::kIdescO, ks > 0 ? 1u : 0u);
                         }
                         mma_commit(o_full(g & 1));
@@ -575,7 +585,7 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
             if (cset == 0) {
                 if (!(ok = mbar_wait_warp(qc_full(qb), (ic >> 1) & 1, abort_flag))) break;
                 if (q_to_e4m3_terms<GP>(smem + C::kQ + qb * C::kQBytes, smem + C::kQC + qb * C::kQCBytes,
-                                        reinterpret_cast<float*>(smem + C::kQs) + (ic & 3) * kMaxG, cw, lane, G) &&
+                                        reinterpret_cast<float*>(smem + C::kQs) + (ic & 3) * kGS, cw, lane, G) &&
                     lane == 0)
                     report_status(a.status, PCP_ERR_RANGE);
                 fence_proxy_async_smem();
@@ -626,7 +636,7 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
                 ok &= mbar_wait_warp(q_ready(ic & 3), (ic >> 2) & 1, abort_flag);
 #pragma unroll
                 for (int h = 0; h < GP; ++h)
-                    qs[h] = reinterpret_cast<const float*>(smem + C::kQs)[(ic & 3) * kMaxG + h];
+                    qs[h] = reinterpret_cast<const float*>(smem + C::kQs)[(ic & 3) * kGS + h];
             }
             float m_run[GP], l_t[GP], acc[GP], a_prev[GP];
 #pragma unroll
@@ -641,15 +651,20 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
             auto accumulate = [&](uint32_t g, const float (&alpha)[GP]) {
                 ok &= mbar_wait_warp(o_full(g & 1), (g >> 1) & 1, abort_flag);
                 tc_fence_after();
-                uint32_t o[16];
-                tmem_ld16(tmem + lane_base + C::kTmemO + (g & 1) * kN, o);
+                uint32_t o[kNO];
+                const uint32_t t_o = tmem + lane_base + C::kTmemO + (g & 1) * kNO;
+                if constexpr (kNO == 32) {
+                    tmem_ld32(t_o, o);
+                } else {
+                    tmem_ld16(t_o, o);
+                }
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(o_free(g & 1));
 #pragma unroll
                 for (int h = 0; h < GP; ++h)
-                    acc[h] = acc[h] * alpha[h] + (__uint_as_float(o[h]) + __uint_as_float(o[kMaxG + h]));
+                    acc[h] = acc[h] * alpha[h] + (__uint_as_float(o[h]) + __uint_as_float(o[kGS + h]));
             };
             uint32_t g_prev = 0;
             bool have_prev = false;
@@ -673,20 +688,20 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
                     x[h] = valid ? sh * sl2 : -INFINITY;
                 }
                 // tile max per head: over the warp, then over the warpgroup's four warps
-                float* rm = red_m + (wg * 2 + ((g >> 1) & 1)) * 4 * kMaxG;  // [warp][head]
+                float* rm = red_m + (wg * 2 + ((g >> 1) & 1)) * 4 * kGS;  // [warp][head]
                 const float wm = warp_scatter<GP, true>(x, lane);
-                if (lane % kSpan == 0) rm[wq * kMaxG + hl] = wm;
+                if (lane % kSpan == 0) rm[wq * kGS + hl] = wm;
                 bar_sync_named(1 + wg, 128);
                 // O(g - 2) out of TMEM first: PV(g - 2) complete frees P buffer g & 1
                 if (have_prev) accumulate(g_prev, a_prev);
                 float alpha[GP];
                 uint8_t* pbuf = smem + C::kP + (g & 1) * C::kPBytes;
                 // this key's column of P^T: chunk (t % 64) / 8 of each row, swizzled by the row
-                uint8_t* pcol = pbuf + (t >> 6) * C::kRowsBytes + (t & 7) * 2;
+                uint8_t* pcol = pbuf + (t >> 6) * (kNO * 128) + (t & 7) * 2;
                 const int chunk = (t & 63) >> 3;
 #pragma unroll
                 for (int h = 0; h < GP; ++h) {
-                    const float mt = fmaxf(fmaxf(rm[h], rm[kMaxG + h]), fmaxf(rm[2 * kMaxG + h], rm[3 * kMaxG + h]));
+                    const float mt = fmaxf(fmaxf(rm[h], rm[kGS + h]), fmaxf(rm[2 * kGS + h], rm[3 * kGS + h]));
                     const float m_new = fmaxf(m_run[h], mt);  // finite: the tile has a valid key
                     alpha[h] = fast_exp2(m_run[h] - m_new);   // 0 on the warpgroup's first tile
                     m_run[h] = m_new;
@@ -695,7 +710,7 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
                     const uint16_t hi = to16<F8>(pe);
                     const uint16_t lo = to16<F8>(pe - from16<F8>(hi));
                     *reinterpret_cast<uint16_t*>(pcol + h * 128 + ((chunk ^ (h & 7)) << 4)) = hi;
-                    *reinterpret_cast<uint16_t*>(pcol + (kMaxG + h) * 128 + ((chunk ^ (h & 7)) << 4)) = lo;
+                    *reinterpret_cast<uint16_t*>(pcol + (kGS + h) * 128 + ((chunk ^ (h & 7)) << 4)) = lo;
                 }
                 if (!F8 && nvalid < kKeys) {
                     // keys past the split's end: zero their V rows (unwritten cache slots in
@@ -722,20 +737,20 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
             }
             if (have_prev) accumulate(g_prev, a_prev);
             gt += it.nt;
-            float* rl = red_l + (ic & 1) * 8 * kMaxG;  // [warp 0..7][head]
+            float* rl = red_l + (ic & 1) * 8 * kGS;  // [warp 0..7][head]
             const float wl = warp_scatter<GP, false>(l_t, lane);
-            if (lane % kSpan == 0) rl[warp * kMaxG + hl] = wl;
+            if (lane % kSpan == 0) rl[warp * kGS + hl] = wl;
             const float vd = F8 ? __ldg(a.v_descale + (size_t)it.req * a.hkv + it.hk) : 1.f;
-            if constexpr (F8) {
-                // FP8: each warpgroup writes its own partial of the split (a warpgroup
-                // without a tile of the item writes (0, -inf)); decode_merge_kernel
+            if constexpr (C::kSplitParts) {
+                // FP8 and 16 heads: each warpgroup writes its own partial of the split (a
+                // warpgroup without a tile of the item writes (0, -inf)); decode_merge_kernel
                 // combines the two, so the warpgroups never wait for each other
                 if ((stop = bar_wg_or(1 + wg, !ok))) break;
-                const float* rw = rl + wg * 4 * kMaxG;
+                const float* rw = rl + wg * 4 * kGS;
 #pragma unroll
                 for (int h = 0; h < GP; ++h) {
                     if (h >= G) continue;
-                    const float L = rw[h] + rw[kMaxG + h] + rw[2 * kMaxG + h] + rw[3 * kMaxG + h];
+                    const float L = rw[h] + rw[kGS + h] + rw[2 * kGS + h] + rw[3 * kGS + h];
                     const size_t slot =
                         ((size_t)it.ri * a.hq + it.hk * G + h) * (2 * max_splits) + 2 * it.split + wg;
                     dec_out[slot * kD + t] = L > 0.f ? acc[h] / L * vd : 0.f;
@@ -750,7 +765,7 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
 #pragma unroll
                     for (int h = 0; h < GP; ++h) {
                         if (t == 0) xchg[h] = m_run[h];
-                        xchg[kMaxG + h * kKeys + t] = acc[h];
+                        xchg[kGS + h * kKeys + t] = acc[h];
                     }
                 }
                 if ((stop = bar_all_or(!ok))) break;
@@ -758,14 +773,13 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
 #pragma unroll
                     for (int h = 0; h < GP; ++h) {
                         if (h >= G) continue;
-                        const float L0 = rl[h] + rl[kMaxG + h] + rl[2 * kMaxG + h] + rl[3 * kMaxG + h];
-                        const float L1 =
-                            rl[4 * kMaxG + h] + rl[5 * kMaxG + h] + rl[6 * kMaxG + h] + rl[7 * kMaxG + h];
+                        const float L0 = rl[h] + rl[kGS + h] + rl[2 * kGS + h] + rl[3 * kGS + h];
+                        const float L1 = rl[4 * kGS + h] + rl[5 * kGS + h] + rl[6 * kGS + h] + rl[7 * kGS + h];
                         const float m1 = xchg[h];
                         const float M = fmaxf(m_run[h], m1);  // finite: the item has a tile
                         const float f0 = fast_exp2(m_run[h] - M), f1 = fast_exp2(m1 - M);
                         const float L = L0 * f0 + L1 * f1;
-                        const float O = acc[h] * f0 + xchg[kMaxG + h * kKeys + t] * f1;
+                        const float O = acc[h] * f0 + xchg[kGS + h * kKeys + t] * f1;
                         const size_t slot = ((size_t)it.ri * a.hq + it.hk * G + h) * (2 * max_splits) + it.split;
                         dec_out[slot * kD + t] = L > 0.f ? O / L : 0.f;
                         if (t == 0) dec_lse[slot] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
@@ -816,11 +830,11 @@ int launch_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_
 int launch_decode_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
                      cudaStream_t stream) {
     const int G = a.hkv > 0 ? a.hq / a.hkv : 0;
-    if (a.d != kD || G < 1 || G > kMaxG || a.num_rows > kDecTcMaxRows || a.block_size > kKeys ||
+    if (a.d != kD || G < 1 || G > (a.k_descale ? 8 : kMaxG) || a.num_rows > kDecTcMaxRows || a.block_size > kKeys ||
         kKeys % a.block_size != 0)
         return PCP_ERR_UNSUPPORTED;
     // heads per group padded to a power of two (the padded heads' results are not written)
-    const int GP = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
+    const int GP = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : G <= 8 ? 8 : 16;
     if (a.k_descale) {
         if (GP == 1) return launch_tc<true, 1>(a, dec_out, dec_lse, max_splits, stream);
         if (GP == 2) return launch_tc<true, 2>(a, dec_out, dec_lse, max_splits, stream);
@@ -830,7 +844,8 @@ int launch_decode_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32
     if (GP == 1) return launch_tc<false, 1>(a, dec_out, dec_lse, max_splits, stream);
     if (GP == 2) return launch_tc<false, 2>(a, dec_out, dec_lse, max_splits, stream);
     if (GP == 4) return launch_tc<false, 4>(a, dec_out, dec_lse, max_splits, stream);
-    return launch_tc<false, 8>(a, dec_out, dec_lse, max_splits, stream);
+    if (GP == 8) return launch_tc<false, 8>(a, dec_out, dec_lse, max_splits, stream);
+    return launch_tc<false, 16>(a, dec_out, dec_lse, max_splits, stream);
 }
 
 }  // namespace pcp

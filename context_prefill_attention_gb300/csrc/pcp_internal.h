@@ -124,10 +124,11 @@ int launch_schedule(const PrefillArgs& a, int32_t flags, Unit* units, Unit* unit
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 int launch_decode(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
                   cudaStream_t stream);
-// The tensor-core decode (head_dim 128, up to 8 q heads per kv head, at most
-// kDecTcMaxRows rows); PCP_ERR_UNSUPPORTED for any other shape. Over an FP8
-// cache it writes two partials per split (slots 2 split and 2 split + 1 of the
-// row's 2 x max_splits), else one (slot split).
+// The tensor-core decode (head_dim 128, up to 16 q heads per kv head with a
+// bf16 cache and 8 with an FP8 one, at most kDecTcMaxRows rows);
+// PCP_ERR_UNSUPPORTED for any other shape. Over an FP8 cache and with more
+// than 8 q heads per kv head it writes two partials per split (slots 2 split
+// and 2 split + 1 of the row's 2 x max_splits), else one (slot split).
 constexpr int kDecTcMaxRows = 1024;
 int launch_decode_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
                      cudaStream_t stream);

@@ -172,9 +172,9 @@ size_t pcp_attn_workspace_size(int32_t num_rows, int32_t total_q, int32_t num_q_
  * pcp_attn_varlen — device. Attention of every planned row in one call:
  * prefill rows (end-aligned causal over the new tokens, plus the non-causal
  * context over the cached prefix) on the tensor cores, decode rows on a
- * split-KV bandwidth path (tensor cores for head_dim 128 with up to 8 q heads
- * per kv head and at most 1024 rows, P carried as bf16 hi + lo; CUDA cores in
- * fp32 otherwise). ("Feat/pcp qwen36 hybrid", "Changes"; "[MRv2]
+ * split-KV bandwidth path (tensor cores for head_dim 128 with up to 16 q heads
+ * per kv head, 8 over an FP8 cache, and at most 1024 rows, P carried as bf16
+ * hi + lo; CUDA cores in fp32 otherwise). ("Feat/pcp qwen36 hybrid", "Changes"; "[MRv2]
  * FlashAttention PCP support ...", overview and the context-pass call returning
  * (ctx_out, ctx_lse); "Carry the row plan ...", "What made it removable".)
  *
@@ -283,8 +283,9 @@ int pcp_kv_cache_write_fp8(const void* k, const void* v, const int64_t* slot_map
  * or per q head (decode rows); the terms sum to the bf16 q exactly except for
  * elements below 2^-10 of the row's largest, whose error is at most 2^-18 of
  * it. V is widened to f16 (exact) and the softmax weights P are f16 (decode
- * rows: two f16 parts). head_dim 64: the prefill rows' products run in f16
- * (codes widened, q converted to f16, P f16) and decode rows in fp32. An
+ * rows with up to 8 q heads per kv head: two f16 parts; more: fp32). head_dim
+ * 64: the prefill rows' products run in f16 (codes widened, q converted to f16,
+ * P f16) and decode rows in fp32. An
  * element of q beyond +-65504 sets *status = PCP_ERR_RANGE (with head_dim 64
  * it is saturated to +-65504). The descales multiply the fp32 scores and
  * outputs.

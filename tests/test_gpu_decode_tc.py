@@ -2,12 +2,12 @@
 
 Decode rows ("[MRv2] FlashAttention PCP support for GQA on MRv2", overview:
 mixed-batch decode next to the prefill rows) go to the tensor-core decode
-kernel for head_dim 128, up to 8 q heads per kv head and at most 1024 rows,
-and to the CUDA-core kernel otherwise. The tensor-core kernel walks 128-key
+kernel for head_dim 128, up to 16 q heads per kv head (8 over an FP8 cache)
+and at most 1024 rows, and to the CUDA-core kernel otherwise. The tensor-core kernel walks 128-key
 tiles of 1024-key splits through shared-memory rings that run on across work
 items, so these cases aim at its boundaries: context lengths around the tile
 and split sizes (1, 127, 128, 129, 1023, 1024, 1025 keys, ...), every block
-size, every group size up to 8 (padded to 1, 2, 4 or 8 in the kernel), the FP8
+size, every group size up to 8 and 12, 16 (padded to 1, 2, 4, 8 or 16), the FP8
 cache with both converter layouts (G <= 4: K and V widened by two warp sets;
 G = 8: one set), many more work items than CTAs, and a plan with more rows
 than the kernel takes (the CUDA-core kernel then runs). The caches start out
@@ -40,10 +40,11 @@ def test_decode_lengths_every_block_size(bs):
     _check(spec)
 
 
-@pytest.mark.parametrize("G", [1, 2, 3, 5, 6, 7, 8])
+@pytest.mark.parametrize("G", [1, 2, 3, 5, 6, 7, 8, 12, 16])
 def test_decode_group_sizes(G):
-    """Group sizes that the kernel pads (3 -> 4, 5..7 -> 8) and the exact ones,
-    beside a prefill row."""
+    """Group sizes that the kernel pads (3 -> 4, 5..7 -> 8, 12 -> 16) and the
+    exact ones, beside a prefill row (16 heads: 32 P^T rows, a partial per
+    softmax warpgroup)."""
     spec = W.custom_spec([1, 1, 1, 40], [700, 1030, 3, 0], num_q_heads=2 * G, num_kv_heads=2, head_dim=128,
                          seed=910 + G)
     _check(spec)
