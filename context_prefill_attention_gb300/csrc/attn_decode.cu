@@ -6,7 +6,7 @@
 // bound by HBM bandwidth (every key's K and V read once per kv head), so this
 // path is CUDA-core code built around the memory system:
 //  * split-KV: CTA (split, kv head, row) streams keys [C s, C (s+1)) of one
-//    kv head for all G q heads of its group (C = kDecodeChunk = 1024 keys);
+//    kv head for all G q heads of its group (C = kDecodeChunk = 2048 keys);
 //  * a producer warp reads the chunk's block-table entries once, then streams
 //    32-key slabs of K and V into a 4-stage shared-memory ring with TMA: one
 //    unswizzled box per page (the head's D contiguous elements of each of its

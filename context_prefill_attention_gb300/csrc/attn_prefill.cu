@@ -937,7 +937,7 @@ __device__ __forceinline__ int32_t unit_cost(const Unit& u, const pcp_row_t* row
 
 // Check every row, then build the prefill work list: one unit per (valid
 // non-decode row, 128-token tile, pass), ordered by the number of key tiles,
-// longest first. Also counts the decode work items (kv head x 1024-key split of
+// longest first. Also counts the decode work items (kv head x kDecodeChunk-key split of
 // each valid decode row): dec_pre[i] = items of rows before row i, header[1] =
 // their total.
 __global__ void __launch_bounds__(kSchedThreads, 1)

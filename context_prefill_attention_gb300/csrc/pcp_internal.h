@@ -15,7 +15,7 @@ constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 // Keys per split of the decode kernel.
 #ifndef PCP_DECODE_CHUNK
-#define PCP_DECODE_CHUNK 1024  // measured: 1024 > 512 > 256 keys per split on the mixed workload
+#define PCP_DECODE_CHUNK 2048  // measured: 2048 >= 1024 > 512 > 256 keys per split on the mixed workload
 #endif
 constexpr int kDecodeChunk = PCP_DECODE_CHUNK;
 
@@ -83,7 +83,7 @@ struct PrefillArgs {
     const int32_t* row_ok;
     const Unit* units;
     const int32_t* num_units;   // header: [0] prefill units, [1] decode work items
-    // decode work items (kv head x 1024-key split of a decode row) of the rows
+    // decode work items (kv head x kDecodeChunk-key split of a decode row) of the rows
     // before row i, for i = 0..num_rows (the last entry is the total)
     const int32_t* dec_pre;
     int32_t* status;

@@ -4,9 +4,9 @@ Decode rows ("[MRv2] FlashAttention PCP support for GQA on MRv2", overview:
 mixed-batch decode next to the prefill rows) go to the tensor-core decode
 kernel for head_dim 128, up to 16 q heads per kv head (8 over an FP8 cache)
 and at most 1024 rows, and to the CUDA-core kernel otherwise. The tensor-core kernel walks 128-key
-tiles of 1024-key splits through shared-memory rings that run on across work
+tiles of 2048-key splits through shared-memory rings that run on across work
 items, so these cases aim at its boundaries: context lengths around the tile
-and split sizes (1, 127, 128, 129, 1023, 1024, 1025 keys, ...), every block
+and split sizes (1, 127, 128, 129, 2047, 2048, 2049 keys, ...), every block
 size, every group size up to 8 and 12, 16 (padded to 1, 2, 4, 8 or 16), the FP8
 cache with both converter layouts (G <= 4: K and V widened by two warp sets;
 G = 8: one set), many more work items than CTAs, and a plan with more rows
@@ -21,7 +21,7 @@ from pcp_case import LSE_TOL, OUT_TOL, Case
 
 pytestmark = pytest.mark.gpu
 
-LENGTHS = [1, 2, 127, 128, 129, 1023, 1024, 1025, 2500]
+LENGTHS = [1, 2, 127, 128, 129, 1023, 1024, 1025, 2047, 2048, 2049, 4500]
 
 
 def _check(spec, kv_fp8=False, descales="layer"):

@@ -80,7 +80,7 @@ def expected_units(rows: np.ndarray, flags: int, bs: int):
     return out
 
 
-DECODE_CHUNK = 1024
+DECODE_CHUNK = 2048
 
 
 def read_schedule(case: Case):
@@ -109,7 +109,7 @@ def read_decode_prefix(case: Case):
 
 
 def expected_decode_prefix(rows: np.ndarray, num_kv_heads: int) -> np.ndarray:
-    """Items of the rows before each row: kv heads x 1024-key splits of every
+    """Items of the rows before each row: kv heads x 2048-key splits of every
     decode row, none for prefill rows."""
     cnt = [num_kv_heads * (-(-int(r[5]) // DECODE_CHUNK)) if int(r[7]) else 0 for r in rows]
     return np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32)

@@ -98,7 +98,7 @@ def test_noalloc_rejects_oversized_batch():
     lse = torch.full((8, 64), 3.0, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     ptr = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
-    # 64 rows x 8 heads x (2^26 keys / 1024 per split) x 128 dims of fp32 partials: 16 GiB
+    # 64 rows x 8 heads x (2^26 keys / 2048 per split) x 2 partials x 128 dims of fp32: 16 GiB
     rc = lib.pcp_attn_varlen_noalloc(ptr(q), ptr(kc), ptr(kc), ptr(bt), 1, 1 << 22, 4, 16, ptr(rows), 64, 64, 8,
                                      2, 128, 0.1, ptr(out), ptr(lse), 0, ptr(status), None)
     torch.cuda.synchronize()
