@@ -85,3 +85,25 @@ def test_invalid_plan_rows_are_skipped_and_reported():
     eo, el = case.compare(out, lse, np.arange(200))                                   # valid rows still right
     assert eo <= OUT_TOL and el <= LSE_TOL
     assert keep.sum() > 0
+
+
+@pytest.mark.parametrize("kv_fp8,hq", [(False, 8), (True, 8), (True, 32)],
+                         ids=["tc_bf16", "tc_fp8", "cuda_core_fp8_g16"])
+def test_decode_page_past_the_cache_is_reported(kv_fp8, hq):
+    """A decode-only batch with one bad page in one row's context: the decode
+    kernel that runs (tensor cores for G = 4; CUDA cores for FP8 at G = 16)
+    reports PCP_ERR_RANGE, reads a zero-filled page instead, and the other row
+    still matches the oracle."""
+    P = _P()
+    spec = W.custom_spec([1, 1], [500, 3000], num_q_heads=hq, num_kv_heads=2, head_dim=128, seed=12)
+    case = Case(spec, kv_fp8=kv_fp8)
+    case.run()
+    bad = case.bt.clone()
+    bad[0, 5] = case.num_blocks + 3             # a page inside request 0's context, past the cache
+    case.step.status.zero_()
+    out, lse = case.step.attend(case.q_dev, case.kc, case.vc, bad.cuda(), spec.scale)
+    torch.cuda.synchronize()
+    assert int(case.step.status.item()) == P.PCP_ERR_RANGE
+    assert torch.isfinite(out[:spec.total_q].float()).all()
+    eo, el = case.compare(out, lse, np.array([1]))
+    assert eo <= OUT_TOL and el <= LSE_TOL
