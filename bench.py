@@ -320,14 +320,16 @@ def time_rows(P, step, q, kc, vc, bt_dev, rows_np, scale, stream, flush, iters: 
     return statistics.mean(pre), statistics.mean(dec)
 
 
-def time_e2e(P, spec, bt, bt_dev, kc, vc, q, k, v, steps2, stream, iters: int):
+def time_e2e(P, spec, bt, bt_dev, kc, vc, q, k, v, steps2, stream, iters: int, kernels: bool = True):
     """The step end to end from pinned host memory: each step's q, k, v and plan
     copied in, and its out and lse copied back, inside the timed region. Two
     buffer sets alternate so that step i + 1's uploads (on a copy-in stream)
     and step i - 1's downloads (on a copy-out stream) run under step i's
     kernels; the kernels stay in order on the compute stream (the cache write of
-    step i + 1 after the attention of step i). Returns (ms per step, H2D bytes,
-    D2H bytes per step)."""
+    step i + 1 after the attention of step i). With ``kernels=False`` the same
+    copies run with the same stream order and no kernel: the time the host link
+    alone needs for the step's bytes. Returns (ms per step, H2D bytes, D2H bytes
+    per step)."""
     dev = q.device
     cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     host = [x.cpu().pin_memory() for x in (q, k, v)]
@@ -358,8 +360,12 @@ def time_e2e(P, spec, bt, bt_dev, kc, vc, q, k, v, steps2, stream, iters: int):
             stream.wait_event(ev_in[b])
             if i >= 2:
                 stream.wait_event(ev_out[b])  # step i - 2's result has left buffer set b
-            st.write_cache(bufs[b][1], bufs[b][2], kc, vc, stream)
-            out, lse = st.attend(bufs[b][0], kc, vc, bt_dev, spec.scale, stream)
+            if kernels:
+                st.write_cache(bufs[b][1], bufs[b][2], kc, vc, stream)
+                out, lse = st.attend(bufs[b][0], kc, vc, bt_dev, spec.scale, stream)
+            else:
+                T = int(q.shape[0])
+                out, lse = st.out[:T], st.lse_buf[:T * spec.num_q_heads].view(spec.num_q_heads, T)
             ev_comp[b].record(stream)
             with torch.cuda.stream(cout):
                 cout.wait_event(ev_comp[b])
@@ -528,6 +534,8 @@ def run_gpu(args):
         step2.v_descale.copy_(step.v_descale)
     e2e, h2d, d2h = time_e2e(P, spec, bt, bt_dev, kc, vc, q, k, v, [step, step2], stream, max(8, args.steps))
     e2e = max_over_ranks(e2e, ws)
+    copy_ms = max_over_ranks(time_e2e(P, spec, bt, bt_dev, kc, vc, q, k, v, [step, step2], stream,
+                                      max(8, args.steps), kernels=False)[0], ws)
     del step2
 
     merge_ms = time_lse_merge(P, spec.total_q, spec.num_q_heads, spec.head_dim, device, stream, flush)
@@ -555,7 +563,9 @@ def run_gpu(args):
         "e2e": {"value": round(ws * step_flop / (e2e * 1e-3) / 1e12, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e, 4),
                 "host_link_gbs": round((h2d + d2h) / (e2e * 1e-3) / 1e9, 1),
-                "timed": "pinned host buffers, two buffer sets, copies on their own streams"},
+                "copy_only_ms": round(copy_ms, 4),
+                "timed": "pinned host buffers, two buffer sets, copies on their own streams; copy_only_ms: "
+                         "the same copies and stream order without the kernels"},
         "gpu_launches": args.steps * (5 + (1 if args.flags & 1 else 0)),
         "clocks": clocks.summary(),
     }
