@@ -67,7 +67,7 @@ WorkspaceLayout workspace_layout(int32_t num_rows, int32_t total_q, int32_t num_
     w.row_ok = o;
     o = align256(o + (size_t)num_rows * sizeof(int32_t));
     w.dec_pre = o;
-    o = align256(o + ((size_t)num_rows + 1) * sizeof(int32_t));
+    o = align256(o + (2 * (size_t)num_rows + 1) * sizeof(int32_t));
     w.units = o;
     o = align256(o + (size_t)w.max_units * sizeof(Unit));
     w.units_sorted = o;

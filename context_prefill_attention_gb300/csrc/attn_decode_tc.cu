@@ -20,9 +20,10 @@
 //
 // Design (sm_103a, head_dim 128, one CTA per SM, persistent):
 //  * work item = (decode row, kv head, split of kDecodeChunk keys); the
-//    scheduler kernel counts them per row (dec_pre), and CTA b takes items b,
-//    b + grid, ...; partial (out, lse) per split as the CUDA-core decode kernel
-//    writes them, merged by decode_merge_kernel;
+//    scheduler kernel lists the full splits first and the partial last splits
+//    after them, longest first (dec_pre), and the CTAs take items in snake
+//    order; partial (out, lse) per split as the CUDA-core decode kernel writes
+//    them, merged by decode_merge_kernel;
 //  * warps 8 (K) and 9 (V) produce: per item the block-table entries of its
 //    keys, then per 128-key tile one TMA box per page (bf16: two 64-dim halves,
 //    128-byte swizzled; FP8: the codes, D bytes per row, into the upper half of
@@ -141,19 +142,33 @@ struct DecItem {
     int32_t ri, req, q_start, hk, split, lo, hi, nt;
 };
 
-// Item p of the decode work list. The caller's items rise, so the row cursor
-// ri only walks forward over the prefix (rows without items are skipped).
-__device__ __forceinline__ DecItem dec_item(const int32_t* pre, int32_t& ri, int32_t p, const pcp_row_t* rows) {
-    while (pre[ri + 1] <= p) ++ri;
-    const pcp_row_t row = rows[ri];
-    const int32_t nsplit = (row.kv_end + kDecodeChunk - 1) / kDecodeChunk;
-    const int32_t rem = p - pre[ri];
+// Item p of the decode work list: first every full kDecodeChunk-key split (row
+// by row, kv head by kv head; pre[i] counts those of the rows before row i,
+// pre[num_rows] all of them), then the partial last splits, hkv items per row
+// in the order of tail_rows (longest partial first). Dealt in snake order, the
+// CTAs then end within a fraction of a split of each other. The caller's items
+// rise, so the row cursor ri only walks forward over the prefix.
+__device__ __forceinline__ DecItem dec_item(const int32_t* pre, int32_t& ri, int32_t p, const pcp_row_t* rows,
+                                            const int32_t* tail_rows, int32_t num_rows, int32_t hkv) {
+    const int32_t nfull = pre[num_rows];
+    const bool full = p < nfull;
+    int32_t r, rem;
+    if (full) {
+        while (pre[ri + 1] <= p) ++ri;
+        r = ri;
+        rem = p - pre[r];
+    } else {
+        rem = p - nfull;
+        r = tail_rows[rem / hkv];
+    }
+    const pcp_row_t row = rows[r];
+    const int32_t nf = row.kv_end / kDecodeChunk;  // full splits of the row (>= 1 on the full side)
     DecItem it;
-    it.ri = ri;
+    it.ri = r;
     it.req = row.req;
     it.q_start = row.q_start;
-    it.hk = rem / nsplit;
-    it.split = rem % nsplit;
+    it.hk = full ? rem / nf : rem % hkv;
+    it.split = full ? rem % nf : nf;
     it.lo = it.split * kDecodeChunk;
     it.hi = min(row.kv_end, it.lo + kDecodeChunk);
     it.nt = (it.hi - it.lo + kKeys - 1) / kKeys;
@@ -373,6 +388,13 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
     const int G = a.hq / a.hkv;
     const int32_t bs = a.block_size;
     const int32_t step = (int32_t)gridDim.x;
+    // item of this CTA in round rd: snake order (forward on even rounds, backward
+    // on odd ones) over the list, whose full splits come first and partial ones
+    // longest first
+    auto item_of_round = [&](int32_t rd) -> int32_t {
+        return rd * step + ((rd & 1) ? step - 1 - (int32_t)blockIdx.x : (int32_t)blockIdx.x);
+    };
+    const int32_t* tail_rows = a.dec_pre + a.num_rows + 1;
 
     for (int i = threadIdx.x; i <= a.num_rows; i += tc_threads(F8, GP)) pre[i] = a.dec_pre[i];
     if (threadIdx.x == 0) {
@@ -431,8 +453,8 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
         uint32_t gt = 0, ic = 0;
         int32_t ri = 0;
         bool ok = true;
-        for (int32_t p = blockIdx.x; p < total && ok; p += step) {
-            const DecItem it = dec_item(pre, ri, p, a.rows);
+        for (int32_t rd = 0, p = item_of_round(0); p < total && ok; p = item_of_round(++rd)) {
+            const DecItem it = dec_item(pre, ri, p, a.rows, tail_rows, a.num_rows, a.hkv);
             // the split's block-table entries as first cache rows; a bad id maps to a
             // row past the cache (zero filled) and reports PCP_ERR_RANGE
             const int32_t* table = a.block_table + (size_t)it.req * a.max_blocks;
@@ -515,8 +537,8 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
             int32_t ri = 0;
             bool ok = true;
             const bool s_role = warp == kMmaWarp;
-            for (int32_t p = blockIdx.x; p < total && ok; p += step) {
-                const DecItem it = dec_item(pre, ri, p, a.rows);
+            for (int32_t rd = 0, p = item_of_round(0); p < total && ok; p = item_of_round(++rd)) {
+                const DecItem it = dec_item(pre, ri, p, a.rows, tail_rows, a.num_rows, a.hkv);
                 const int qb = ic & 1;
                 if (s_role && !(ok = mbar_wait(q_full(qb), (ic >> 1) & 1, abort_flag))) break;
                 for (int j = 0; j < it.nt; ++j, ++g) {
@@ -579,8 +601,8 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
         uint32_t gt = 0, ic = 0;
         int32_t ri = 0;
         bool ok = true;
-        for (int32_t p = blockIdx.x; p < total && ok; p += step) {
-            const DecItem it = dec_item(pre, ri, p, a.rows);
+        for (int32_t rd = 0, p = item_of_round(0); p < total && ok; p = item_of_round(++rd)) {
+            const DecItem it = dec_item(pre, ri, p, a.rows, tail_rows, a.num_rows, a.hkv);
             const int qb = ic & 1;
             if (cset == 0) {
                 if (!(ok = mbar_wait_warp(qc_full(qb), (ic >> 1) & 1, abort_flag))) break;
@@ -624,8 +646,8 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
         int32_t ri = 0;
         bool ok = true;     // every wait of this thread so far completed
         bool stop = false;  // the joint decision to stop (FP8: the warpgroup's; bf16: both's), once per item
-        for (int32_t p = blockIdx.x; p < total && !stop; p += step, ++ic) {
-            const DecItem it = dec_item(pre, ri, p, a.rows);
+        for (int32_t rd = 0, p = item_of_round(0); p < total && !stop; p = item_of_round(++rd), ++ic) {
+            const DecItem it = dec_item(pre, ri, p, a.rows, tail_rows, a.num_rows, a.hkv);
             const float kd = F8 ? __ldg(a.k_descale + (size_t)it.req * a.hkv + it.hk) : 1.f;
             const float sl2 = a.scale * kd * kLog2e;
             // FP8: the power of two that undoes each head's q scaling (see q_to_e4m3_terms)

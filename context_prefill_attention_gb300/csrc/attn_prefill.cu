@@ -954,15 +954,28 @@ __device__ __forceinline__ int32_t unit_cost(const Unit& u, const pcp_row_t* row
     return tiles_of(u.k_lo, min(u.k_hi, pos0 + rv), bs);
 }
 
+// Partial last splits of decode rows, bucketed by their 128-key tiles (1 .. 16).
+constexpr int kTailBuckets = kDecodeChunk / kBlockN;
+
 // Check every row, then build the prefill work list: one unit per (valid
 // non-decode row, 128-token tile, pass), ordered by the number of key tiles,
-// longest first. Also counts the decode work items (kv head x kDecodeChunk-key split of
-// each valid decode row): dec_pre[i] = items of rows before row i, header[1] =
-// their total.
+// longest first. Also lays out the decode work items (kv head x kDecodeChunk-key
+// split of each valid decode row), full splits first and partial last splits
+// after them, longest first: dec_pre[i] = full-split items of the rows before
+// row i (dec_pre[num_rows]: all of them), dec_pre[num_rows + 1 + t] = the t-th
+// row with a partial last split, header[1] = the number of items.
 __global__ void __launch_bounds__(kSchedThreads, 1)
     schedule_kernel(PrefillArgs a, int32_t flags, Unit* units, Unit* sorted, int32_t* header,
                     int32_t* row_ok, int32_t* dec_pre, int64_t max_units) {
     __shared__ int32_t warp_sums[32];
+    // decode rows with a partial last split per bucket, their first list
+    // position, and the positions taken so far
+    __shared__ int32_t tail_cnt[kTailBuckets + 1], tail_off[kTailBuckets + 1], tail_fill[kTailBuckets + 1];
+    if (threadIdx.x <= kTailBuckets) {
+        tail_cnt[threadIdx.x] = 0;
+        tail_fill[threadIdx.x] = 0;
+    }
+    __syncthreads();
     // bitonic sort keys, or the counters of the counting sort
     __shared__ __align__(16) unsigned long long keys[kSortCap];
     const pcp_row_t* rows = a.rows;
@@ -986,7 +999,11 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
             row_ok[ri] = ok ? 1 : 0;
             if (!ok) report_status(a.status, PCP_ERR_RANGE);
             if (ok && !row.is_decode) cnt = ((row.q_len + kBlockM - 1) / kBlockM) * passes;
-            if (ok && row.is_decode) dcnt = ((row.kv_end + kDecodeChunk - 1) / kDecodeChunk) * a.hkv;
+            if (ok && row.is_decode) {
+                dcnt = (row.kv_end / kDecodeChunk) * a.hkv;
+                const int32_t part = row.kv_end % kDecodeChunk;
+                if (part) atomicAdd(&tail_cnt[(part + kBlockN - 1) / kBlockN], 1);
+            }
         }
         int32_t dtot;
         const int32_t doff = dbase + block_exclusive_scan(dcnt, warp_sums, &dtot);
@@ -1016,10 +1033,27 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
         base += tot;
     }
     const int32_t n = (int32_t)min((int64_t)base, max_units);
+    __syncthreads();  // tail counts complete
     if (threadIdx.x == 0) {
+        int32_t t = 0;
+        for (int b = kTailBuckets; b >= 1; --b) {
+            tail_off[b] = t;
+            t += tail_cnt[b];
+        }
         header[0] = n;
-        header[1] = dbase;
+        header[1] = dbase + t * a.hkv;
         dec_pre[num_rows] = dbase;
+    }
+    __syncthreads();
+    // the rows with a partial last split, longest first (any order within a
+    // bucket: every item writes only its own partial, so the order changes no result)
+    for (int32_t ri = threadIdx.x; ri < num_rows; ri += kSchedThreads) {
+        if (!row_ok[ri]) continue;
+        const pcp_row_t row = rows[ri];
+        const int32_t part = row.kv_end % kDecodeChunk;
+        if (!row.is_decode || !part) continue;
+        const int b = (part + kBlockN - 1) / kBlockN;
+        dec_pre[num_rows + 1 + tail_off[b] + atomicAdd(&tail_fill[b], 1)] = ri;
     }
     // every thread's units[] writes must be visible before any thread reads them
     __syncthreads();

@@ -33,7 +33,9 @@ struct Unit {
 struct WorkspaceLayout {
     size_t header;        // int32[64]: [0] = number of units
     size_t row_ok;        // int32[num_rows]: 1 for a row that passed the checks
-    size_t dec_pre;       // int32[num_rows + 1]: decode work items of the rows before each row
+    size_t dec_pre;       // int32[2 num_rows + 1]: full-split decode items of the rows before each
+                          // row ([num_rows]: all of them), then the rows with a partial last
+                          // split, longest partial first
     size_t units;         // Unit[max_units], unsorted
     size_t units_sorted;  // Unit[max_units], longest first
     size_t part_out;      // nparts x fp32 [T][Hq][D] (separate-context / KV-shard modes)
@@ -83,8 +85,9 @@ struct PrefillArgs {
     const int32_t* row_ok;
     const Unit* units;
     const int32_t* num_units;   // header: [0] prefill units, [1] decode work items
-    // decode work items (kv head x kDecodeChunk-key split of a decode row) of the rows
-    // before row i, for i = 0..num_rows (the last entry is the total)
+    // decode work items (kv head x kDecodeChunk-key split of a decode row): full-split
+    // items of the rows before row i, for i = 0..num_rows (the last entry: all full
+    // splits), then from [num_rows + 1] the rows with a partial last split, longest first
     const int32_t* dec_pre;
     int32_t* status;
     // FP8 (e4m3) cache: per-(request, kv head) descales [num_reqs][hkv]; both

@@ -86,13 +86,13 @@ DECODE_CHUNK = 2048
 def read_schedule(case: Case):
     """Unit count and sorted units from the workspace of the last call. The
     offsets follow pcp_attn_varlen's workspace layout: a 64-entry int32 header
-    (the unit count first), the row flags, the decode-item prefix (num_rows + 1
+    (the unit count first), the row flags, the decode-item layout (2 num_rows + 1
     int32), the unsorted units, then the sorted units (16 bytes each), every
     part 256-byte aligned."""
     spec, flags = case.spec, case.flags
     n_rows = int(case.plan["rows"].shape[0])
     max_units = _passes(flags) * (-(-spec.total_q // BLOCK_M) + n_rows)
-    off_units = 256 + _align256(n_rows * 4) + _align256((n_rows + 1) * 4)
+    off_units = 256 + _align256(n_rows * 4) + _align256((2 * n_rows + 1) * 4)
     off_sorted = off_units + _align256(max_units * 16)
     ws = case.step.workspace[:off_sorted + max_units * 16].cpu().numpy()
     n = int(ws[:4].view(np.int32)[0])
@@ -100,19 +100,38 @@ def read_schedule(case: Case):
     return n, units
 
 
-def read_decode_prefix(case: Case):
-    """header[1] and the decode-item prefix of the last call."""
+def read_decode_items(case: Case):
+    """header[1], the full-split prefix (num_rows + 1 int32) and the list of rows
+    with a partial last split, as the last call left them."""
     n_rows = int(case.plan["rows"].shape[0])
     off = 256 + _align256(n_rows * 4)
-    ws = case.step.workspace[:off + (n_rows + 1) * 4].cpu().numpy()
-    return int(ws[4:8].view(np.int32)[0]), ws[off:off + (n_rows + 1) * 4].view(np.int32).copy()
+    ws = case.step.workspace[:off + (2 * n_rows + 1) * 4].cpu().numpy()
+    region = ws[off:off + (2 * n_rows + 1) * 4].view(np.int32).copy()
+    return int(ws[4:8].view(np.int32)[0]), region[:n_rows + 1], region[n_rows + 1:]
 
 
-def expected_decode_prefix(rows: np.ndarray, num_kv_heads: int) -> np.ndarray:
-    """Items of the rows before each row: kv heads x 2048-key splits of every
-    decode row, none for prefill rows."""
-    cnt = [num_kv_heads * (-(-int(r[5]) // DECODE_CHUNK)) if int(r[7]) else 0 for r in rows]
+def expected_full_prefix(rows: np.ndarray, num_kv_heads: int) -> np.ndarray:
+    """Full-split items of the rows before each row: kv heads x whole 2048-key
+    splits of every decode row, none for prefill rows."""
+    cnt = [num_kv_heads * (int(r[5]) // DECODE_CHUNK) if int(r[7]) else 0 for r in rows]
     return np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32)
+
+
+def check_decode_items(case: Case) -> int:
+    """The decode work list: the full splits' prefix, then every decode row with
+    a partial last split exactly once, in non-increasing order of that split's
+    128-key tiles; header[1] counts kv heads x (full splits + partial splits)."""
+    rows = case.plan["rows"]
+    hkv = case.spec.num_kv_heads
+    total, pre, tail_area = read_decode_items(case)
+    np.testing.assert_array_equal(pre, expected_full_prefix(rows, hkv))
+    tail_rows = [i for i, r in enumerate(rows) if int(r[7]) and int(r[5]) % DECODE_CHUNK]
+    listed = [int(x) for x in tail_area[:len(tail_rows)]]
+    assert sorted(listed) == tail_rows, "every row with a partial split once"
+    tiles = [-(-(int(rows[i][5]) % DECODE_CHUNK) // 128) for i in listed]
+    assert all(x >= y for x, y in zip(tiles, tiles[1:])), "partial splits longest first"
+    assert total == int(pre[-1]) + hkv * len(tail_rows)
+    return total
 
 
 def check_schedule(case: Case):
@@ -140,15 +159,29 @@ def _run(spec, flags, tokens=None):
 
 def test_bitonic_path_order_and_parity():
     """A list under the limit: exact longest-first order. The decode rows'
-    work-item prefix is checked too."""
+    work list is checked too."""
     spec = W.custom_spec([3, 64, 129, 1, 17, 256, 2, 90, 1, 500], [0, 5, 0, 44, 130, 0, 1, 7, 300, 0],
                          num_q_heads=8, num_kv_heads=4, head_dim=128, seed=31)
     case = _run(spec, 0)
     assert 0 < check_schedule(case) <= SORT_CAP
-    total, pre = read_decode_prefix(case)
-    want = expected_decode_prefix(case.plan["rows"], spec.num_kv_heads)
-    assert total == int(want[-1]) > 0
-    np.testing.assert_array_equal(pre, want)
+    assert check_decode_items(case) > 0
+
+
+def test_decode_items_full_splits_then_partials_longest_first():
+    """Decode rows whose keys (cached context + the new token) end on, before
+    and after split boundaries (2048 keys: one full split, no partial; 2049: a
+    one-key partial; 6000: two full splits and a 1904-key partial; ...), beside
+    a prefill row: the work list holds the full splits first and the partial
+    ones longest first, and the result matches the oracle."""
+    keys = [2048, 2049, 2047, 6000, 2, 130, 4096, 5000, 128, 4200]
+    spec = W.custom_spec([1] * len(keys) + [70], [k - 1 for k in keys] + [300], num_q_heads=8, num_kv_heads=2,
+                         head_dim=128, seed=47)
+    case = _run(spec, 0)
+    rows = case.plan["rows"]
+    n_partial = sum(1 for r in rows if int(r[7]) and int(r[5]) % DECODE_CHUNK)
+    assert n_partial == 8
+    assert check_decode_items(case) == 2 * (int(sum(int(r[5]) // DECODE_CHUNK for r in rows if int(r[7]))) +
+                                            n_partial)
 
 
 def test_kv_shards_64_over_limit():
