@@ -527,6 +527,41 @@ def run_gpu(args):
         dec_line = {"gbs": round(dec_gbs, 1), "ms": round(dec_avg, 4), "frac_hbm_peak": round(dec_gbs / peaks["hbm"], 4),
                     "bytes": work["decode_bytes"]}
 
+    # ---- the same steps with the decode rows beside the prefill rows (the SMs
+    # pcp_decode_sms picks from the plan); each kernel then runs on part of the
+    # GPU, so the headline above keeps the sequence and this is reported apart
+    beside = None
+    step.decode_beside = True
+    step.build_plan(spec.query_len, spec.num_computed, bt)
+    if step.decode_sms > 0:
+        for _ in range(args.warmup):
+            one_step()
+        torch.cuda.synchronize()
+        ev2 = [[_mk() for _ in range(6)] for _ in range(args.steps)]
+        for e in ev2:  # recorded once here so that torch accepts those the library records
+            for x in e:
+                x.record(stream)
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            P.pcp_set_profile_events(ev2[i][2], ev2[i][3], ev2[i][4], ev2[i][5])
+            ev2[i][0].record(stream)
+            one_step()
+            ev2[i][1].record(stream)
+        P.pcp_set_profile_events()
+        torch.cuda.synchronize()
+        step.check_status()
+        b_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in ev2), ws) / args.steps
+        beside = {"decode_sms": step.decode_sms, "ms_per_step": round(b_ms, 4),
+                  "value": round(ws * step_flop / (b_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+                  "prefill_ms": round(statistics.mean(e[2].elapsed_time(e[3]) for e in ev2), 4),
+                  "decode_ms": round(statistics.mean(e[4].elapsed_time(e[5]) for e in ev2), 4),
+                  "timed": f"{args.steps} more steps, L2 flushed between them, decode rows on "
+                           f"{step.decode_sms} SMs of a second stream beside the prefill rows "
+                           "(PCP_ATTN_DECODE_SMS)"}
+    step.decode_beside = False
+    step.build_plan(spec.query_len, spec.num_computed, bt)
+
     # ---- end to end from pinned host buffers, copies overlapped with the kernels
     step2 = make_step(P, spec, bt, device, args.flags, kv_fp8)
     if kv_fp8:
@@ -566,6 +601,7 @@ def run_gpu(args):
                 "copy_only_ms": round(copy_ms, 4),
                 "timed": "pinned host buffers, two buffer sets, copies on their own streams; copy_only_ms: "
                          "the same copies and stream order without the kernels"},
+        "decode_beside_prefill": beside,
         "gpu_launches": args.steps * (5 + (1 if args.flags & 1 else 0)),
         "clocks": clocks.summary(),
     }

@@ -34,10 +34,16 @@ def PCP_ATTN_KV_SHARDS(n: int) -> int:
     (decode-context-parallel emulation) and merge them by LSE."""
     return (int(n) & 0xFF) << 8
 
+
+def PCP_ATTN_DECODE_SMS(n: int) -> int:
+    """Flag: run the decode rows on n SMs beside the prefill rows (see
+    :func:`pcp_decode_sms`)."""
+    return (int(n) & 0xFF) << 16
+
 ROW_FIELDS = ("req", "shard", "q_start", "q_len", "ctx_len", "kv_end", "causal_off", "is_decode")
 
 # every symbol include/pcp.h declares
-EXPORTS = ("pcp_build_row_plan", "pcp_mask_slots_for_shard", "pcp_kv_cache_write",
+EXPORTS = ("pcp_build_row_plan", "pcp_mask_slots_for_shard", "pcp_decode_sms", "pcp_kv_cache_write",
            "pcp_kv_cache_write_fp8", "pcp_attn_workspace_size", "pcp_attn_varlen", "pcp_attn_varlen_noalloc",
            "pcp_attn_varlen_fp8kv", "pcp_lse_merge",
            "pcp_set_profile_events", "pcp_selftest_bounded_wait",
@@ -73,6 +79,8 @@ def load(path: Optional[str] = None):
     lib.pcp_build_row_plan.restype = ctypes.c_int
     lib.pcp_mask_slots_for_shard.argtypes = [P, P, i32, i32, P]
     lib.pcp_mask_slots_for_shard.restype = ctypes.c_int
+    lib.pcp_decode_sms.argtypes = [P, i32, i32, i32, i32, i32, i32]
+    lib.pcp_decode_sms.restype = i32
     lib.pcp_kv_cache_write.argtypes = [P, P, P, i32, P, P, i64, i32, i32, i32, P, P]
     lib.pcp_kv_cache_write.restype = ctypes.c_int
     lib.pcp_kv_cache_write_fp8.argtypes = [P, P, P, i32, P, P, i64, i32, i32, i32, f32, f32, P, P]
@@ -232,6 +240,18 @@ def pcp_mask_slots_for_shard(slot_mapping: np.ndarray, owner_shard: np.ndarray, 
     _check(lib.pcp_mask_slots_for_shard(_np_ptr(s), _np_ptr(o), int(s.shape[0]), shard, _np_ptr(out)),
            "pcp_mask_slots_for_shard")
     return out
+
+
+def pcp_decode_sms(rows: np.ndarray, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                   kv_cache_fp8: bool, num_sms: int) -> int:
+    """SMs for the decode rows of a host row plan (int32 ``[n, 8]``) beside its
+    prefill rows, or 0 to run them in sequence (host function, no GPU)."""
+    lib = load()
+    r = np.ascontiguousarray(rows, dtype=np.int32)
+    if r.ndim != 2 or (r.shape[0] and r.shape[1] != 8):
+        raise ValueError(f"rows: shape {r.shape}, expected [n, 8]")
+    return int(lib.pcp_decode_sms(_np_ptr(r), int(r.shape[0]), int(num_q_heads), int(num_kv_heads),
+                                  int(head_dim), 1 if kv_cache_fp8 else 0, int(num_sms)))
 
 
 def pcp_kv_cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,

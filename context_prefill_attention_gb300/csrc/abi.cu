@@ -1,11 +1,13 @@
 // The C ABI of libpcp (declared in include/pcp.h): argument validation on the
 // host, workspace layout and the launch sequence of one attention call.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
 
 #include <mutex>
 
+#include "ctx_table.h"
 #include "pcp.h"
 #include "pcp_internal.h"
 
@@ -41,6 +43,68 @@ inline bool overlaps_any(Span out, const Span* ins, int n) {
 }  // namespace
 
 void set_last_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
+
+namespace {
+using PFN_ctxGetCurrent = CUresult (*)(CUcontext*);
+using PFN_ctxGetId = CUresult (*)(CUcontext, unsigned long long*);
+
+// A driver API function by name, or nullptr.
+void* driver_entry(const char* name) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return p;
+}
+
+// The internal stream of PCP_ATTN_DECODE_SMS with its fork and join events, one
+// per CUDA context (streams and events belong to the context that made them).
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t forked = nullptr, done = nullptr;
+    std::mutex mu;  // one call's fork, launches and join at a time
+};
+CtxTable<32> g_side;
+std::mutex g_side_create;
+
+// The current context's side stream, created on first use; nullptr if it
+// cannot be had (the call then runs its decode rows in sequence).
+SideStream* side_stream() {
+    uint64_t id = 0;
+    if (!current_ctx_id(&id)) return nullptr;
+    if (void* p = g_side.find(id)) return static_cast<SideStream*>(p);
+    std::lock_guard<std::mutex> lock(g_side_create);
+    if (void* p = g_side.find(id)) return static_cast<SideStream*>(p);
+    SideStream* ss = new SideStream();
+    if (cudaStreamCreateWithFlags(&ss->stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss->forked, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss->done, cudaEventDisableTiming) != cudaSuccess) {
+        if (ss->done) cudaEventDestroy(ss->done);
+        if (ss->forked) cudaEventDestroy(ss->forked);
+        if (ss->stream) cudaStreamDestroy(ss->stream);
+        delete ss;
+        cudaGetLastError();
+        return nullptr;
+    }
+    g_side.put(id, ss);
+    return ss;
+}
+}  // namespace
+
+bool current_ctx_id(uint64_t* id) {
+    // resolved once (thread-safe static initialisation)
+    static const PFN_ctxGetCurrent get_current =
+        reinterpret_cast<PFN_ctxGetCurrent>(driver_entry("cuCtxGetCurrent"));
+    static const PFN_ctxGetId get_id = reinterpret_cast<PFN_ctxGetId>(driver_entry("cuCtxGetId"));
+    if (!get_current || !get_id) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    unsigned long long v = 0;
+    if (get_id(ctx, &v) != CUDA_SUCCESS) return false;
+    *id = v;
+    return true;
+}
 
 int num_sms() {
     static int cached[64] = {0};
@@ -262,15 +326,47 @@ int pcp::attn_call(const void* q, const void* key_cache, const void* value_cache
                              reinterpret_cast<int32_t*>(ws + w.row_ok),
                              reinterpret_cast<int32_t*>(ws + w.dec_pre), w.max_units, s);
     if (rc != PCP_OK) return rc;
-    if (g_profile[2]) cudaEventRecord(g_profile[2], s);
-    rc = launch_decode(a, reinterpret_cast<float*>(ws + w.dec_out), reinterpret_cast<float*>(ws + w.dec_lse),
-                       w.max_splits, s);
-    if (rc != PCP_OK) return rc;
-    if (g_profile[3]) cudaEventRecord(g_profile[3], s);
-    if (g_profile[0]) cudaEventRecord(g_profile[0], s);
-    rc = launch_prefill(a, s);
-    if (rc != PCP_OK) return rc;
-    if (g_profile[1]) cudaEventRecord(g_profile[1], s);
+    float* dec_out = reinterpret_cast<float*>(ws + w.dec_out);
+    float* dec_lse = reinterpret_cast<float*>(ws + w.dec_lse);
+    const int nsm = num_sms();
+    const int kdec = attn_decode_sms(flags);
+    SideStream* side = (kdec > 0 && kdec < nsm && decode_side_applies(a)) ? side_stream() : nullptr;
+    if (side) {
+        // decode rows on kdec SMs of the side stream, prefill rows on the others
+        std::lock_guard<std::mutex> lock(side->mu);
+        cudaError_t e = cudaEventRecord(side->forked, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->forked, 0);
+        if (e != cudaSuccess) {
+            set_last_cuda_error(e);
+            return PCP_ERR_CUDA;
+        }
+        if (g_profile[2]) cudaEventRecord(g_profile[2], side->stream);
+        rc = launch_decode(a, dec_out, dec_lse, w.max_splits, side->stream, kdec);
+        if (rc == PCP_OK) {
+            if (g_profile[3]) cudaEventRecord(g_profile[3], side->stream);
+            if (g_profile[0]) cudaEventRecord(g_profile[0], s);
+            rc = launch_prefill(a, s, nsm - kdec);
+            if (rc == PCP_OK && g_profile[1]) cudaEventRecord(g_profile[1], s);
+        }
+        // joined even after a failed launch: nothing of this call runs on after the
+        // caller's stream has moved past it
+        e = cudaEventRecord(side->done, side->stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, side->done, 0);
+        if (rc != PCP_OK) return rc;
+        if (e != cudaSuccess) {
+            set_last_cuda_error(e);
+            return PCP_ERR_CUDA;
+        }
+    } else {
+        if (g_profile[2]) cudaEventRecord(g_profile[2], s);
+        rc = launch_decode(a, dec_out, dec_lse, w.max_splits, s);
+        if (rc != PCP_OK) return rc;
+        if (g_profile[3]) cudaEventRecord(g_profile[3], s);
+        if (g_profile[0]) cudaEventRecord(g_profile[0], s);
+        rc = launch_prefill(a, s);
+        if (rc != PCP_OK) return rc;
+        if (g_profile[1]) cudaEventRecord(g_profile[1], s);
+    }
     if (a.nparts > 0) rc = launch_separate_merge(a, s);
     return rc;
 }

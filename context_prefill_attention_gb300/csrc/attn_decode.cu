@@ -493,10 +493,12 @@ int launch_decode_d(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_
 #define PCP_DECODE_TC 1  // 1: the tensor-core decode where it applies (head_dim 128, G <= 8)
 #endif
 
+bool decode_side_applies(const PrefillArgs& a) { return PCP_DECODE_TC && decode_tc_applies(a); }
+
 int launch_decode(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, int grid) {
     if (a.d != 64 && a.d != 128) return PCP_ERR_UNSUPPORTED;
-    int rc = PCP_DECODE_TC ? launch_decode_tc(a, dec_out, dec_lse, max_splits, stream) : PCP_ERR_UNSUPPORTED;
+    int rc = PCP_DECODE_TC ? launch_decode_tc(a, dec_out, dec_lse, max_splits, stream, grid) : PCP_ERR_UNSUPPORTED;
     // partials per split: the tensor-core kernel writes one per softmax warpgroup
     // over an FP8 cache and with more than 8 q heads per kv head
     int pps = (a.k_descale || a.hq / a.hkv > 8) ? 2 : 1;

@@ -824,7 +824,8 @@ __global__ void __launch_bounds__(tc_threads(F8, GP), 1)
 }
 
 template <bool F8, int GP>
-int launch_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits, cudaStream_t stream) {
+int launch_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits, cudaStream_t stream,
+              int grid) {
     const int64_t slots = a.num_blocks * a.block_size;
     const int q_rows = a.hq < kN ? a.hq : kN;
     CUtensorMap tq, tk, tv;
@@ -840,7 +841,8 @@ int launch_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_
     cudaError_t e =
         cudaFuncSetAttribute(decode_tc_kernel<F8, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
-    decode_tc_kernel<F8, GP><<<num_sms(), tc_threads(F8, GP), smem, stream>>>(tq, tk, tv, a, dec_out, dec_lse,
+    const int ctas = grid > 0 && grid < num_sms() ? grid : num_sms();
+    decode_tc_kernel<F8, GP><<<ctas, tc_threads(F8, GP), smem, stream>>>(tq, tk, tv, a, dec_out, dec_lse,
                                                                               max_splits, q_rows);
     e = cudaGetLastError();
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
@@ -849,25 +851,29 @@ int launch_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_
 
 }  // namespace
 
-int launch_decode_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
-                     cudaStream_t stream) {
+bool decode_tc_applies(const PrefillArgs& a) {
     const int G = a.hkv > 0 ? a.hq / a.hkv : 0;
-    if (a.d != kD || G < 1 || G > (a.k_descale ? 8 : kMaxG) || a.num_rows > kDecTcMaxRows || a.block_size > kKeys ||
-        kKeys % a.block_size != 0)
-        return PCP_ERR_UNSUPPORTED;
+    return a.d == kD && G >= 1 && G <= (a.k_descale ? 8 : kMaxG) && a.num_rows <= kDecTcMaxRows &&
+           a.block_size <= kKeys && kKeys % a.block_size == 0;
+}
+
+int launch_decode_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
+                     cudaStream_t stream, int grid) {
+    if (!decode_tc_applies(a)) return PCP_ERR_UNSUPPORTED;
+    const int G = a.hq / a.hkv;
     // heads per group padded to a power of two (the padded heads' results are not written)
     const int GP = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : G <= 8 ? 8 : 16;
     if (a.k_descale) {
-        if (GP == 1) return launch_tc<true, 1>(a, dec_out, dec_lse, max_splits, stream);
-        if (GP == 2) return launch_tc<true, 2>(a, dec_out, dec_lse, max_splits, stream);
-        if (GP == 4) return launch_tc<true, 4>(a, dec_out, dec_lse, max_splits, stream);
-        return launch_tc<true, 8>(a, dec_out, dec_lse, max_splits, stream);
+        if (GP == 1) return launch_tc<true, 1>(a, dec_out, dec_lse, max_splits, stream, grid);
+        if (GP == 2) return launch_tc<true, 2>(a, dec_out, dec_lse, max_splits, stream, grid);
+        if (GP == 4) return launch_tc<true, 4>(a, dec_out, dec_lse, max_splits, stream, grid);
+        return launch_tc<true, 8>(a, dec_out, dec_lse, max_splits, stream, grid);
     }
-    if (GP == 1) return launch_tc<false, 1>(a, dec_out, dec_lse, max_splits, stream);
-    if (GP == 2) return launch_tc<false, 2>(a, dec_out, dec_lse, max_splits, stream);
-    if (GP == 4) return launch_tc<false, 4>(a, dec_out, dec_lse, max_splits, stream);
-    if (GP == 8) return launch_tc<false, 8>(a, dec_out, dec_lse, max_splits, stream);
-    return launch_tc<false, 16>(a, dec_out, dec_lse, max_splits, stream);
+    if (GP == 1) return launch_tc<false, 1>(a, dec_out, dec_lse, max_splits, stream, grid);
+    if (GP == 2) return launch_tc<false, 2>(a, dec_out, dec_lse, max_splits, stream, grid);
+    if (GP == 4) return launch_tc<false, 4>(a, dec_out, dec_lse, max_splits, stream, grid);
+    if (GP == 8) return launch_tc<false, 8>(a, dec_out, dec_lse, max_splits, stream, grid);
+    return launch_tc<false, 16>(a, dec_out, dec_lse, max_splits, stream, grid);
 }
 
 }  // namespace pcp

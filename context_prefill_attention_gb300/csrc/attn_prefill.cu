@@ -1165,7 +1165,7 @@ bool make_row_map(CUtensorMap* m, const void* base, int D, int esize, int64_t mi
 }
 
 template <int D, bool F8>
-int launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
+int launch_prefill_d(const PrefillArgs& a, cudaStream_t stream, int grid) {
     CUtensorMap tq, tk, tv;
     const int64_t slots = a.num_blocks * a.block_size;
     // FP8: K codes 128-byte swizzled where they are the MMA operand (D = 128)
@@ -1179,7 +1179,10 @@ int launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
     cudaError_t e =
         cudaFuncSetAttribute(prefill_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
-    prefill_kernel<D, F8><<<num_sms(), kThreads, smem, stream>>>(tq, tk, tv, a);
+    // persistent: the work list is dealt over however many CTAs run (fewer when
+    // the decode rows take some SMs beside it)
+    const int ctas = grid > 0 && grid < num_sms() ? grid : num_sms();
+    prefill_kernel<D, F8><<<ctas, kThreads, smem, stream>>>(tq, tk, tv, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) { set_last_cuda_error(e); return PCP_ERR_CUDA; }
     return PCP_OK;
@@ -1197,10 +1200,12 @@ int launch_schedule(const PrefillArgs& a, int32_t flags, Unit* units, Unit* unit
     return PCP_OK;
 }
 
-int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int grid) {
     const bool f8 = a.k_descale != nullptr;
-    if (a.d == 64) return f8 ? launch_prefill_d<64, true>(a, stream) : launch_prefill_d<64, false>(a, stream);
-    if (a.d == 128) return f8 ? launch_prefill_d<128, true>(a, stream) : launch_prefill_d<128, false>(a, stream);
+    if (a.d == 64)
+        return f8 ? launch_prefill_d<64, true>(a, stream, grid) : launch_prefill_d<64, false>(a, stream, grid);
+    if (a.d == 128)
+        return f8 ? launch_prefill_d<128, true>(a, stream, grid) : launch_prefill_d<128, false>(a, stream, grid);
     return PCP_ERR_UNSUPPORTED;
 }
 

@@ -34,41 +34,12 @@ __device__ __align__(256) unsigned char g_scratch[kStaticScratchBytes];
 // a context created after a device reset looks the address up again.
 pcp::CtxTable<32> g_scratch_addr;
 
-using PFN_ctxGetCurrent = CUresult (*)(CUcontext*);
-using PFN_ctxGetId = CUresult (*)(CUcontext, unsigned long long*);
-
-// A driver API function by name, or nullptr.
-void* driver_entry(const char* name) {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-        return nullptr;
-    return p;
-}
-
-// ID of the current context; false when no context is current yet or the
-// driver lacks the query.
-bool current_ctx_id(uint64_t* id) {
-    // resolved once (thread-safe static initialisation)
-    static const PFN_ctxGetCurrent get_current =
-        reinterpret_cast<PFN_ctxGetCurrent>(driver_entry("cuCtxGetCurrent"));
-    static const PFN_ctxGetId get_id = reinterpret_cast<PFN_ctxGetId>(driver_entry("cuCtxGetId"));
-    if (!get_current || !get_id) return false;
-    CUcontext ctx = nullptr;
-    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
-    unsigned long long v = 0;
-    if (get_id(ctx, &v) != CUDA_SUCCESS) return false;
-    *id = v;
-    return true;
-}
-
 // The workspace provider of pcp_attn_varlen_noalloc: the scratch array of the
 // current device, if the call fits in it.
 int scratch_workspace(size_t need, void** ws, size_t* bytes) {
     if (need > kStaticScratchBytes) return PCP_ERR_WORKSPACE;
     uint64_t id = 0;
-    bool have_id = current_ctx_id(&id);
+    bool have_id = pcp::current_ctx_id(&id);
     void* p = have_id ? g_scratch_addr.find(id) : nullptr;
     if (!p) {
         const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
@@ -76,7 +47,7 @@ int scratch_workspace(size_t need, void** ws, size_t* bytes) {
             pcp::set_last_cuda_error(e);
             return PCP_ERR_CUDA;
         }
-        if (!have_id) have_id = current_ctx_id(&id);  // the lookup made the context current
+        if (!have_id) have_id = pcp::current_ctx_id(&id);  // the lookup made the context current
         if (have_id) g_scratch_addr.put(id, p);
     }
     *ws = p;

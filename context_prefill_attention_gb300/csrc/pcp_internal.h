@@ -52,7 +52,7 @@ struct WorkspaceLayout {
 inline int32_t attn_partials(int32_t flags) {
     const int32_t shards = (flags >> 8) & 0xFF;
     const bool separate = (flags & PCP_ATTN_SEPARATE_CONTEXT) != 0;
-    if (flags & ~(PCP_ATTN_SEPARATE_CONTEXT | PCP_ATTN_SPLIT_AT_ROW_START | 0xFF00)) return -1;
+    if (flags & ~(PCP_ATTN_SEPARATE_CONTEXT | PCP_ATTN_SPLIT_AT_ROW_START | 0xFF00 | 0xFF0000)) return -1;
     if (shards == 1 || shards > 64 || (shards && separate)) return -1;
     return separate ? 2 : shards;
 }
@@ -60,7 +60,13 @@ inline int32_t attn_partials(int32_t flags) {
 WorkspaceLayout workspace_layout(int32_t num_rows, int32_t total_q, int32_t num_q_heads,
                                  int32_t head_dim, int32_t max_kv_len, int32_t flags);
 
+// SMs for the decode rows beside the prefill (PCP_ATTN_DECODE_SMS), 0: in sequence.
+inline int32_t attn_decode_sms(int32_t flags) { return (flags >> 16) & 0xFF; }
+
 void set_last_cuda_error(cudaError_t e);
+// ID of the current CUDA context (process-unique, never reused); false when no
+// context is current or the driver lacks the query.
+bool current_ctx_id(uint64_t* id);
 int num_sms();
 
 struct PrefillArgs {
@@ -124,17 +130,24 @@ int attn_call(const void* q, const void* key_cache, const void* value_cache, con
 int launch_schedule(const PrefillArgs& a, int32_t flags, Unit* units, Unit* units_sorted,
                     int32_t* header, int32_t* row_ok, int32_t* dec_pre, int64_t max_units,
                     cudaStream_t stream);
-int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+// grid: CTAs of the persistent kernel (0: one per SM).
+int launch_prefill(const PrefillArgs& a, cudaStream_t stream, int grid = 0);
+// grid: CTAs of the tensor-core decode kernel (0: one per SM); the CUDA-core
+// decode sizes its own grid.
 int launch_decode(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
-                  cudaStream_t stream);
+                  cudaStream_t stream, int grid = 0);
 // The tensor-core decode (head_dim 128, up to 16 q heads per kv head with a
 // bf16 cache and 8 with an FP8 one, at most kDecTcMaxRows rows);
 // PCP_ERR_UNSUPPORTED for any other shape. Over an FP8 cache and with more
 // than 8 q heads per kv head it writes two partials per split (slots 2 split
 // and 2 split + 1 of the row's 2 x max_splits), else one (slot split).
 constexpr int kDecTcMaxRows = 1024;
+bool decode_tc_applies(const PrefillArgs& a);
 int launch_decode_tc(const PrefillArgs& a, float* dec_out, float* dec_lse, int32_t max_splits,
-                     cudaStream_t stream);
+                     cudaStream_t stream, int grid = 0);
+// True when launch_decode takes the tensor-core kernel for these arguments (the
+// persistent kernel that PCP_ATTN_DECODE_SMS confines to a few SMs).
+bool decode_side_applies(const PrefillArgs& a);
 int launch_separate_merge(const PrefillArgs& a, cudaStream_t stream);
 int launch_cache_write(const void* k, const void* v, const int64_t* slot, int32_t num_tokens,
                        int32_t vec_per_tok, void* key_cache, void* value_cache, int64_t num_slots,

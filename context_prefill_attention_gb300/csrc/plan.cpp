@@ -6,6 +6,7 @@
 // a row's seq_len is its end position). Contiguous per-rank slices:
 // "Feat/pcp qwen36 hybrid", "Changes". Slot mapping and PAD masking: commit
 // "drop pcp_has_prefill" on the row-plan page.
+#include <cmath>
 #include <cstdint>
 #include <vector>
 
@@ -116,4 +117,55 @@ extern "C" int pcp_mask_slots_for_shard(const int64_t* slot_mapping, const int8_
     if (num_tokens > 0 && (!slot_mapping || !owner_shard || !out)) return PCP_ERR_ARG;
     for (int32_t t = 0; t < num_tokens; ++t) out[t] = owner_shard[t] == shard ? slot_mapping[t] : -1;
     return PCP_OK;
+}
+
+// SMs for the decode rows beside the prefill rows (PCP_ATTN_DECODE_SMS), from
+// the host row plan. Each side's SM time, at rates measured with this library's
+// kernels on GB300 (the ratio is what matters, so the clock cancels):
+//  * decode rows: their K and V bytes at what one SM of the tensor-core decode
+//    streams once HBM is not shared by every SM, plus a cost per work item
+//    (2048-key split x kv head);
+//  * prefill rows: per work item (128-token tile x head pair, or x head for an
+//    odd group) plus per 128-key tile it visits (end-aligned causal).
+// The SMs are split in proportion, rounding towards the decode side: a decode
+// that ends last costs the whole difference, a prefill that ends last only its
+// share of one SM.
+extern "C" int32_t pcp_decode_sms(const pcp_row_t* rows, int32_t num_rows, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t kv_cache_fp8, int32_t num_sms) {
+    if (!rows || num_rows <= 0 || num_rows > 1024 || num_sms < 2 || num_q_heads < 1 || num_kv_heads < 1 ||
+        num_q_heads % num_kv_heads != 0)
+        return 0;
+    const int32_t G = num_q_heads / num_kv_heads;
+    if (head_dim != 128 || G > 16 || kv_cache_fp8) return 0;
+    constexpr double kDecodeBytesPerSmS = 78.6e9;  // K/V bytes per second and SM
+    constexpr double kDecodeItemS = 1.0e-6;        // per split and kv head
+    constexpr double kPrefillItemS = 3.65e-6;      // per work item
+    constexpr double kPrefillTileS = 1.68e-6;      // per 128-key tile of a two-head item
+    constexpr double kPrefillTileOneHeadS = 1.0e-6;
+    constexpr int32_t kSplit = 2048, kTile = 128;
+    const bool dual = G % 2 == 0;
+    const double items_per_tile = dual ? num_q_heads / 2 : num_q_heads;
+    const double tile_s = dual ? kPrefillTileS : kPrefillTileOneHeadS;
+    double dec = 0.0, pre = 0.0;
+    for (int32_t i = 0; i < num_rows; ++i) {
+        const pcp_row_t& r = rows[i];
+        if (r.q_len < 1 || r.kv_end < r.q_len) continue;
+        if (r.is_decode) {
+            const double bytes = (double)r.kv_end * num_kv_heads * head_dim * 2.0 * 2.0;
+            const double items = (double)((r.kv_end + kSplit - 1) / kSplit) * num_kv_heads;
+            dec += bytes / kDecodeBytesPerSmS + items * kDecodeItemS;
+            continue;
+        }
+        for (int32_t t = 0; t * kTile < r.q_len; ++t) {
+            const int64_t last = (int64_t)r.kv_end - r.q_len + (r.q_len < (t + 1) * kTile ? r.q_len : (t + 1) * kTile);
+            const double key_tiles = (double)((last + kTile - 1) / kTile);
+            pre += items_per_tile * (kPrefillItemS + key_tiles * tile_s);
+        }
+    }
+    if (dec <= 0.0 || pre <= 0.0) return 0;
+    const double d = 1.05 * dec;
+    int32_t k = (int32_t)std::ceil(num_sms * d / (d + pre));
+    if (k < 1) k = 1;
+    if (2 * k >= num_sms) return 0;  // decode-heavy: HBM, not the SM count, bounds it
+    return k;
 }

@@ -7,7 +7,10 @@ A step ("Feat/pcp qwen36 hybrid", "Changes"; "[MRv2][PCP] Carry the row plan
 2. the plan (rows, slots) copied to the device from pinned staging buffers;
 3. ``pcp_kv_cache_write``: the new tokens' K/V into the paged cache, ordered
    before attention on the same stream;
-4. ``pcp_attn_varlen``: prefill, context and decode rows in one call.
+4. ``pcp_attn_varlen``: prefill, context and decode rows in one call. With
+   ``decode_beside_prefill=True`` (and a bf16 cache) the decode rows run on the
+   SMs ``pcp_decode_sms`` picks from the host plan, beside the prefill rows
+   (``PCP_ATTN_DECODE_SMS``): a shorter step, with each kernel on part of the GPU.
 
 With ``kv_cache_dtype="fp8"`` the cache holds e4m3 codes: step 3 is
 ``pcp_kv_cache_write_fp8`` with the layer's k/v scales and step 4
@@ -36,7 +39,7 @@ class PcpStep:
     def __init__(self, *, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
                  num_shards: int, split_mode: int, max_tokens: int, max_reqs: int, max_kv_len: int,
                  flags: int = 0, device: str = "cuda", kv_cache_dtype: str = "bf16", k_scale: float = 1.0,
-                 v_scale: float = 1.0):
+                 v_scale: float = 1.0, decode_beside_prefill: bool = False):
         if kv_cache_dtype not in ("bf16", "fp8"):
             raise ValueError(f"kv_cache_dtype {kv_cache_dtype!r}: 'bf16' or 'fp8'")
         self.kv_fp8 = kv_cache_dtype == "fp8"
@@ -44,6 +47,11 @@ class PcpStep:
         self.hq, self.hkv, self.d = num_q_heads, num_kv_heads, head_dim
         self.bs, self.shards, self.split_mode, self.flags = block_size, num_shards, split_mode, flags
         self.device = torch.device(device)
+        # decode rows beside the prefill rows, on request, unless the caller's flags
+        # already say how many SMs they take
+        self.decode_beside = decode_beside_prefill and (flags >> 16) & 0xFF == 0
+        self.num_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
+        self.decode_sms = 0
         self.max_rows = max(1, 2 * num_shards * max_reqs)
         self.max_tokens = max_tokens
         ws = L.pcp_attn_workspace_size(self.max_rows, max_tokens, num_q_heads, head_dim, max_kv_len, flags)
@@ -70,6 +78,8 @@ class PcpStep:
         (:func:`plan_summary`) goes to stderr."""
         self.plan = L.pcp_build_row_plan(query_len, num_computed, block_table_host, self.bs, self.shards,
                                          self.split_mode, rows_capacity=self.max_rows)
+        self.decode_sms = (L.pcp_decode_sms(self.plan["rows"], self.hq, self.hkv, self.d, self.kv_fp8,
+                                            self.num_sms) if self.decode_beside else 0)
         debug_plan(self.plan, self.shards)
         return self.plan
 
@@ -97,14 +107,15 @@ class PcpStep:
         n = int(self.plan["rows"].shape[0])
         out = self.out[:T]
         lse = self.lse_buf[:T * self.hq].view(self.hq, T)
+        flags = self.flags | L.PCP_ATTN_DECODE_SMS(self.decode_sms)
         if self.kv_fp8:
             R = int(block_table_dev.shape[0])
             return L.pcp_attn_varlen_fp8kv(q, key_cache, value_cache, self.k_descale[:R], self.v_descale[:R],
                                            block_table_dev, self.rows_dev[:n], scale, out=out, lse=lse,
-                                           workspace=self.workspace, flags=self.flags, status=self.status,
+                                           workspace=self.workspace, flags=flags, status=self.status,
                                            stream=stream)
         return L.pcp_attn_varlen(q, key_cache, value_cache, block_table_dev, self.rows_dev[:n], scale,
-                                 out=out, lse=lse, workspace=self.workspace, flags=self.flags,
+                                 out=out, lse=lse, workspace=self.workspace, flags=flags,
                                  status=self.status, stream=stream)
 
     def run(self, q, k_new, v_new, key_cache, value_cache, block_table_dev, scale: float, stream=None):

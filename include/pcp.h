@@ -83,6 +83,16 @@ typedef struct CUstream_st* pcp_stream_t; /* == cudaStream_t */
  * would each compute — and the partials are merged by LSE in the same call
  * (2 <= n <= 64; not combinable with PCP_ATTN_SEPARATE_CONTEXT). */
 #define PCP_ATTN_KV_SHARDS(n) (((n) & 0xFF) << 8)
+/* Decode rows beside the prefill: the decode rows run on n SMs on a stream of the
+ * library's own while the prefill rows take the other SMs, instead of one after
+ * the other on every SM (1 <= n < the SM count; pcp_decode_sms picks n). Used
+ * where the tensor-core decode applies (head_dim 128, a bf16 or FP8 cache, see
+ * pcp_attn_varlen); otherwise ignored. The prefill rows' results are the same bits
+ * either way; the decode rows' agree up to the rounding of their fp32 sums (the key
+ * tiles of a decode item are shared between two softmax warpgroups by a count that
+ * runs on across a CTA's items, so another split adds the same terms in another
+ * order). A given split gives the same bits on every run. */
+#define PCP_ATTN_DECODE_SMS(n) (((n) & 0xFF) << 16)
 
 /* One row of the plan: a contiguous run of one request's new tokens that one
  * shard evaluates. All fields are int32.
@@ -140,6 +150,27 @@ int pcp_build_row_plan(int32_t num_reqs, const int32_t* query_len, const int32_t
  */
 int pcp_mask_slots_for_shard(const int64_t* slot_mapping, const int8_t* owner_shard,
                              int32_t num_tokens, int32_t shard, int64_t* out);
+
+/*
+ * pcp_decode_sms — host function, pure. The SMs to give the decode rows of a
+ * row plan (rows, num_rows in host memory, as pcp_build_row_plan wrote them)
+ * when they run beside its prefill rows (PCP_ATTN_DECODE_SMS), or 0 to run them
+ * one after the other. Mixed prefill + decode batches are the pages' case
+ * ("[MRv2] FlashAttention PCP support for GQA on MRv2", overview); the split is
+ * this library's. On a few SMs the decode rows are no longer held to the
+ * SMs' share of HBM bandwidth, so they take less SM time than on all of them.
+ * The function balances that time (K and V bytes of the decode rows at a
+ * per-SM rate) against the prefill rows' (per work item and per 128-key tile
+ * at the measured rates of this library's kernels), rounding towards the
+ * decode side. It returns 0 when either side is empty, when the decode rows
+ * would need half the SMs or more, when the tensor-core decode does not apply
+ * (head_dim != 128, Hq / Hkv > 16, more than 1024 rows), and for an FP8 cache
+ * (kv_cache_fp8 != 0: its decode is bound by widening V on few SMs; measured no
+ * gain). num_sms: the SM count of the device (>= 2). Errors: none (bad
+ * arguments return 0).
+ */
+int32_t pcp_decode_sms(const pcp_row_t* rows, int32_t num_rows, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t kv_cache_fp8, int32_t num_sms);
 
 /*
  * pcp_kv_cache_write — device. Scatter the new tokens' K and V into the paged
@@ -201,6 +232,12 @@ size_t pcp_attn_workspace_size(int32_t num_rows, int32_t total_q, int32_t num_q_
  * PCP_ATTN_KV_SHARDS(n) computes n partials over n contiguous key shards and
  * merges them (decode rows are always split-KV internally; flags do not change
  * their result). Every mode gives the same attention up to rounding.
+ * PCP_ATTN_DECODE_SMS(n) runs the decode rows on n SMs beside the prefill rows,
+ * on an internal stream forked from `stream` after the row checks and joined
+ * back into `stream` before the call returns (a capture of `stream` takes both;
+ * the first such call in a CUDA context creates the internal stream and its two
+ * events, so make it before any stream capture). Calls from several host
+ * threads take turns on that stream.
  * Numerics: scores, softmax and sums in fp32, P rounded to bf16 for the
  * P V product; the result is finite whenever every scale * q . k is finite in
  * fp32 and ceil(keys / 128) * max |v| < 2^64, e.g. |v| < 2^54 at 131072 keys

@@ -52,11 +52,12 @@ class Case:
 
     ``kv_fp8=True`` runs the FP8 cache path; ``descales="layer"`` uses the layer
     scales broadcast to (num_reqs, Hkv), ``descales="varied"`` a seeded
-    different descale per (request, kv head). ``inputs_hook(case)`` may modify
+    different descale per (request, kv head); ``decode_beside=True`` lets the
+    step run the decode rows beside the prefill rows where it picks a split. ``inputs_hook(case)`` may modify
     ``case.q``, ``case.kfull``, ``case.vfull`` before anything is written."""
 
     def __init__(self, spec: W.WorkloadSpec, flags: int = 0, device: str = "cuda", kv_fp8: bool = False,
-                 descales: str = "layer", inputs_hook=None):
+                 descales: str = "layer", inputs_hook=None, decode_beside: bool = False):
         P = _pcp()
         self.spec, self.flags, self.device, self.kv_fp8 = spec, flags, device, kv_fp8
         self.bt, self.num_blocks = W.block_tables(spec)
@@ -89,7 +90,7 @@ class Case:
                               split_mode=spec.split_mode, max_tokens=spec.total_q, max_reqs=spec.num_reqs,
                               max_kv_len=max_kv, flags=flags, device=device,
                               kv_cache_dtype="fp8" if kv_fp8 else "bf16", k_scale=FP8_K_SCALE,
-                              v_scale=FP8_V_SCALE)
+                              v_scale=FP8_V_SCALE, decode_beside_prefill=decode_beside)
         self.k_descale = self.v_descale = None
         if kv_fp8:
             R = spec.num_reqs

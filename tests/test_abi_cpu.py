@@ -132,6 +132,10 @@ def test_attn_varlen_validates_before_launch(P):
     assert _attn(lib, flags=P.PCP_ATTN_KV_SHARDS(1)) == P.PCP_ERR_ARG
     assert _attn(lib, flags=P.PCP_ATTN_KV_SHARDS(65)) == P.PCP_ERR_ARG
     assert _attn(lib, flags=P.PCP_ATTN_SEPARATE_CONTEXT | P.PCP_ATTN_KV_SHARDS(2)) == P.PCP_ERR_ARG
+    assert _attn(lib, flags=1 << 24) == P.PCP_ERR_ARG
+    assert _attn(lib, nrows=0, flags=P.PCP_ATTN_DECODE_SMS(18)) == P.PCP_OK
+    assert P.pcp_attn_workspace_size(2, 100, 8, 128, 64, P.PCP_ATTN_DECODE_SMS(18)) == \
+        P.pcp_attn_workspace_size(2, 100, 8, 128, 64, 0)
     assert P.pcp_attn_workspace_size(2, 100, 8, 128, 64, P.PCP_ATTN_KV_SHARDS(4)) > \
         P.pcp_attn_workspace_size(2, 100, 8, 128, 64, P.PCP_ATTN_KV_SHARDS(2))
     assert _attn(lib, q=FAKE + 8) == P.PCP_ERR_ALIGN
@@ -410,3 +414,56 @@ def test_binding_marshals_consistent_tensors_and_checks_every_argument(P, monkey
     for args in ((oa, la, ob[:5], lb), (oa, la.t(), ob, lb), (oa, la, ob, lb.double()), (oa.bfloat16(), la, ob, lb)):
         with pytest.raises((TypeError, ValueError)):
             P.pcp_lse_merge(*args, stream=0)
+
+
+def _plan_rows(P, spec):
+    bt, _ = W.block_tables(spec)
+    return P.pcp_build_row_plan(spec.query_len, spec.num_computed, bt, spec.block_size, spec.num_shards,
+                                spec.split_mode)["rows"]
+
+
+def test_decode_sms_on_the_mixed_workload(P):
+    """The mixed benchmark batch (8 prompts + 56 decode rows, 32 q / 8 kv heads)
+    on 152 SMs: measured on GB300, 18 decode SMs gave the shortest step (20:
+    1 % longer, 16: 12 % longer); the function may round up, not down."""
+    rows = _plan_rows(P, W.workload_spec(4))
+    k = P.pcp_decode_sms(rows, 32, 8, 128, False, 152)
+    assert 18 <= k <= 20, k
+
+
+def test_decode_sms_hand_worked():
+    """One prefill row of 128 tokens without context (one 128-key tile, 4 two-head
+    items at 8 q / 2 kv heads: 4 x (3.65 + 1.68) us = 21.32 us of SM time) and one
+    decode row of 256 keys (256 x 2 kv heads x 128 dims x 2 bytes x 2 (K, V) =
+    262144 bytes at 78.6 GB/s = 3.335 us, plus 2 items x 1 us = 5.335 us).
+    Decode side rounded up by 5 %: 5.602 us; ceil(152 x 5.602 / 26.92) = 32."""
+    import context_prefill_attention_gb300 as P
+    P.load()
+    rows = np.array([[0, 0, 0, 128, 0, 128, 0, 0],
+                     [1, 0, 128, 1, 255, 256, 0, 1]], dtype=np.int32)
+    assert P.pcp_decode_sms(rows, 8, 2, 128, False, 152) == 32
+
+
+def test_decode_sms_zero_cases(P):
+    """0 (decode rows in sequence) whenever the split does not apply."""
+    mixed = _plan_rows(P, W.workload_spec(4))
+    assert P.pcp_decode_sms(_plan_rows(P, W.workload_spec(2)), 16, 8, 128, False, 152) == 0  # no decode rows
+    decode_only = mixed[mixed[:, 7] == 1]
+    assert len(decode_only) == 56 and P.pcp_decode_sms(decode_only, 32, 8, 128, False, 152) == 0
+    assert P.pcp_decode_sms(mixed, 32, 8, 128, True, 152) == 0     # FP8 cache
+    assert P.pcp_decode_sms(mixed, 32, 8, 64, False, 152) == 0     # head_dim 64: CUDA-core decode
+    assert P.pcp_decode_sms(mixed, 32, 1, 128, False, 152) == 0    # 32 q heads per kv head
+    assert P.pcp_decode_sms(mixed, 32, 8, 128, False, 1) == 0
+    assert P.pcp_decode_sms(mixed[:0], 32, 8, 128, False, 152) == 0
+    many = np.concatenate([mixed] * 20)                              # more rows than the kernel takes
+    assert len(many) > 1024 and P.pcp_decode_sms(many, 32, 8, 128, False, 152) == 0
+    # decode-heavy: one short prompt beside the 56 long decode rows needs half the SMs or more
+    short = np.concatenate([decode_only, [[0, 0, 0, 16, 0, 16, 0, 0]]]).astype(np.int32)
+    assert P.pcp_decode_sms(short, 32, 8, 128, False, 152) == 0
+
+
+def test_decode_sms_grows_with_decode_work(P):
+    mixed = _plan_rows(P, W.workload_spec(4))
+    prefill, decode = mixed[mixed[:, 7] == 0], mixed[mixed[:, 7] == 1]
+    ks = [P.pcp_decode_sms(np.concatenate([prefill, decode[:n]]), 32, 8, 128, False, 152) for n in (4, 14, 28, 56)]
+    assert all(a <= b for a, b in zip(ks, ks[1:])) and ks[0] >= 1 and ks[-1] > ks[0], ks

@@ -7,7 +7,8 @@ metadata", sections 1-2), the attention flags (fused, separate context pass,
 row-start split, n key shards merged by LSE), the cache type (bf16, or FP8
 codes with a different descale per request and kv head), and a mix of request
 kinds: decode rows (one new token over a cached context), short and long new
-token runs with or without a cached prefix, and requests with no new tokens.
+token runs with or without a cached prefix, and requests with no new tokens;
+every other case lets the step run its decode rows beside its prefill rows.
 Every token of every head is compared with the oracle at the fixed bounds
 (max |out - oracle| <= 1e-2, max |lse - oracle| <= 1e-3). The caches start out
 NaN-filled, so a read of a slot the step should not touch poisons the result.
@@ -80,7 +81,8 @@ def test_random_batch_matches_oracle(i):
     flags = P.PCP_ATTN_KV_SHARDS(c["n_kv"]) if c["flags"] is None else c["flags"]
     spec = W.custom_spec(c["q_len"], c["ctx"], num_q_heads=c["hq"], num_kv_heads=c["hkv"], head_dim=c["d"],
                          block_size=c["bs"], num_shards=c["shards"], split_mode=c["mode"], seed=c["seed"])
-    case = Case(spec, flags=flags, kv_fp8=c["kv_fp8"], descales="varied")
+    # odd cases let the step run decode rows beside the prefill rows where it picks a split
+    case = Case(spec, flags=flags, kv_fp8=c["kv_fp8"], descales="varied", decode_beside=bool(i % 2))
     out, lse = case.run()
     eo, el = case.compare(out, lse)
     assert eo <= OUT_TOL and el <= LSE_TOL, (c, eo, el)
