@@ -86,8 +86,9 @@ typedef struct CUstream_st* pcp_stream_t; /* == cudaStream_t */
 /* Decode rows beside the prefill: the decode rows run on n SMs on a stream of the
  * library's own while the prefill rows take the other SMs, instead of one after
  * the other on every SM (1 <= n < the SM count; pcp_decode_sms picks n). Used
- * where the tensor-core decode applies (head_dim 128, a bf16 or FP8 cache, see
- * pcp_attn_varlen); otherwise ignored. The prefill rows' results are the same bits
+ * where the tensor-core decode applies (head_dim 128, up to 16 q heads per kv head
+ * with a bf16 cache and 8 with an FP8 one, at most 1024 rows); with n = 0, n at or
+ * above the SM count, or another shape the rows run in sequence. The prefill rows' results are the same bits
  * either way; the decode rows' agree up to the rounding of their fp32 sums (the key
  * tiles of a decode item are shared between two softmax warpgroups by a count that
  * runs on across a CTA's items, so another split adds the same terms in another
