@@ -60,6 +60,8 @@ void* driver_entry(const char* name) {
 
 // The internal stream of PCP_ATTN_DECODE_SMS with its fork and join events, one
 // per CUDA context (streams and events belong to the context that made them).
+// Kept for the life of the process and never freed, so a pointer handed out
+// stays valid even if its table entry is later reused for another context.
 struct SideStream {
     cudaStream_t stream = nullptr;
     cudaEvent_t forked = nullptr, done = nullptr;
