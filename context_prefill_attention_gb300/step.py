@@ -49,7 +49,7 @@ class PcpStep:
         self.device = torch.device(device)
         # decode rows beside the prefill rows, on request, unless the caller's flags
         # already say how many SMs they take
-        self.decode_beside = decode_beside_prefill and (flags >> 16) & 0xFF == 0
+        self.decode_beside = decode_beside_prefill and ((flags >> 16) & 0xFF) == 0
         self.num_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
         self.decode_sms = 0
         self.max_rows = max(1, 2 * num_shards * max_reqs)
