@@ -289,8 +289,9 @@ __device__ __forceinline__ void widen_tile(uint8_t* tile, int nvalid, int ct) {
 // the remainder x - term is a multiple of x's last bit no larger than 8 of
 // them (x has 8 significant bits), so it is an e4m3 value too and the two
 // terms sum to x exactly, unless the remainder falls under e4m3's smallest
-// subnormal (2^-9 of the scaled unit: elements below 2^-10 of the head's
-// largest can lose bits, at most 2^-18 of it). qscale[h] = 2^(ex - 8) undoes
+// subnormal (2^-9 of the scaled unit, where the largest element lies in
+// [128, 256): only elements below 2^-9 of the head's largest can lose bits, at
+// most 2^-17 of it). qscale[h] = 2^(ex - 8) undoes
 // the scaling. Warp w of the converter set does heads w and w + 4, lane l dims
 // 4l .. 4l + 3. Returns whether an element of one of the G real heads lies
 // beyond +-65504 (reported as PCP_ERR_RANGE, as the prefill rows' q is).

@@ -248,8 +248,9 @@ __device__ __forceinline__ bool convert_q_f16(uint8_t* q_base, int bytes, int ct
 // bits), and the remainder, a multiple of x's last bit no larger than 8 of them
 // (x has bf16's 8 significant bits), is an e4m3 value too: the terms sum to x
 // exactly unless the remainder falls under e4m3's smallest subnormal (2^-9 of
-// the scaled unit; an element below 2^-10 of its row's largest can lose bits,
-// at most 2^-18 of that largest). Run by the row's own softmax thread, which
+// the scaled unit, where the largest element lies in [128, 256): only an element
+// below 2^-9 of its row's largest can lose bits, at most 2^-17 of that largest).
+// Run by the row's own softmax thread, which
 // reads the whole row before writing it. Returns 2^(ex - 8), the factor that
 // undoes the scaling; *over is set if an element lies beyond +-65504.
 __device__ __forceinline__ float q_row_to_e4m3(uint8_t* tile, int r, bool* over) {

@@ -318,9 +318,9 @@ int pcp_kv_cache_write_fp8(const void* k, const void* v, const int64_t* slot_map
  * same attention as pcp_attn_varlen over those keys and values. head_dim 128:
  * the scores take the K codes as e4m3 MMA operands against q written as two
  * e4m3 terms per element after a power-of-two scale per query row (prefill)
- * or per q head (decode rows); the terms sum to the bf16 q exactly except for
- * elements below 2^-10 of the row's largest, whose error is at most 2^-18 of
- * it. V is widened to f16 (exact) and the softmax weights P are f16 (decode
+ * or per q head (decode rows); the terms sum to the bf16 q exactly for every
+ * element of at least 2^-9 of the row's largest magnitude; a smaller element
+ * can lose bits, at most 2^-17 of that largest. V is widened to f16 (exact) and the softmax weights P are f16 (decode
  * rows with up to 8 q heads per kv head: two f16 parts; more: fp32). head_dim
  * 64: the prefill rows' products run in f16 (codes widened, q converted to f16,
  * P f16) and decode rows in fp32. An

@@ -69,6 +69,10 @@ def test_row_scaling_keeps_every_element_below_256():
         # below 2^-17 (2^-10 of the scaled unit over a row maximum of at least 128)
         rel = ((rec - q).abs() / m[:, None]).max()
         assert float(rel) <= 2.0 ** -17, float(rel)
+        # and every element of at least 2^-9 of its row's largest comes back exactly
+        # (scaled, it is at least 2^-9 x 128 = 2^-2, where the terms are exact)
+        big = q.abs() >= m[:, None] * 2.0 ** -9
+        assert torch.equal(rec[big], q[big])
 
 
 @pytest.mark.parametrize("v", [1.0, 1.9921875, 255.0, 0.25, 127.5])
